@@ -1,0 +1,486 @@
+"""Benchmark of the OAL hot path on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Step (default workload, Qwen2.5-0.5B-shaped prefill: B=1, Hq=14, Hkv=2,
+d=64, T=4096, G=4, bf16 inputs, packed fp32 states): coefficient expansion,
+chunked causal prefill of 4096 tokens, then one decode token continuing from
+the prefill state -- every step of the method in one pass.  Inputs are
+resident in HBM; L2 is flushed (256 MiB write) before every timed step and
+each step is timed with CUDA events on the launching stream.
+
+The JSON line also carries:
+  roofline      the dominant kernel's algorithmic FLOP/s (or bytes/s) against
+                the measured peak in MEASURED_PEAKS.json;
+  e2e           the same step through the C ABI with host buffers: pinned
+                host->device copies of the inputs and device->host copies of
+                the outputs inside the timed region;
+  decode        the decode workload (B=64, Hq=14, Hkv=2, full fp32 state of
+                4161 x 65 per KV head, 1024 steps after a 2048-token prefill):
+                steps/s and achieved HBM bandwidth;
+  cpu_baseline  the fp64 CPU oracle timed on a bounded sample of the same
+                workload on this host's cores (rank 0, N = 1 only);
+  clocks        SM clocks and throttle reasons sampled during the timed region.
+
+Under torchrun (N > 1) every rank runs its own copy of the workload on its
+own GPU (independent sequences, no data exchange): weak scaling, value =
+tokens of all ranks / max over ranks of the timed region.
+
+--impl reference times the fp64 CPU oracle (the only reference there is:
+the pages publish no code) on bounded samples of the same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "OAL prefill tokens/s & decode steps/s (1×GB300), % of tensor/HBM roofline"
+D = 64
+F_PACKED = 1 + D + D * (D + 1) // 2      # 2145
+F_FULL = 1 + D + D * D                   # 4161
+U = D + 1
+FP32_SIMT_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # CUDA-core fp32 FMA at 2070 MHz
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu_id)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxs.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs),
+                "samples": len(sms), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- CPU oracle leg
+def oracle_sample(w, target_s, seed=0, max_rows=None):
+    """Time the fp64 oracle on a stride sample of query rows; returns dict."""
+    import oracle
+    total_rows = w.B * w.Hq * w.T_prefill
+    probe = np.arange(0, total_rows, max(1, total_rows // 64))
+    t0 = time.perf_counter()
+    oracle.direct(w.Q[:, :, :w.T_prefill], w.K[:, :, :w.T_prefill], w.V[:, :, :w.T_prefill],
+                  w.L, w.group, w.eps, rows=probe)
+    per_row = (time.perf_counter() - t0) / probe.size
+    n = int(min(total_rows, max(probe.size, target_s / max(per_row, 1e-9))))
+    if max_rows:
+        n = min(n, max_rows)
+    rows = np.unique(np.linspace(0, total_rows - 1, n).astype(np.int64))
+    t0 = time.perf_counter()
+    oracle.direct(w.Q[:, :, :w.T_prefill], w.K[:, :, :w.T_prefill], w.V[:, :, :w.T_prefill],
+                  w.L, w.group, w.eps, rows=rows)
+    dt = time.perf_counter() - t0
+    tokens_per_s = rows.size / w.Hq / dt
+    return {"value": tokens_per_s, "unit": "tokens/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": "%d of %d query rows (uniform stride over batch x heads x tokens); "
+                      "tokens/s = rows / Hq / time" % (rows.size, total_rows)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from grouped_quadratic_gb300 import inputs
+    w = inputs.config(args.config, decode_steps=1, T=inputs.CONFIGS[args.config]["T"] + 1)
+    per_step = max(2.0, min(20.0, args.ref_seconds / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step)
+    vals, secs = [], 0.0
+    last = None
+    for _ in range(args.steps):
+        last = oracle_sample(w, per_step)
+        vals.append(last["value"])
+        secs += last["seconds"]
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * secs / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, args),
+            "cpu_baseline": {"kind": "oracle", "cores": last["cores"], "value": value,
+                             "unit": "tokens/s", "sample": last["sample"]},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, args):
+    return {"workload": "qwen2.5-0.5b-prefill+1-decode B%d Hq%d Hkv%d T%d+1 d64 G%d"
+                        % (w.B, w.Hq, w.Hkv, w.T_prefill, w.G),
+            "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T_prefill, "decode_tokens": 1,
+            "d": 64, "dv": 64, "G": w.G, "state_layout": args.layout, "chunk": args.chunk,
+            "l2": "flushed (256 MiB write) before every timed step",
+            "seed": w.seed}
+
+
+# ----------------------------------------------------------------- GPU legs
+def algorithmic_flops(B, Hq, Hkv, T, chunk):
+    """Per-kernel algorithmic FLOPs (packed state F_p = 2145)."""
+    readout = 2.0 * B * T * Hq * F_PACKED * U
+    intra = float(B) * T * Hq * chunk * (D + U)      # causal half of the C x C tile
+    update = 2.0 * B * T * Hkv * F_PACKED * U
+    return {"readout": readout + intra, "update": update, "total": readout + intra + update}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from grouped_quadratic_gb300 import build as gq_build
+    from grouped_quadratic_gb300 import inputs, oal
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (no CPU fallback)")
+    gq_build.build()
+    lib = oal.load_library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    layout = oal.OAL_STATE_PACKED if args.layout == "packed" else oal.OAL_STATE_FULL
+    cfg = inputs.CONFIGS[args.config]
+    w = inputs.config(args.config, T=cfg["T"] + 1, decode_steps=1)
+    Tp = w.T_prefill
+    chunk = args.chunk
+    Qh, Kh, Vh = w.torch_inputs("cpu")
+    Q = Qh[:, :, :Tp].contiguous().to(dev)
+    K = Kh[:, :, :Tp].contiguous().to(dev)
+    V = Vh[:, :, :Tp].contiguous().to(dev)
+    q1 = Qh[:, :, Tp].contiguous().to(dev)
+    k1 = Kh[:, :, Tp].contiguous().to(dev)
+    v1 = Vh[:, :, Tp].contiguous().to(dev)
+    L = torch.from_numpy(w.L).to(dev)
+    group = torch.from_numpy(w.group).to(dev)
+    dt = oal.OAL_BF16 if w.dtype == "bf16" else oal.OAL_F32
+    Hq, Hkv, B = w.Hq, w.Hkv, w.B
+    a = torch.empty(Hq, device=dev)
+    b = torch.empty(Hq, D, device=dev)
+    C = torch.empty(Hq, oal.oal_coeff_table_elems(D, layout), device=dev)
+    state = torch.empty(B, Hkv, oal.oal_state_rows(D, layout), U, device=dev)
+    Y = torch.empty(B, Hq, Tp, D, dtype=Q.dtype, device=dev)
+    y1 = torch.empty(B, Hq, D, dtype=Q.dtype, device=dev)
+    ws_p = torch.empty(max(256, oal.oal_prefill_workspace_bytes(B, Hq, Hkv, Tp, D, D, dt, layout,
+                                                                chunk)), dtype=torch.uint8, device=dev)
+    ws_d = torch.empty(max(256, oal.oal_decode_workspace_bytes(B, Hq, Hkv, D, D, layout)),
+                       dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        oal.oal_expand_coeffs(L, group, w.eps, layout, a, b, C, stream=stream)
+        oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, layout, state=state, Y=Y,
+                        chunk=chunk, workspace=ws_p, stream=stream)
+        oal.oal_decode_step(q1, k1, v1, a, b, C, state, layout, y=y1, workspace=ws_d,
+                            stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    oal.oal_sync_status()
+
+    # per-kernel events for the prefill call (timing hook of the C ABI)
+    n_ev = 8
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    for evs in kev:
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+    ev_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    import ctypes
+    ev_arrays = [(ctypes.c_void_p * n_ev)(*[e.cuda_event for e in evs]) for evs in kev]
+
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = lib.oal_launch_counter()
+    names = None
+    gpu_id = "GPU-%s" % torch.cuda.get_device_properties(dev).uuid
+    with ClockSampler(gpu_id) as clk:
+        for s in range(args.steps):
+            flush.zero_()
+            ev_start[s].record(stream)
+            oal.oal_expand_coeffs(L, group, w.eps, layout, a, b, C, stream=stream)
+            lib.oal_set_launch_events(ev_arrays[s], n_ev)
+            oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, layout, state=state, Y=Y,
+                            chunk=chunk, workspace=ws_p, stream=stream)
+            nk = lib.oal_last_call_launches()
+            names = [lib.oal_last_call_launch_name(i).decode() for i in range(nk)]
+            lib.oal_set_launch_events(None, 0)
+            oal.oal_decode_step(q1, k1, v1, a, b, C, state, layout, y=y1, workspace=ws_d,
+                                stream=stream)
+            ev_end[s].record(stream)
+        torch.cuda.synchronize()
+    launches = lib.oal_launch_counter() - launches0
+    barrier(world)
+    oal.oal_sync_status()
+    step_ms = [ev_start[s].elapsed_time(ev_end[s]) for s in range(args.steps)]
+    total_s = max_over_ranks(sum(step_ms) / 1000.0, world)
+    tokens_per_step = B * (Tp + 1)
+    value = tokens_per_step * world * args.steps / total_s
+
+    # per-kernel durations inside the prefill call
+    nk = len(names)
+    per_kernel = {}
+    for s in range(args.steps):
+        for k in range(min(nk, n_ev - 1)):
+            per_kernel.setdefault(names[k], []).append(kev[s][k].elapsed_time(kev[s][k + 1]))
+    pk = {k: statistics.mean(v) for k, v in per_kernel.items()}
+    dom = max(pk, key=pk.get)
+    pks = peaks()
+    fl = algorithmic_flops(B, Hq, Hkv, Tp, chunk if chunk else 64)
+    tensor = "tc" in dom or "umma" in dom
+    if dom.startswith("readout") or dom.startswith("tc_readout"):
+        work = fl["readout"]
+    elif "state" in dom or "delta" in dom:
+        work = fl["update"]
+    else:
+        work = fl["total"]
+    achieved = work / (pk[dom] / 1000.0) / 1e12
+    peak = pks["bf16_tflops"] if tensor else FP32_SIMT_PEAK_TFLOPS
+    roofline = {"bound": "tensor" if tensor else "alu", "kernel": dom,
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None,
+                "peak_source": ("measured bf16 burst (MEASURED_PEAKS.json)" if tensor else
+                                "fp32 CUDA-core FMA peak: 152 SMs x 128 lanes x 2 x 2.07 GHz"),
+                "kernel_ms": pk[dom],
+                "kernel_share": pk[dom] / statistics.mean(step_ms),
+                "per_kernel_ms": pk,
+                "algorithmic_flops_per_launch": work}
+
+    # e2e through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        Qp, Kp, Vp = (t[:, :, :Tp].contiguous().pin_memory() for t in (Qh, Kh, Vh))
+        q1p, k1p, v1p = (t[:, :, Tp].contiguous().pin_memory() for t in (Qh, Kh, Vh))
+        Lp = torch.from_numpy(w.L).pin_memory()
+        gp = torch.from_numpy(w.group).pin_memory()
+        Yp = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
+        y1p = torch.empty(y1.shape, dtype=y1.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (Qp, Kp, Vp, q1p, k1p, v1p, Lp, gp))
+        d2h = Yp.numel() * Yp.element_size() + y1p.numel() * y1p.element_size()
+
+        def e2e_step():
+            for dst, src in ((Q, Qp), (K, Kp), (V, Vp), (q1, q1p), (k1, k1p), (v1, v1p),
+                             (L, Lp), (group, gp)):
+                dst.copy_(src, non_blocking=True)
+            step()
+            Yp.copy_(Y, non_blocking=True)
+            y1p.copy_(y1, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier(world)
+        for s in range(args.steps):
+            flush.zero_()
+            es[s].record(stream)
+            e2e_step()
+            ee[s].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_s = max_over_ranks(sum(es[s].elapsed_time(ee[s]) for s in range(args.steps)) / 1e3,
+                               world)
+        e2e = {"value": tokens_per_step * world * args.steps / e2e_s, "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": 1e3 * e2e_s / args.steps}
+
+    decode = None if args.no_decode else run_decode(args, world, dev, stream, lib, pks)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample(w, args.cpu_seconds)
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": workload_config(w, args), "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": e2e, "gpu_launches": int(launches), "clocks": clk.summary(),
+            "decode": decode, "peaks_source": pks["source"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_decode(args, world, dev, stream, lib, pks):
+    """Decode workload: B=64, Hq=14, Hkv=2, 2048-token prefill then decode steps."""
+    import torch
+    from grouped_quadratic_gb300 import inputs, oal
+    n_steps = args.decode_steps
+    w = inputs.config(3, T=2048 + n_steps, decode_steps=n_steps)
+    layout = oal.OAL_STATE_FULL if args.decode_layout == "full" else oal.OAL_STATE_PACKED
+    Tp = w.T_prefill
+    Qh, Kh, Vh = w.torch_inputs("cpu")
+    Q = Qh[:, :, :Tp].contiguous().to(dev)
+    K = Kh[:, :, :Tp].contiguous().to(dev)
+    V = Vh[:, :, :Tp].contiguous().to(dev)
+    qd = Qh[:, :, Tp:].permute(2, 0, 1, 3).contiguous().to(dev)   # [steps, B, Hq, 64]
+    kd = Kh[:, :, Tp:].permute(2, 0, 1, 3).contiguous().to(dev)
+    vd = Vh[:, :, Tp:].permute(2, 0, 1, 3).contiguous().to(dev)
+    L = torch.from_numpy(w.L).to(dev)
+    group = torch.from_numpy(w.group).to(dev)
+    a, b, C = oal.oal_expand_coeffs(L, group, w.eps, layout)
+    _, state = oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, layout)
+    del Q, K, V
+    y = torch.empty(n_steps, w.B, w.Hq, D, dtype=qd.dtype, device=dev)
+    ws = torch.empty(oal.oal_decode_workspace_bytes(w.B, w.Hq, w.Hkv, D, D, layout),
+                     dtype=torch.uint8, device=dev)
+    for t in range(min(3, n_steps)):     # warm-up on a copy of the state
+        s2 = state.clone()
+        oal.oal_decode_step(qd[t], kd[t], vd[t], a, b, C, s2, layout, y=y[t], workspace=ws)
+    del s2
+    oal.oal_sync_status()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    c0 = lib.oal_launch_counter()
+    e0.record(stream)
+    for t in range(n_steps):
+        oal.oal_decode_step(qd[t], kd[t], vd[t], a, b, C, state, layout, y=y[t], workspace=ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = lib.oal_launch_counter() - c0
+    oal.oal_sync_status()
+    secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    F = F_FULL if layout == oal.OAL_STATE_FULL else F_PACKED
+    state_bytes = w.B * w.Hkv * F * U * 4
+    io_bytes = (w.B * w.Hq * D * 2 + 2 * w.B * w.Hkv * D) * qd.element_size()
+    bytes_per_step = 2 * state_bytes + io_bytes
+    gbs = bytes_per_step * n_steps / secs / 1e9
+    return {"workload": "qwen2.5-0.5b-decode B%d Hq%d Hkv%d prefill %d then %d steps, %s state"
+                        % (w.B, w.Hq, w.Hkv, Tp, n_steps, args.decode_layout),
+            "steps_per_s": world * n_steps / secs, "ms_per_step": 1e3 * secs / n_steps,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pks["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / pks["hbm_gbs"], "traffic": None,
+                         "algorithmic_bytes_per_step": bytes_per_step},
+            "gpu_launches": int(launches), "l2": "state set %.0f MB vs 129 MB L2" % (
+                state_bytes / 1e6)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 4])
+    ap.add_argument("--layout", choices=["packed", "full"], default="packed")
+    ap.add_argument("--chunk", type=int, default=0)
+    ap.add_argument("--decode-steps", type=int, default=1024)
+    ap.add_argument("--decode-layout", choices=["packed", "full"], default="full")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

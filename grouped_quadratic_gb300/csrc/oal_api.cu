@@ -1,0 +1,300 @@
+// oal_api.cu -- the extern "C" entry points of liboal.so (include/oal.h):
+// argument validation, workspace sizing, dispatch to the kernels, error
+// reporting.  No allocation happens here; all memory is the caller's.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "oal_internal.cuh"
+
+namespace oal {
+oal_status launch_expand_coeffs(const float *L, const int32_t *group, int Hq, int G,
+                                float eps, int packed, float *a, float *b, float *C,
+                                cudaStream_t stream);
+size_t simt_prefill_workspace_bytes(int B, int Hkv, int T, int packed, int chunk);
+oal_status launch_prefill_simt(const void *Q, const void *K, const void *V, int is_bf16,
+                               int B, int Hq, int Hkv, int T, const float *L,
+                               const int32_t *group, int G, float eps, const float *a,
+                               const float *b, const float *C, int packed, float *state,
+                               int cont, void *Y, int chunk, void *ws, cudaStream_t stream);
+size_t decode_workspace_bytes(int B, int Hkv, int packed);
+int decode_max_rho();
+oal_status launch_decode(const void *q, const void *k, const void *v, int is_bf16, int B,
+                         int Hq, int Hkv, const float *a, const float *b, const float *C,
+                         int packed, float *state, void *y, void *ws, cudaStream_t stream);
+
+// Device status word (one per device the library runs on).
+__device__ int g_status_word;
+}  // namespace oal
+
+static thread_local char t_msg[512] = "";
+
+oal_status oal_fail(oal_status st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_msg, sizeof t_msg, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+oal_status oal_check_launch(const char *what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return oal_fail(OAL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return OAL_OK;
+}
+
+// ---- launch accounting and the timing hook
+#include <atomic>
+static std::atomic<unsigned long long> g_launches{0};
+static thread_local cudaEvent_t *t_events = nullptr;
+static thread_local int t_nevents = 0;
+static thread_local int t_call_launches = 0;
+static thread_local const char *t_call_names[32];
+
+void oal_begin_call(cudaStream_t stream) {
+  t_call_launches = 0;
+  if (t_events && t_nevents > 0) cudaEventRecord(t_events[0], stream);
+}
+
+oal_status oal_after_launch(const char *name, cudaStream_t stream) {
+  const oal_status st = oal_check_launch(name);
+  if (st != OAL_OK) return st;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  const int k = ++t_call_launches;
+  if (k <= 32) t_call_names[k - 1] = name;
+  if (t_events && k < t_nevents) cudaEventRecord(t_events[k], stream);
+  return OAL_OK;
+}
+
+int *oal_device_status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  static int *addr[64] = {nullptr};
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, oal::g_status_word) != cudaSuccess) return nullptr;
+    addr[dev] = (int *)p;
+  }
+  return addr[dev];
+}
+
+namespace {
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+oal_status check_ptr(const void *p, const char *name) {
+  if (!p) return oal_fail(OAL_ERR_INVALID_ARG, "%s is null", name);
+  if (!aligned16(p)) return oal_fail(OAL_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return OAL_OK;
+}
+
+oal_status check_common(int B, int Hq, int Hkv, int d, int dv, oal_dtype dtype,
+                        oal_state_layout layout) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0)
+    return oal_fail(OAL_ERR_INVALID_ARG, "bad sizes B=%d Hq=%d Hkv=%d", B, Hq, Hkv);
+  if (Hq % Hkv != 0)
+    return oal_fail(OAL_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  if (dtype != OAL_F32 && dtype != OAL_BF16)
+    return oal_fail(OAL_ERR_INVALID_ARG, "bad dtype %d", (int)dtype);
+  if (layout != OAL_STATE_FULL && layout != OAL_STATE_PACKED)
+    return oal_fail(OAL_ERR_INVALID_ARG, "bad state layout %d", (int)layout);
+  if (d != oal::kD || dv != oal::kDv)
+    return oal_fail(OAL_ERR_UNSUPPORTED, "only d = dv = 64 is supported (d=%d dv=%d)", d, dv);
+  return OAL_OK;
+}
+
+#define OAL_TRY(x)                        \
+  do {                                    \
+    const oal_status _s = (x);            \
+    if (_s != OAL_OK) return _s;          \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char *oal_version(void) { return "0.1.0"; }
+
+uint64_t oal_launch_counter(void) { return g_launches.load(std::memory_order_relaxed); }
+
+oal_status oal_set_launch_events(cudaEvent_t *events, int n) {
+  if (n < 0) return oal_fail(OAL_ERR_INVALID_ARG, "n=%d", n);
+  t_events = (events && n > 0) ? events : nullptr;
+  t_nevents = t_events ? n : 0;
+  return OAL_OK;
+}
+
+int oal_last_call_launches(void) { return t_call_launches; }
+
+const char *oal_last_call_launch_name(int k) {
+  if (k < 0 || k >= t_call_launches || k >= 32) return "";
+  return t_call_names[k];
+}
+
+const char *oal_last_error(void) { return t_msg; }
+
+size_t oal_state_rows(int d, oal_state_layout layout) {
+  if (d <= 0) return 0;
+  const size_t dd = (size_t)d;
+  if (layout == OAL_STATE_FULL) return 1 + dd + dd * dd;
+  if (layout == OAL_STATE_PACKED) return 1 + dd + dd * (dd + 1) / 2;
+  return 0;
+}
+
+size_t oal_state_elems(int d, int dv, oal_state_layout layout) {
+  if (dv <= 0) return 0;
+  return oal_state_rows(d, layout) * (size_t)(dv + 1);
+}
+
+size_t oal_coeff_table_elems(int d, oal_state_layout layout) {
+  if (d <= 0) return 0;
+  if (layout == OAL_STATE_FULL) return (size_t)d * d;
+  if (layout == OAL_STATE_PACKED) return (size_t)d * (d + 1) / 2;
+  return 0;
+}
+
+oal_status oal_expand_coeffs(const float *L, const int32_t *group, int Hq, int G, int d,
+                             float eps, oal_state_layout layout, float *a, float *b,
+                             float *C, cudaStream_t stream) {
+  t_msg[0] = 0;
+  if (Hq <= 0) return oal_fail(OAL_ERR_INVALID_ARG, "Hq=%d", Hq);
+  if (layout != OAL_STATE_FULL && layout != OAL_STATE_PACKED)
+    return oal_fail(OAL_ERR_INVALID_ARG, "bad state layout %d", (int)layout);
+  if (d != oal::kD) return oal_fail(OAL_ERR_UNSUPPORTED, "only d = 64 is supported (d=%d)", d);
+  if (G < 1 || G > oal::kMaxG)
+    return oal_fail(OAL_ERR_UNSUPPORTED, "G=%d outside 1..%d", G, oal::kMaxG);
+  if (!(eps > 0.f)) return oal_fail(OAL_ERR_INVALID_ARG, "eps must be > 0 (got %g)", eps);
+  OAL_TRY(check_ptr(L, "L"));
+  OAL_TRY(check_ptr(group, "group"));
+  OAL_TRY(check_ptr(a, "a"));
+  OAL_TRY(check_ptr(b, "b"));
+  OAL_TRY(check_ptr(C, "C"));
+  oal_begin_call(stream);
+  return oal::launch_expand_coeffs(L, group, Hq, G, eps, layout == OAL_STATE_PACKED, a, b,
+                                   C, stream);
+}
+
+static int default_chunk(oal_dtype dtype) { return dtype == OAL_BF16 ? 64 : 64; }
+
+size_t oal_prefill_workspace_bytes(int B, int Hq, int Hkv, int T, int d, int dv,
+                                   oal_dtype dtype, oal_state_layout layout, int chunk) {
+  if (check_common(B, Hq, Hkv, d, dv, dtype, layout) != OAL_OK || T < 0) return 0;
+  if (chunk == 0) chunk = default_chunk(dtype);
+  if (chunk != 64 && chunk != 128 && chunk != 256) return 0;
+  if (T == 0 || B == 0) return 256;
+  return oal::simt_prefill_workspace_bytes(B, Hkv, T, layout == OAL_STATE_PACKED, chunk);
+}
+
+oal_status oal_prefill(const void *Q, const void *K, const void *V, oal_dtype dtype, int B,
+                       int Hq, int Hkv, int T, int d, int dv, const float *L,
+                       const int32_t *group, int G, float eps, const float *a,
+                       const float *b, const float *C, oal_state_layout layout,
+                       float *state, int continue_from_state, void *Y, int chunk,
+                       void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  t_msg[0] = 0;
+  OAL_TRY(check_common(B, Hq, Hkv, d, dv, dtype, layout));
+  if (T < 0) return oal_fail(OAL_ERR_INVALID_ARG, "T=%d", T);
+  if (G < 1 || G > oal::kMaxG)
+    return oal_fail(OAL_ERR_UNSUPPORTED, "G=%d outside 1..%d", G, oal::kMaxG);
+  if (!(eps > 0.f)) return oal_fail(OAL_ERR_INVALID_ARG, "eps must be > 0 (got %g)", eps);
+  if (chunk == 0) chunk = default_chunk(dtype);
+  if (chunk != 64 && chunk != 128 && chunk != 256)
+    return oal_fail(OAL_ERR_INVALID_ARG, "chunk=%d (allowed: 0, 64, 128, 256)", chunk);
+  t_call_launches = 0;
+  if (B == 0) return OAL_OK;
+  OAL_TRY(check_ptr(state, "state"));
+  const int packed = layout == OAL_STATE_PACKED;
+  if (T == 0) {
+    if (!continue_from_state) {
+      const size_t bytes = (size_t)B * Hkv * oal_state_elems(d, dv, layout) * sizeof(float);
+      if (cudaMemsetAsync(state, 0, bytes, stream) != cudaSuccess)
+        return oal_check_launch("state reset");
+    }
+    return OAL_OK;
+  }
+  OAL_TRY(check_ptr(Q, "Q"));
+  OAL_TRY(check_ptr(K, "K"));
+  OAL_TRY(check_ptr(V, "V"));
+  OAL_TRY(check_ptr(Y, "Y"));
+  OAL_TRY(check_ptr(L, "L"));
+  OAL_TRY(check_ptr(group, "group"));
+  OAL_TRY(check_ptr(a, "a"));
+  OAL_TRY(check_ptr(b, "b"));
+  OAL_TRY(check_ptr(C, "C"));
+  OAL_TRY(check_ptr(workspace, "workspace"));
+  if (((uintptr_t)workspace & 255u) != 0)
+    return oal_fail(OAL_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  const size_t need =
+      oal_prefill_workspace_bytes(B, Hq, Hkv, T, d, dv, dtype, layout, chunk);
+  if (workspace_bytes < need)
+    return oal_fail(OAL_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes",
+                    workspace_bytes, need);
+  if ((long long)T * Hq * B > (1LL << 40))
+    return oal_fail(OAL_ERR_UNSUPPORTED, "problem too large");
+  oal_begin_call(stream);
+  return oal::launch_prefill_simt(Q, K, V, dtype == OAL_BF16, B, Hq, Hkv, T, L, group, G,
+                                  eps, a, b, C, packed, state, continue_from_state != 0,
+                                  Y, chunk, workspace, stream);
+}
+
+size_t oal_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int dv,
+                                  oal_state_layout layout) {
+  if (check_common(B, Hq, Hkv, d, dv, OAL_F32, layout) != OAL_OK) return 0;
+  if (B == 0) return 256;
+  return oal::decode_workspace_bytes(B, Hkv, layout == OAL_STATE_PACKED);
+}
+
+oal_status oal_decode_step(const void *q, const void *k, const void *v, oal_dtype dtype,
+                           int B, int Hq, int Hkv, int d, int dv, const float *a,
+                           const float *b, const float *C, oal_state_layout layout,
+                           float *state, void *y, void *workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  t_msg[0] = 0;
+  OAL_TRY(check_common(B, Hq, Hkv, d, dv, dtype, layout));
+  if (Hq / Hkv > oal::decode_max_rho())
+    return oal_fail(OAL_ERR_UNSUPPORTED, "Hq/Hkv=%d exceeds %d", Hq / Hkv,
+                    oal::decode_max_rho());
+  if (B == 0) return OAL_OK;
+  OAL_TRY(check_ptr(q, "q"));
+  OAL_TRY(check_ptr(k, "k"));
+  OAL_TRY(check_ptr(v, "v"));
+  OAL_TRY(check_ptr(y, "y"));
+  OAL_TRY(check_ptr(a, "a"));
+  OAL_TRY(check_ptr(b, "b"));
+  OAL_TRY(check_ptr(C, "C"));
+  OAL_TRY(check_ptr(state, "state"));
+  OAL_TRY(check_ptr(workspace, "workspace"));
+  if (((uintptr_t)workspace & 255u) != 0)
+    return oal_fail(OAL_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  const size_t need = oal_decode_workspace_bytes(B, Hq, Hkv, d, dv, layout);
+  if (workspace_bytes < need)
+    return oal_fail(OAL_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes",
+                    workspace_bytes, need);
+  oal_begin_call(stream);
+  return oal::launch_decode(q, k, v, dtype == OAL_BF16, B, Hq, Hkv, a, b, C,
+                            layout == OAL_STATE_PACKED, state, y, workspace, stream);
+}
+
+oal_status oal_sync_status(cudaStream_t stream) {
+  t_msg[0] = 0;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess)
+    return oal_fail(OAL_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  int *w = oal_device_status_word();
+  if (!w) return oal_fail(OAL_ERR_CUDA, "status word unavailable");
+  int v = 0;
+  e = cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return oal_fail(OAL_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (v != 0) {
+    const int zero = 0;
+    cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    const char *what = v == OAL_ERR_INVALID_ARG ? "a group id was outside 1..G"
+                       : v == OAL_ERR_TIMEOUT   ? "a device-side wait timed out"
+                                                : "device error";
+    return oal_fail((oal_status)v, "device status %d: %s", v, what);
+  }
+  return OAL_OK;
+}
+
+}  // extern "C"

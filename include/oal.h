@@ -1,0 +1,185 @@
+/*
+ * oal.h -- C ABI of liboal.so: OAL causal attention on one GB300 (sm_103a).
+ *
+ * Method: "Not All Dimensions Are Equal: Outlier-Aware Attention
+ * Linearization with Grouped Quadratic Kernels" (arXiv:2610.13674), cited as
+ * [OAL].  With x_r = q_r k_r / sqrt(d), group sums s_g = sum_{r in G_g} x_r
+ * and s_bar = [1, s_1..s_G], the kernel is
+ *     kappa(q,k) = eps + s_bar^T L L^T s_bar                  [OAL] Eq. (7)
+ * and the output is the normalised inclusive causal average
+ *     y_i = sum_{j<=i} kappa(q_i,k_j) v_j / sum_{j<=i} kappa(q_i,k_j),
+ * evaluated in linear time through the prefix states of Eq. (5),
+ *     H0 = sum u_j,  H1_r = sum k_{j,r} u_j,  H2_rt = sum k_{j,r} k_{j,t} u_j,
+ *     u_j = [v_j; 1],
+ * and the readout of Eq. (6),
+ *     u~_i = a H0 + (1/sqrt d) sum_r b_r q_r H1_r + (1/d) sum_rt C_rt q_r q_t H2_rt,
+ *     y_i  = u~_i[0:dv] / u~_i[dv].
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller, contiguous
+ *    in the stated row-major layout, and 16-byte aligned.  The library keeps
+ *    no allocation between calls; scratch memory is passed in `workspace`.
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream).
+ *    Argument errors are detected on the host and returned synchronously,
+ *    with nothing launched.  Errors found on the device (a group id out of
+ *    range, a bounded wait that gave up) are recorded in a per-process device
+ *    status word and returned by the next oal_sync_status().
+ *  - Grouped-query attention: query head h reads key/value head
+ *    h / (Hq / Hkv); Hq must be a multiple of Hkv.  L and the group map are
+ *    per query head; the state is per (batch, key/value head).
+ *  - Supported sizes: d == dv == 64, 1 <= G <= 7.  Other values return
+ *    OAL_ERR_UNSUPPORTED.
+ *  - On error, oal_last_error() returns a message for the calling thread.
+ */
+#ifndef OAL_H
+#define OAL_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  OAL_OK = 0,
+  OAL_ERR_INVALID_ARG = 1, /* null/unaligned pointer, bad size, bad enum */
+  OAL_ERR_UNSUPPORTED = 2, /* valid but outside the supported sizes      */
+  OAL_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed       */
+  OAL_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up         */
+} oal_status;
+
+typedef enum { OAL_F32 = 0, OAL_BF16 = 1 } oal_dtype;
+
+/*
+ * State layouts ([OAL] Eq. (5); App. D "Exact state and parameter counts").
+ * The state of one (batch, KV head) is F rows of dv+1 fp32 values
+ * (the last value of a row belongs to the "1" of u = [v; 1]):
+ *   row 0                 H0
+ *   rows 1 .. d           H1_r,            r = row - 1
+ *   FULL   (F = 1+d+d*d):        row 1+d + r*d + t            holds H2_rt
+ *   PACKED (F = 1+d+d(d+1)/2):   row 1+d + r*d - r(r-1)/2 + (t-r) holds H2_rt,
+ *                                r <= t (H2 is symmetric; App. D)
+ * For d = dv = 64: FULL is 4161 x 65 fp32 (1,081,860 B), PACKED 2145 x 65
+ * (557,700 B) per (batch, KV head).
+ */
+typedef enum { OAL_STATE_FULL = 0, OAL_STATE_PACKED = 1 } oal_state_layout;
+
+/* Rows F of one state, and F*(dv+1), for the layout; 0 for a bad layout. */
+size_t oal_state_rows(int d, oal_state_layout layout);
+size_t oal_state_elems(int d, int dv, oal_state_layout layout);
+/* Entries of one head's C table: d*d (FULL) or d(d+1)/2 (PACKED). */
+size_t oal_coeff_table_elems(int d, oal_state_layout layout);
+
+/*
+ * oal_expand_coeffs -- coefficient map of [OAL] Sec. 4.3 ("Positive
+ * group-aware kernel"), Algorithm 1 line 5:  M = L L^T,
+ *     a = eps + M_00,  b_r = 2 M_{0,g(r)},  C_rt = M_{g(r),g(t)}.
+ *  L      [Hq][G+1][G+1] fp32, row-major; only the lower triangle is read.
+ *  group  [Hq][d] int32, the group of each dimension, values 1..G.
+ *  a [Hq], b [Hq][d] fp32.
+ *  C [Hq][d*d] (FULL: C_rt at r*d+t) or [Hq][d(d+1)/2] (PACKED: the
+ *    readout weight of pair r <= t at r*d - r(r-1)/2 + (t-r), which is
+ *    C_rt on the diagonal and 2*C_rt off it -- App. D's multiplicity).
+ * Rounding (the pages fix none): M_gh = sum_{c=0}^{min(g,h)} L[g][c]*L[h][c]
+ * in fp64 with c ascending, then a = fp32(fp64(eps) + M_00),
+ * b_r = fp32(2 M), C = fp32(M) or fp32(2 M), round to nearest even.  The
+ * tables are therefore reproducible bit for bit.
+ * A group id outside 1..G is reported by oal_sync_status() as
+ * OAL_ERR_INVALID_ARG (the tables are then unspecified).
+ */
+oal_status oal_expand_coeffs(const float *L, const int32_t *group, int Hq,
+                             int G, int d, float eps, oal_state_layout layout,
+                             float *a, float *b, float *C, cudaStream_t stream);
+
+/*
+ * oal_prefill -- causal OAL attention over T tokens ([OAL] Algorithm 1,
+ * causal-evaluation stage, lines 5-12), evaluated in chunks of `chunk`
+ * tokens: inter-chunk terms through the prefix states (Eqs. 5-6),
+ * intra-chunk terms pair by pair from the group sums (Eq. 7).  Exact in
+ * real arithmetic ([OAL] App. D, Eq. (25)).
+ *  Q [B][Hq][T][d], K [B][Hkv][T][d], V [B][Hkv][T][dv] in `dtype`.
+ *  L, group, G, eps: the kernel parameters (as for oal_expand_coeffs).
+ *  a, b, C: the tables oal_expand_coeffs produced from the same
+ *    (L, group, eps) in the same `layout` (not checked).
+ *  state [B][Hkv][F][dv+1] fp32 in `layout`: on return, the states after
+ *    token T-1.  continue_from_state != 0 starts from the values in `state`
+ *    (resume after an earlier prefill or decode); 0 starts from zero.
+ *  Y [B][Hq][T][dv] in `dtype` (bf16 outputs are rounded once from fp32).
+ *  chunk: 0 (default) or one of 64, 128, 256.
+ *  workspace: device scratch of at least oal_prefill_workspace_bytes(...)
+ *    bytes, 256-byte aligned; contents need not be initialised.
+ * Arithmetic: OAL_F32 inputs use fp32 CUDA-core FMA throughout.  OAL_BF16
+ * inputs use bf16 tensor-core products with fp32 accumulation and fp32
+ * states (the state snapshots read by the readout are rounded to bf16).
+ * T == 0 leaves Y untouched and sets `state` to zero unless
+ * continue_from_state != 0.
+ */
+size_t oal_prefill_workspace_bytes(int B, int Hq, int Hkv, int T, int d,
+                                   int dv, oal_dtype dtype,
+                                   oal_state_layout layout, int chunk);
+oal_status oal_prefill(const void *Q, const void *K, const void *V,
+                       oal_dtype dtype, int B, int Hq, int Hkv, int T, int d,
+                       int dv, const float *L, const int32_t *group, int G,
+                       float eps, const float *a, const float *b,
+                       const float *C, oal_state_layout layout, float *state,
+                       int continue_from_state, void *Y, int chunk,
+                       void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/*
+ * oal_decode_step -- one token of [OAL] Algorithm 1 (lines 7-10) for every
+ * sequence: u = [v; 1]; H0 += u; H1_r += k_r u; H2_rt += k_r k_t u; then the
+ * Eq. (6) readout for each query head of the KV head (inclusive: the new
+ * token attends to itself).
+ *  q [B][Hq][d], k [B][Hkv][d], v [B][Hkv][dv] in `dtype`; y [B][Hq][dv].
+ *  a, b, C, layout: as for oal_prefill.  state: in/out, fp32.
+ *  workspace: at least oal_decode_workspace_bytes(...) bytes, 256-byte
+ *    aligned, contents need not be initialised.
+ * Arithmetic: fp32 state update and fp32 accumulation (CUDA cores).
+ */
+size_t oal_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int dv,
+                                  oal_state_layout layout);
+oal_status oal_decode_step(const void *q, const void *k, const void *v,
+                           oal_dtype dtype, int B, int Hq, int Hkv, int d,
+                           int dv, const float *a, const float *b,
+                           const float *C, oal_state_layout layout,
+                           float *state, void *y, void *workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * oal_sync_status -- synchronises `stream`, then returns and clears the
+ * device status word (OAL_OK if no kernel recorded an error), or
+ * OAL_ERR_CUDA if the synchronisation itself failed.
+ */
+oal_status oal_sync_status(cudaStream_t stream);
+
+/*
+ * Launch accounting and per-kernel timing, for benchmarks and tracing.
+ *  oal_launch_counter: kernels this library has launched in this process.
+ *  oal_set_launch_events: thread-local hook.  While `events` is non-null,
+ *    each entry-point call made by the calling thread records events[0] on its
+ *    stream before its first kernel and events[k] right after its k-th kernel
+ *    (k = 1 .. n-1; launches beyond n-1 are not bracketed).  The events are
+ *    caller-owned cudaEvent_t handles created on the current device.
+ *    Pass NULL (or n = 0) to switch the hook off.
+ *  oal_last_call_launches / oal_last_call_launch_name: number and names of
+ *    the kernels launched by the calling thread's last entry-point call
+ *    (memset nodes are not counted).
+ */
+uint64_t oal_launch_counter(void);
+oal_status oal_set_launch_events(cudaEvent_t *events, int n);
+int oal_last_call_launches(void);
+const char *oal_last_call_launch_name(int k);
+
+/* Message of the calling thread's last non-OK status ("" if none). */
+const char *oal_last_error(void);
+
+/* Library version, e.g. "0.1.0". */
+const char *oal_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* OAL_H */
