@@ -16,6 +16,12 @@ oal_status launch_prefill_simt(const void *Q, const void *K, const void *V, int 
                                const int32_t *group, int G, float eps, const float *a,
                                const float *b, const float *C, int packed, float *state,
                                int cont, void *Y, int chunk, void *ws, cudaStream_t stream);
+size_t tc_prefill_workspace_bytes(int B, int Hq, int Hkv, int T);
+oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B, int Hq,
+                             int Hkv, int T, const float *L, const int32_t *group, int G,
+                             float eps, const float *a, const float *b, const float *C,
+                             int packed, float *state, int cont, void *Y, void *ws,
+                             cudaStream_t stream);
 size_t decode_workspace_bytes(int B, int Hkv, int packed);
 int decode_max_rho();
 oal_status launch_decode(const void *q, const void *k, const void *v, int is_bf16, int B,
@@ -175,7 +181,11 @@ oal_status oal_expand_coeffs(const float *L, const int32_t *group, int Hq, int G
                                    C, stream);
 }
 
-static int default_chunk(oal_dtype dtype) { return dtype == OAL_BF16 ? 64 : 64; }
+static int default_chunk(oal_dtype dtype) { return dtype == OAL_BF16 ? 128 : 64; }
+
+// bf16 inputs with 128-token chunks run on the tensor cores (tcgen05); every
+// other combination runs the fp32 CUDA-core kernels.
+static bool use_tc(oal_dtype dtype, int chunk) { return dtype == OAL_BF16 && chunk == 128; }
 
 size_t oal_prefill_workspace_bytes(int B, int Hq, int Hkv, int T, int d, int dv,
                                    oal_dtype dtype, oal_state_layout layout, int chunk) {
@@ -183,6 +193,7 @@ size_t oal_prefill_workspace_bytes(int B, int Hq, int Hkv, int T, int d, int dv,
   if (chunk == 0) chunk = default_chunk(dtype);
   if (chunk != 64 && chunk != 128 && chunk != 256) return 0;
   if (T == 0 || B == 0) return 256;
+  if (use_tc(dtype, chunk)) return oal::tc_prefill_workspace_bytes(B, Hq, Hkv, T);
   return oal::simt_prefill_workspace_bytes(B, Hkv, T, layout == OAL_STATE_PACKED, chunk);
 }
 
@@ -233,6 +244,9 @@ oal_status oal_prefill(const void *Q, const void *K, const void *V, oal_dtype dt
   if ((long long)T * Hq * B > (1LL << 40))
     return oal_fail(OAL_ERR_UNSUPPORTED, "problem too large");
   oal_begin_call(stream);
+  if (use_tc(dtype, chunk))
+    return oal::launch_prefill_tc(Q, K, V, B, Hq, Hkv, T, L, group, G, eps, a, b, C, packed,
+                                  state, continue_from_state != 0, Y, workspace, stream);
   return oal::launch_prefill_simt(Q, K, V, dtype == OAL_BF16, B, Hq, Hkv, T, L, group, G,
                                   eps, a, b, C, packed, state, continue_from_state != 0,
                                   Y, chunk, workspace, stream);

@@ -1,0 +1,1144 @@
+// prefill_tc.cu -- chunked causal OAL prefill on the Blackwell tensor cores
+// (tcgen05 UMMA, tensor memory, TMA), bf16 inputs, fp32 states.
+//
+// [OAL] = "Not All Dimensions Are Equal: Outlier-Aware Attention
+// Linearization with Grouped Quadratic Kernels".  For token i of chunk c
+// (C = 128 tokens)
+//     u~_i = Phi~(q_i)^T S_{c-1}  +  sum_{j in c, j <= i} kappa(q_i, k_j) u_j,
+// S_{c-1} = the Eq. (5) prefix states over all tokens before the chunk,
+// Phi~ = the Eq. (6) readout weights, kappa = Eq. (7).  The split is exact
+// (App. D, Eq. (25)).
+//
+// Internal feature order (K of every contraction, 2192 = 35 x 64 - 48):
+//   [0, 2112)     H2_rt in "paired" rows: for r = 0..63, t = (r & ~1) .. 63.
+//                 Every row has even length, so bf16 pairs never straddle a
+//                 row; the entry (r, r-1) of an odd row r duplicates
+//                 (r-1, r) (H2 is symmetric) and carries readout weight 0.
+//   [2112, 2176)  H1_r
+//   2176          H0, then 15 zero features
+// Readout weights per head (from the oal_expand_coeffs tables):
+//   H2: C_rt q_r q_t / 64 with multiplicity 2 for t > r (App. D packed
+//   readout), H1: b_r q_r / 8, H0: a.
+//
+// Launches per call:
+//   tc_prep_kernel      per query head: readout weights in the feature order
+//                       above (bf16) and the constants of the intra-chunk
+//                       kernel evaluation.
+//   tc_state_kernel     mode 0 (only when the sequence is split into parts):
+//                       per (feature tile, part): the part's total
+//                       Delta S = sum phi(k_j) u_j^T.
+//                       mode 1: per (feature tile, part): walk the part's
+//                       chunks with the fp32 state resident in tensor memory;
+//                       before each chunk write its bf16 snapshot S_{c-1};
+//                       the last part writes the final fp32 state.
+//   tc_readout_kernel   per (chunk, group of <= 4 query heads, batch x KV
+//                       head): inter-chunk readout Phi~(Q_c) S_{c-1} as a
+//                       128 x 80 x 2192 UMMA per head (A = Phi~ built by
+//                       threads straight into tensor memory, B = snapshot
+//                       streamed by TMA), intra-chunk kappa tile from
+//                       s = Q_c K_c^T (UMMA) plus the tail-group sums (fp32
+//                       FMA), P.V by UMMA, then normalisation.
+#include <cudaTypedefs.h>
+
+#include <utility>
+
+#include "oal_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace oal {
+namespace tcp {
+
+using namespace oal::tc;
+
+constexpr int kC = 128;          // tokens per chunk
+constexpr int kKP = 2192;        // internal features
+constexpr int kH2P = 2112;       // paired H2 features
+constexpr int kNKB = 35;         // readout K blocks of 64 (the last one has K = 16)
+constexpr int kTiles = 18;       // 128-feature tiles of the state kernel
+constexpr int kN = 80;           // snapshot rows: 64 value columns, the "1" column, 15 zeros
+constexpr int kMaxNH = 4;        // query heads per readout block
+constexpr int kMaxTailG = 6;     // tail groups (G - 1 <= 6)
+constexpr size_t kSnapBytes = (size_t)kN * kKP * 2;   // 350,720 B per (unit, chunk)
+
+__host__ __device__ constexpr int row_len(int r) { return 64 - (r & ~1); }
+__host__ __device__ constexpr int row_off(int r) {
+  int o = 0;
+  for (int i = 0; i < r; ++i) o += row_len(i);
+  return o;
+}
+__host__ __device__ constexpr int feat_r(int f) {
+  int r = 0;
+  while (r < 63 && row_off(r + 1) <= f) ++r;
+  return r;
+}
+__host__ __device__ constexpr int feat_t(int f) { return (feat_r(f) & ~1) + (f - row_off(feat_r(f))); }
+
+static_assert(row_off(64) == kH2P, "paired H2 size");
+
+// code: H2 -> r << 8 | t ; H1 -> 0x8000 | r ; H0 -> 0xC000 ; padding -> 0xFFFF
+struct FeatTable {
+  uint16_t code[kKP];
+};
+__host__ __device__ constexpr FeatTable make_feat_table() {
+  FeatTable ft{};
+  int f = 0;
+  for (int r = 0; r < 64; ++r)
+    for (int t = r & ~1; t < 64; ++t) ft.code[f++] = (uint16_t)((r << 8) | t);
+  for (int r = 0; r < 64; ++r) ft.code[f++] = (uint16_t)(0x8000 | r);
+  ft.code[f++] = 0xC000;
+  while (f < kKP) ft.code[f++] = 0xFFFF;
+  return ft;
+}
+static __device__ const FeatTable g_feat = make_feat_table();
+
+// Row of the external state (FULL or PACKED layout) holding feature `code`;
+// -1 for padding.  `mirror` (FULL only) receives the (t, r) row or -1.
+__device__ __forceinline__ int ext_row(uint16_t code, int packed, int *mirror) {
+  *mirror = -1;
+  if (code == 0xFFFF) return -1;
+  if (code == 0xC000) return 0;
+  if (code & 0x8000) return 1 + (code & 0xff);
+  int r = code >> 8, t = code & 0xff;
+  if (t < r) { const int x = r; r = t; t = x; }   // duplicate of (r-1, r)
+  if (packed) return 1 + kD + r * kD - r * (r - 1) / 2 + (t - r);
+  if (t != r) *mirror = 1 + kD + t * kD + r;
+  return 1 + kD + r * kD + t;
+}
+
+// H2 entry (r, r-1) of an odd row: a copy of (r-1, r), not exported.
+__device__ __forceinline__ bool is_duplicate(uint16_t code) {
+  return !(code & 0x8000) && (code >> 8) > (code & 0xff);
+}
+
+// Constants of the intra-chunk kernel evaluation for one query head.
+//   w_c = L00 [c == 0] + alpha_c s + sum_g' beta[g'][c] s_g',
+//   kappa = eps + sum_c w_c^2,
+// where s = q.k (unscaled) and s_g' = sum over the dims of tail group g' of
+// q_r k_r.  The bulk group g* (largest) is eliminated through
+// s_{g*} = s - sum_{g != g*} s_g; alpha/beta carry the 1/sqrt(64) scale.
+struct KPlan {
+  float alpha[8];
+  float beta[kMaxTailG][8];
+  float L00, eps;
+  int ntg;                     // tail groups (G - 1)
+  int nd[kMaxTailG];           // dims per tail group
+  int dims[kMaxTailG][2];      // the dims when nd <= 2 (fast path)
+  int fast;                    // every tail group has <= 2 dims
+  int goff[kMaxTailG + 1];     // generic path: dims of tail group g' in gdims[goff[g']..]
+  int gdims[64];
+  int G;
+};
+
+// ---------------------------------------------------------------- prep
+__global__ void __launch_bounds__(256)
+tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
+               const float *__restrict__ Ctab, const float *__restrict__ L,
+               const int32_t *__restrict__ group, int G, float eps, int packed,
+               __nv_bfloat16 *__restrict__ coef, KPlan *__restrict__ plans, int *status) {
+  const int h = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int G1 = G + 1;
+  __shared__ int sgrp[kD];
+  __shared__ float sL[64];
+  __shared__ int scnt[8];
+  if (tid < 8) scnt[tid] = 0;
+  if (tid < G1 * G1) sL[tid] = L[(size_t)h * G1 * G1 + tid];
+  __syncthreads();
+  if (tid < kD) {
+    int g = group[(size_t)h * kD + tid];
+    if (g < 1 || g > G) { atomicCAS(status, kStatusOk, (int)OAL_ERR_INVALID_ARG); g = 1; }
+    sgrp[tid] = g;
+    atomicAdd(&scnt[g], 1);
+  }
+  // readout weights in the internal feature order (blockIdx.y splits the rows)
+  const float *Ch = Ctab + (size_t)h * (packed ? kH2Packed : kH2Full);
+  for (int f = blockIdx.y * blockDim.x + tid; f < kKP; f += blockDim.x * gridDim.y) {
+    const uint16_t code = g_feat.code[f];
+    float w = 0.f;
+    if (code == 0xC000) {
+      w = a[h];
+    } else if (code == 0xFFFF) {
+      w = 0.f;
+    } else if (code & 0x8000) {
+      w = b[(size_t)h * kD + (code & 0xff)] * 0.125f;
+    } else {
+      const int r = code >> 8, t = code & 0xff;
+      if (t < r) w = 0.f;
+      else if (packed) w = Ch[r * kD - r * (r - 1) / 2 + (t - r)] * 0.015625f;
+      else w = Ch[r * kD + t] * (t == r ? 0.015625f : 0.03125f);
+    }
+    coef[(size_t)h * kKP + f] = __float2bfloat16_rn(w);
+  }
+  __syncthreads();
+  if (blockIdx.y != 0) return;
+  // kappa constants: the bulk group g* is the largest; the others are tail groups
+  int gstar = 1;
+  for (int g = 2; g <= G; ++g)
+    if (scnt[g] > scnt[gstar]) gstar = g;
+  auto Lat = [&](int g, int c) { return c <= g ? sL[g * G1 + c] : 0.f; };
+  KPlan *P = plans + h;
+  if (tid >= 1 && tid <= G && tid != gstar) {
+    const int g = tid;
+    const int slot = g < gstar ? g - 1 : g - 2;
+    int off = 0;
+    for (int gg = 1; gg < g; ++gg)
+      if (gg != gstar) off += scnt[gg];
+    P->goff[slot] = off;
+    int k = 0;
+    P->dims[slot][0] = P->dims[slot][1] = 0;
+    for (int r = 0; r < kD; ++r) {
+      if (sgrp[r] != g) continue;
+      if (k < 2) P->dims[slot][k] = r;
+      P->gdims[off + k] = r;
+      ++k;
+    }
+    P->nd[slot] = k;
+    for (int c = 0; c < 8; ++c) P->beta[slot][c] = c <= G ? (Lat(g, c) - Lat(gstar, c)) * 0.125f : 0.f;
+  }
+  if (tid == 0) {
+    int fast = 1, tot = 0;
+    for (int g = 1; g <= G; ++g)
+      if (g != gstar) { fast &= scnt[g] <= 2; tot += scnt[g]; }
+    for (int slot = G - 1; slot < kMaxTailG; ++slot) {
+      for (int c = 0; c < 8; ++c) P->beta[slot][c] = 0.f;
+      P->nd[slot] = 0;
+      P->dims[slot][0] = P->dims[slot][1] = 0;
+      P->goff[slot] = tot;
+    }
+    P->goff[kMaxTailG] = tot;
+    for (int c = 0; c < 8; ++c) P->alpha[c] = c <= G ? Lat(gstar, c) * 0.125f : 0.f;
+    P->ntg = G - 1;
+    P->fast = fast;
+    P->L00 = sL[0];
+    P->eps = eps;
+    P->G = G;
+  }
+}
+
+// ---------------------------------------------------------------- swizzle helpers
+// Byte offset of 16-byte chunk `c` of row `m` in a 128B-swizzled tile.
+__device__ __forceinline__ uint32_t sw128(int m, int c) {
+  return (uint32_t)(m * 128 + ((c ^ (m & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t x, uint32_t y) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
+  return r;
+}
+__device__ __forceinline__ uint32_t bcast_lo(uint32_t x) { return __byte_perm(x, 0, 0x1010); }
+__device__ __forceinline__ uint32_t bcast_hi(uint32_t x) { return __byte_perm(x, 0, 0x3232); }
+__device__ __forceinline__ uint32_t tmem_lane_addr(uint32_t base, int warp, int col) {
+  return base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)col;
+}
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// ================================================================= state kernel
+// One block per (128-feature tile, part of the sequence, batch x KV head).
+// Per chunk c of the part: Delta S_c = phi(K_c)^T [V_c | 1] by UMMA into one
+// of two tensor-memory accumulators; phi is split exactly into two bf16
+// terms (hi = bf16(k_r k_t), lo = k_r k_t - hi; the product of two bf16
+// values has at most 16 significant bits), so the fp32 state is exact up to
+// fp32 accumulation.  The epilogue warps keep the running fp32 state of their
+// feature row in registers, add each Delta S_c, and (mode 1) write the bf16
+// snapshot S_{c-1} that the readout of chunk c consumes.
+constexpr int kStateStages = 3;
+
+struct __align__(1024) StateSmem {
+  __nv_bfloat16 kv[kStateStages][2][kC * 64];   // [stage][K | V] 128B-swizzled tiles
+  __nv_bfloat16 ones[kC * 64];                  // MN-major B tile whose column 0 is 1
+  __nv_bfloat16 kT[64][kC + 8];                 // K transposed: [dim][token]
+  uint64_t kv_full[kStateStages], kv_empty[kStateStages];
+  uint64_t a_full[2], a_empty[2], d_full[2], d_empty[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(StateSmem) + 1024 <= 227 * 1024, "state shared memory");
+
+struct StateArgs {
+  int T, nC, U, cpp, nparts, packed, cont, mode;
+  const float *state_in;     // external state (continue) or null
+  float *state_out;          // external state (mode 1, last part)
+  float *ptot;               // [U][nparts][kTiles][128][kN] fp32 part totals
+  __nv_bfloat16 *snap;       // [U*nC][kN][kKP]
+  int *status;
+};
+
+constexpr int kStateThreads = 384;
+constexpr int kStateD = 0;          // accumulators at cols 0 and 128 (80 wide)
+constexpr int kStateA = 256;        // A slots at 256 and 384: [hi 64 | lo 64]
+
+__device__ __forceinline__ uint32_t hfma2_bf16(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+__global__ void __launch_bounds__(kStateThreads, 1)
+tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                StateArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  StateSmem &s = *reinterpret_cast<StateSmem *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tile = blockIdx.x, part = blockIdx.y, unit = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c0 = part * args.cpp;
+  const int c1 = min(args.nC, c0 + args.cpp);
+  const int nchunks = c1 - c0;
+  const int mode = args.mode;
+
+  if (tid == 0) {
+    s.abort_flag = 0;
+    for (int i = 0; i < kStateStages; ++i) {
+      mbar_init(&s.kv_full[i], 1);
+      mbar_init(&s.kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.a_full[i], 4);
+      mbar_init(&s.a_empty[i], 1);
+      mbar_init(&s.d_full[i], 1);
+      mbar_init(&s.d_empty[i], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp >= 4 && warp < 8) {
+    // ones tile (MN-major B of the "1" column): row j = token j, element 0 = 1
+    const int j = tid - 128;
+    for (int c = 0; c < 8; ++c) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (c == 0) v.x = 0x3F80u;
+      *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(s.ones) + sw128(j, c)) = v;
+    }
+    fence_proxy_async();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = s.tmem_base;
+  volatile int *abort_flag = &s.abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int issued = 0;
+      for (int i = 0; i < nchunks; ++i) {
+        const int st = i % kStateStages;
+        if (!mbar_wait(&s.kv_empty[st], ((i / kStateStages) & 1) ^ 1, abort_flag, args.status))
+          break;
+        mbar_arrive_expect_tx(&s.kv_full[st], 2 * kC * 64 * 2);
+        tma_load_3d(s.kv[st][0], &tmK, &s.kv_full[st], 0, (c0 + i) * kC, unit);
+        tma_load_3d(s.kv[st][1], &tmV, &s.kv_full[st], 0, (c0 + i) * kC, unit);
+        issued = i + 1;
+      }
+      // copies still in flight must land before the block exits
+      for (int i = max(0, issued - kStateStages); i < issued; ++i)
+        mbar_wait_teardown(&s.kv_full[i % kStateStages], (i / kStateStages) & 1, args.status);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      const uint32_t idv = idesc_bf16_f32(128, 64, 1);
+      const uint32_t id1 = idesc_bf16_f32(128, 16, 1);
+      const uint32_t oaddr = smem_u32(s.ones);
+      for (int i = 0; i < nchunks; ++i) {
+        const int sl = i & 1, st = i % kStateStages;
+        if (!mbar_wait(&s.a_full[sl], (i >> 1) & 1, abort_flag, args.status)) break;
+        if (!mbar_wait(&s.d_empty[sl], ((i >> 1) & 1) ^ 1, abort_flag, args.status)) break;
+        tc_fence_after();
+        const uint32_t vaddr = smem_u32(s.kv[st][1]);
+        const uint32_t d = tb + kStateD + 128 * sl;
+        for (int k = 0; k < 16; ++k) {     // K = 256: hi half then lo half
+          const uint32_t acc = k > 0 ? 1u : 0u;
+          const uint32_t at = tb + kStateA + 128 * sl + 8 * k;
+          const uint32_t brow = 2048 * (k & 7);
+          umma_ts(d, at, sdesc_sw128(vaddr + brow, 16, 1024), idv, acc);
+          umma_ts(d + 64, at, sdesc_sw128(oaddr + brow, 16, 1024), id1, acc);
+        }
+        umma_commit(&s.a_empty[sl]);
+        umma_commit(&s.kv_empty[st]);
+        umma_commit(&s.d_full[sl]);
+      }
+      // no MMA in flight at dealloc: drain through the accumulator barriers
+      for (int i = max(0, nchunks - 2); i < nchunks; ++i)
+        mbar_wait_teardown(&s.d_full[i & 1], (i >> 1) & 1, args.status);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- builders: transpose K, then A = phi(K_c)^T (hi | lo)
+    const int l = tid - 128;                 // TMEM lane = feature row, = token when transposing
+    const int f = tile * 128 + l;
+    const uint16_t code = f < kKP ? g_feat.code[f] : (uint16_t)0xFFFF;
+    for (int i = 0; i < nchunks; ++i) {
+      const int sl = i & 1, st = i % kStateStages;
+      const int c = c0 + i;
+      if (!mbar_wait(&s.kv_full[st], (i / kStateStages) & 1, abort_flag, args.status)) break;
+      named_bar(1, 128);   // the previous chunk's builds are done with kT
+      {
+        const uint8_t *krow = reinterpret_cast<const uint8_t *>(s.kv[st][0]);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(krow + sw128(l, cc));
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int dd = cc * 8 + 2 * e;
+            reinterpret_cast<uint16_t *>(&s.kT[dd][0])[l] = (uint16_t)(w[e] & 0xffff);
+            reinterpret_cast<uint16_t *>(&s.kT[dd + 1][0])[l] = (uint16_t)(w[e] >> 16);
+          }
+        }
+      }
+      named_bar(1, 128);
+      if (!mbar_wait(&s.a_empty[sl], ((i >> 1) & 1) ^ 1, abort_flag, args.status)) break;
+      const int nvalid = min(kC, args.T - c * kC);
+      const uint32_t abase = kStateA + 128 * sl;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t hi[16], lo[16];
+        if (code == 0xFFFF) {
+#pragma unroll
+          for (int w = 0; w < 16; ++w) hi[w] = lo[w] = 0u;
+        } else if (code == 0xC000) {
+#pragma unroll
+          for (int w = 0; w < 16; ++w) {
+            const int j = 32 * q + 2 * w;
+            hi[w] = (j < nvalid ? 0x3F80u : 0u) | (j + 1 < nvalid ? 0x3F800000u : 0u);
+            lo[w] = 0u;
+          }
+        } else if (code & 0x8000) {
+          const uint4 *kr = reinterpret_cast<const uint4 *>(&s.kT[code & 0xff][32 * q]);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint4 x = kr[v];
+            hi[4 * v] = x.x; hi[4 * v + 1] = x.y; hi[4 * v + 2] = x.z; hi[4 * v + 3] = x.w;
+            lo[4 * v] = lo[4 * v + 1] = lo[4 * v + 2] = lo[4 * v + 3] = 0u;
+          }
+        } else {
+          const uint4 *kr = reinterpret_cast<const uint4 *>(&s.kT[code >> 8][32 * q]);
+          const uint4 *kt = reinterpret_cast<const uint4 *>(&s.kT[code & 0xff][32 * q]);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint4 x = kr[v], y = kt[v];
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t h2 = hmul2(xs[e], ys[e]);
+              hi[4 * v + e] = h2;
+              lo[4 * v + e] = hfma2_bf16(xs[e], ys[e], h2 ^ 0x80008000u);   // exact residual
+            }
+          }
+        }
+        tmem_st16(tmem_lane_addr(tb, warp, abase + 16 * q), hi);
+        tmem_st16(tmem_lane_addr(tb, warp, abase + 64 + 16 * q), lo);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.a_full[sl]);
+    }
+  } else if (warp >= 8) {
+    // ---------------- epilogue: running fp32 state of this feature row
+    const int l = tid - 256;
+    const int f = tile * 128 + l;
+    const uint16_t code = f < kKP ? g_feat.code[f] : (uint16_t)0xFFFF;
+    int mirror;
+    const int erow = ext_row(code, args.packed, &mirror);
+    const size_t FU = (size_t)state_rows(args.packed) * kU;
+    float S[kU];   // columns 65..79 of the accumulators stay zero
+#pragma unroll
+    for (int n = 0; n < kU; ++n) S[n] = 0.f;
+    if (mode == 1) {
+      if (args.cont && erow >= 0) {
+        const float *src = args.state_in + (size_t)unit * FU + (size_t)erow * kU;
+#pragma unroll
+        for (int n = 0; n < kU; ++n) S[n] = src[n];
+      }
+      for (int p = 0; p < part; ++p) {
+        const float4 *src = reinterpret_cast<const float4 *>(
+            args.ptot + ((((size_t)unit * args.nparts + p) * kTiles + tile) * 128 + l) * kN);
+#pragma unroll
+        for (int n4 = 0; n4 < 16; ++n4) {
+          const float4 v = src[n4];
+          S[4 * n4] += v.x; S[4 * n4 + 1] += v.y; S[4 * n4 + 2] += v.z; S[4 * n4 + 3] += v.w;
+        }
+        S[64] += src[16].x;
+      }
+    }
+    __nv_bfloat16 *snap_row =
+        f < kKP ? args.snap + ((size_t)unit * args.nC + c0) * kN * kKP + f : nullptr;
+    auto write_snapshot = [&](int cc) {   // S_{cc-1} for chunk cc of this part
+      if (snap_row) {
+        __nv_bfloat16 *dst = snap_row + (size_t)cc * kN * kKP;
+#pragma unroll
+        for (int n = 0; n < kN; ++n)
+          dst[(size_t)n * kKP] = n < kU ? __float2bfloat16_rn(S[n]) : __float2bfloat16_rn(0.f);
+      }
+    };
+    if (mode == 1 && nchunks > 0) write_snapshot(0);
+    bool ok = true;
+    for (int i = 0; i < nchunks; ++i) {
+      const int sl = i & 1;
+      if (!mbar_wait(&s.d_full[sl], (i >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < kN / 16; ++q) {
+        uint32_t r[16];
+        tmem_ld16(tmem_lane_addr(tb, warp, kStateD + 128 * sl + 16 * q), r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          if (16 * q + e < kU) S[16 * q + e] += __uint_as_float(r[e]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.d_empty[sl]);
+      if (mode == 1 && i + 1 < nchunks) write_snapshot(i + 1);
+    }
+    if (ok && !*abort_flag) {
+      if (mode == 0) {
+        float4 *dst = reinterpret_cast<float4 *>(
+            args.ptot + ((((size_t)unit * args.nparts + part) * kTiles + tile) * 128 + l) * kN);
+#pragma unroll
+        for (int n4 = 0; n4 < 16; ++n4)
+          dst[n4] = make_float4(S[4 * n4], S[4 * n4 + 1], S[4 * n4 + 2], S[4 * n4 + 3]);
+        dst[16] = make_float4(S[64], 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int n4 = 17; n4 < kN / 4; ++n4) dst[n4] = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else if (part == args.nparts - 1 && erow >= 0 && !is_duplicate(code)) {
+        float *dst = args.state_out + (size_t)unit * FU + (size_t)erow * kU;
+#pragma unroll
+        for (int n = 0; n < kU; ++n) dst[n] = S[n];
+        if (mirror >= 0) {
+          float *dm = args.state_out + (size_t)unit * FU + (size_t)mirror * kU;
+#pragma unroll
+          for (int n = 0; n < kU; ++n) dm[n] = S[n];
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tb, 512);
+  }
+}
+
+// ================================================================= readout kernel
+constexpr int kNB = 6;           // snapshot K-block stages
+constexpr int kNA = 4;           // A slots in tensor memory
+constexpr int kTailSlots = 2 * kMaxTailG;
+
+struct __align__(1024) ReadSmem {
+  __nv_bfloat16 q[kMaxNH][kC * 64];    // 128B-swizzled [token][dim]
+  __nv_bfloat16 k[kC * 64];
+  __nv_bfloat16 v[kC * 64];
+  __nv_bfloat16 b[kNB][kN * 64];       // snapshot K blocks [n][64 features]
+  __nv_bfloat16 coef[kMaxNH][kKP];
+  float kt[kMaxNH][kC][kTailSlots];    // tail-dim key values (fast path)
+  KPlan plan[kMaxNH];
+  uint64_t qkv_full, b_full[kNB], b_empty[kNB], a_full[kNA], a_empty[kNA];
+  uint64_t s_full, p_full, s_free, d_full;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+static_assert(sizeof(ReadSmem) + 1024 <= 227 * 1024, "readout shared memory");
+
+struct ReadArgs {
+  int T, nC, Hq, Hkv, rho, nh_per_block;
+  __nv_bfloat16 *Y;
+  const __nv_bfloat16 *coef;   // [Hq][kKP]
+  const KPlan *plans;          // [Hq]
+  int *status;
+};
+
+constexpr int kReadThreads = 416;   // 13 warps
+constexpr int kTmemD = 0;         // D^h at [80h, 80h + 80)
+constexpr int kTmemA = 320;       // A slots [320, 448)
+constexpr int kTmemS = 448;       // s / P tile [448, 512)
+
+// ---- readout A block builders (compile-time feature layout)
+template <int KB, int P>
+__device__ __forceinline__ uint32_t h2_pair(const uint32_t (&q)[32], uint32_t cw) {
+  constexpr int f = 64 * KB + 2 * P;
+  constexpr int r = feat_r(f);
+  constexpr int t = feat_t(f);
+  const uint32_t qr = (r & 1) ? bcast_hi(q[r >> 1]) : bcast_lo(q[r >> 1]);
+  return hmul2(hmul2(qr, q[t >> 1]), cw);
+}
+
+template <int KB, int... P>
+__device__ __forceinline__ void h2_block(const uint32_t (&q)[32], const uint32_t (&cw)[32],
+                                         uint32_t (&out)[32], std::integer_sequence<int, P...>) {
+  ((out[P] = h2_pair<KB, P>(q, cw[P])), ...);
+}
+
+template <int KB>
+__device__ __forceinline__ void build_block(const uint32_t (&q)[32], const uint32_t (&cw)[32],
+                                            uint32_t (&out)[32]) {
+  if constexpr (KB < 33) {
+    h2_block<KB>(q, cw, out, std::make_integer_sequence<int, 32>{});
+  } else if constexpr (KB == 33) {
+#pragma unroll
+    for (int p = 0; p < 32; ++p) out[p] = hmul2(q[p], cw[p]);
+  } else {
+#pragma unroll
+    for (int p = 0; p < 32; ++p) out[p] = p == 0 ? (cw[0] & 0xffffu) : 0u;
+  }
+}
+
+#define OAL_BUILD_CASE(n) \
+  case n:                 \
+    build_block<n>(q, cw, out); \
+    break;
+
+__device__ __forceinline__ void build_dispatch(int kb, const uint32_t (&q)[32],
+                                               const uint32_t (&cw)[32], uint32_t (&out)[32]) {
+  switch (kb) {
+    OAL_BUILD_CASE(0) OAL_BUILD_CASE(1) OAL_BUILD_CASE(2) OAL_BUILD_CASE(3)
+    OAL_BUILD_CASE(4) OAL_BUILD_CASE(5) OAL_BUILD_CASE(6) OAL_BUILD_CASE(7)
+    OAL_BUILD_CASE(8) OAL_BUILD_CASE(9) OAL_BUILD_CASE(10) OAL_BUILD_CASE(11)
+    OAL_BUILD_CASE(12) OAL_BUILD_CASE(13) OAL_BUILD_CASE(14) OAL_BUILD_CASE(15)
+    OAL_BUILD_CASE(16) OAL_BUILD_CASE(17) OAL_BUILD_CASE(18) OAL_BUILD_CASE(19)
+    OAL_BUILD_CASE(20) OAL_BUILD_CASE(21) OAL_BUILD_CASE(22) OAL_BUILD_CASE(23)
+    OAL_BUILD_CASE(24) OAL_BUILD_CASE(25) OAL_BUILD_CASE(26) OAL_BUILD_CASE(27)
+    OAL_BUILD_CASE(28) OAL_BUILD_CASE(29) OAL_BUILD_CASE(30) OAL_BUILD_CASE(31)
+    OAL_BUILD_CASE(32) OAL_BUILD_CASE(33) OAL_BUILD_CASE(34)
+    default: break;
+  }
+}
+#undef OAL_BUILD_CASE
+
+__device__ __forceinline__ float bf16_at(const __nv_bfloat16 *tile, int row, int col) {
+  const uint8_t *base = reinterpret_cast<const uint8_t *>(tile);
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+      base + sw128(row, col >> 3) + (col & 7) * 2));
+}
+
+// ---- intra-chunk kernel evaluation (Eq. 7) for one 32-key block.
+// Fast path: every tail group has <= 2 dims, constants in registers.
+template <int G>
+struct KConst {
+  float alpha[G + 1];
+  float beta[G > 1 ? G - 1 : 1][G + 1];
+  float L00, eps;
+};
+
+template <int G>
+__device__ __forceinline__ float kappa_g(const KConst<G> &k, float s, const float (&qt)[2 * kMaxTailG],
+                                         const float *ktj) {
+  float sg[G > 1 ? G - 1 : 1];
+#pragma unroll
+  for (int g = 0; g < G - 1; ++g) sg[g] = fmaf(qt[2 * g], ktj[2 * g], qt[2 * g + 1] * ktj[2 * g + 1]);
+  float kap = k.eps;
+#pragma unroll
+  for (int c = 0; c <= G; ++c) {
+    float w = fmaf(k.alpha[c], s, c == 0 ? k.L00 : 0.f);
+#pragma unroll
+    for (int g = 0; g < G - 1; ++g) w = fmaf(k.beta[g][c], sg[g], w);
+    kap = fmaf(w, w, kap);
+  }
+  return kap;
+}
+
+// Generic path (a tail group with more than 2 dims): sums straight from the
+// Q and K tiles, constants from shared memory.
+__device__ float kappa_generic(const KPlan &p, float s, const __nv_bfloat16 *qtile,
+                               const __nv_bfloat16 *ktile, int m, int j) {
+  float sg[kMaxTailG];
+  for (int g = 0; g < kMaxTailG; ++g) {
+    float acc = 0.f;
+    if (g < p.ntg)
+      for (int d = p.goff[g]; d < p.goff[g + 1]; ++d)
+        acc = fmaf(bf16_at(qtile, m, p.gdims[d]), bf16_at(ktile, j, p.gdims[d]), acc);
+    sg[g] = acc;
+  }
+  float kap = p.eps;
+  for (int c = 0; c <= p.G; ++c) {
+    float w = fmaf(p.alpha[c], s, c == 0 ? p.L00 : 0.f);
+    for (int g = 0; g < p.ntg; ++g) w = fmaf(p.beta[g][c], sg[g], w);
+    kap = fmaf(w, w, kap);
+  }
+  return kap;
+}
+
+// The intra-chunk role: for each head and each half of the key range, read
+// s = q.k for this thread's query row from tensor memory, turn it into
+// kappa (masked to keys j <= i), write P (bf16) back in place for the P.V
+// UMMA, and accumulate the denominator from the same rounded weights.
+template <int G>
+__device__ bool intra_worker(ReadSmem &s, const ReadArgs &args, int c, int nh, int warp, int lane,
+                             uint32_t tb, float (&den_intra)[kMaxNH]) {
+  volatile int *abort_flag = &s.abort_flag;
+  const int m = threadIdx.x;                      // query row (TMEM lane), warps 0-3
+  if (!mbar_wait(&s.qkv_full, 0, abort_flag, args.status)) return false;
+  // tail-dim key values of every head (fast path); thread = key row m
+  for (int hh = 0; hh < nh; ++hh) {
+    const KPlan &p = s.plan[hh];
+#pragma unroll
+    for (int g = 0; g < kMaxTailG; ++g) {
+      float k0 = 0.f, k1 = 0.f;
+      if (g < p.ntg && p.nd[g] > 0) k0 = bf16_at(s.k, m, p.dims[g][0]);
+      if (g < p.ntg && p.nd[g] > 1) k1 = bf16_at(s.k, m, p.dims[g][1]);
+      s.kt[hh][m][2 * g] = k0;
+      s.kt[hh][m][2 * g + 1] = k1;
+    }
+  }
+  named_bar(2, 128);
+  const int row_max = 32 * (warp & 3) + 31;       // largest query row of this warp
+  for (int it = 0; it < 2 * nh; ++it) {
+    const int hh = it >> 1, half = it & 1;
+    const KPlan &p = s.plan[hh];
+    KConst<G> kc;
+#pragma unroll
+    for (int cc = 0; cc <= G; ++cc) {
+      kc.alpha[cc] = p.alpha[cc];
+#pragma unroll
+      for (int g = 0; g < G - 1; ++g) kc.beta[g][cc] = p.beta[g][cc];
+    }
+    kc.L00 = p.L00;
+    kc.eps = p.eps;
+    float qt[2 * kMaxTailG];
+#pragma unroll
+    for (int g = 0; g < kMaxTailG; ++g) {
+      qt[2 * g] = (g < p.ntg && p.nd[g] > 0) ? bf16_at(s.q[hh], m, p.dims[g][0]) : 0.f;
+      qt[2 * g + 1] = (g < p.ntg && p.nd[g] > 1) ? bf16_at(s.q[hh], m, p.dims[g][1]) : 0.f;
+    }
+    const bool fast = p.fast != 0;
+    if (!mbar_wait(&s.s_full, it & 1, abort_flag, args.status)) return false;
+    tc_fence_after();
+    float dsum = 0.f;
+#pragma unroll 1
+    for (int sb = 0; sb < 2; ++sb) {            // 32-key sub-blocks
+      const int jbase = half * 64 + sb * 32;
+      uint32_t pk[16];
+      if (row_max >= jbase) {
+        uint32_t sv[32];
+        uint32_t r0[16], r1[16];
+        tmem_ld16(tmem_lane_addr(tb, warp, kTmemS + 32 * sb), r0);
+        tmem_ld16(tmem_lane_addr(tb, warp, kTmemS + 32 * sb + 16), r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) { sv[e] = r0[e]; sv[16 + e] = r1[e]; }
+        if (fast) {
+#pragma unroll
+          for (int jj = 0; jj < 32; jj += 2) {
+            float kv0 = 0.f, kv1 = 0.f;
+            const int j0 = jbase + jj;
+            if (j0 <= m) kv0 = kappa_g<G>(kc, __uint_as_float(sv[jj]), qt, s.kt[hh][j0]);
+            if (j0 + 1 <= m) kv1 = kappa_g<G>(kc, __uint_as_float(sv[jj + 1]), qt, s.kt[hh][j0 + 1]);
+            pk[jj >> 1] = pack_bf16x2(kv0, kv1);
+          }
+        } else {
+          float sl[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sl[e] = __uint_as_float(sv[e]);
+          float kl[32];
+          for (int jj = 0; jj < 32; ++jj)
+            kl[jj] = jbase + jj <= m ? kappa_generic(p, sl[jj], s.q[hh], s.k, m, jbase + jj) : 0.f;
+#pragma unroll
+          for (int jj = 0; jj < 32; jj += 2) pk[jj >> 1] = pack_bf16x2(kl[jj], kl[jj + 1]);
+        }
+        // denominator from the same rounded weights the P.V product uses
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162 *>(&pk[e]);
+          dsum += __low2float(pb) + __high2float(pb);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = 0u;
+      }
+      // P for keys [jbase, jbase + 32) -> columns [16 sb, 16 sb + 16) of the
+      // tile (s of those columns has already been read)
+      tmem_st16(tmem_lane_addr(tb, warp, kTmemS + 16 * sb), pk);
+    }
+#pragma unroll
+    for (int e = 0; e < kMaxNH; ++e)
+      if (e == hh) den_intra[e] += dsum;
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.p_full);
+  }
+  return true;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kReadThreads, 1)
+tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmS,
+                  ReadArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  ReadSmem &s = *reinterpret_cast<ReadSmem *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int hg = blockIdx.x, c = blockIdx.y, unit = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bidx = unit / args.Hkv, kv = unit % args.Hkv;
+  const int h0 = kv * args.rho + hg * args.nh_per_block;
+  const int nh = min(args.nh_per_block, args.rho - hg * args.nh_per_block);
+  const int njobs = kNKB * nh;
+  constexpr int kCtl = 12;        // control warp: TMEM, TMA, UMMA issue
+
+  if (tid == 0) {
+    s.abort_flag = 0;
+    mbar_init(&s.qkv_full, 1);
+    for (int i = 0; i < kNB; ++i) { mbar_init(&s.b_full[i], 1); mbar_init(&s.b_empty[i], 1); }
+    for (int i = 0; i < kNA; ++i) { mbar_init(&s.a_full[i], 4); mbar_init(&s.a_empty[i], 1); }
+    mbar_init(&s.s_full, 1);
+    mbar_init(&s.p_full, 4);
+    mbar_init(&s.s_free, 1);
+    mbar_init(&s.d_full, 1);
+    fence_mbar_init();
+  }
+  if (warp == kCtl) {
+    tmem_alloc(&s.tmem_base, 512);
+    tmem_relinquish();
+  }
+  // per-head readout weights and kappa constants into shared memory
+  for (int n = tid; n < nh * (kKP / 8); n += kReadThreads) {
+    const int hh = n / (kKP / 8), e = n % (kKP / 8);
+    reinterpret_cast<uint4 *>(s.coef[hh])[e] =
+        reinterpret_cast<const uint4 *>(args.coef + (size_t)(h0 + hh) * kKP)[e];
+  }
+  for (int n = tid; n < nh * (int)(sizeof(KPlan) / 4); n += kReadThreads) {
+    const int hh = n / (sizeof(KPlan) / 4), e = n % (sizeof(KPlan) / 4);
+    reinterpret_cast<int *>(&s.plan[hh])[e] =
+        reinterpret_cast<const int *>(&args.plans[h0 + hh])[e];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = s.tmem_base;
+  volatile int *abort_flag = &s.abort_flag;
+
+  if (warp == kCtl) {
+    if (lane == 0) {
+      // ---------------- control: TMA loads and the UMMA issue schedule
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmS);
+      mbar_arrive_expect_tx(&s.qkv_full, (uint32_t)(nh + 2) * kC * 64 * 2);
+      for (int hh = 0; hh < nh; ++hh)
+        tma_load_3d(s.q[hh], &tmQ, &s.qkv_full, 0, c * kC, bidx * args.Hq + h0 + hh);
+      tma_load_3d(s.k, &tmK, &s.qkv_full, 0, c * kC, unit);
+      tma_load_3d(s.v, &tmV, &s.qkv_full, 0, c * kC, unit);
+      const uint32_t id80 = idesc_bf16_f32(128, kN, 0);
+      const uint32_t id64k = idesc_bf16_f32(128, 64, 0);
+      const uint32_t id64mn = idesc_bf16_f32(128, 64, 1);
+      int nb_issued = 0;          // snapshot K blocks requested
+      int jr = 0;                 // next readout job
+      int it = 0;                 // next intra step (head * 2 + half)
+      int istate = 0;             // 0: issue s; 1: waiting for P; 2: waiting for P.V to finish
+      bool qkv_ready = false;
+      int b_seen = -1;            // highest K block whose stage has been waited for
+      uint64_t t_last = globaltimer_ns();
+      while ((jr < njobs || it < 2 * nh) && !*abort_flag) {
+        bool progress = false;
+        // snapshot K blocks into free stages
+        while (nb_issued < kNKB) {
+          const int st = nb_issued % kNB;
+          if (!mbar_test(&s.b_empty[st], ((nb_issued / kNB) & 1) ^ 1)) break;
+          mbar_arrive_expect_tx(&s.b_full[st], kN * 64 * 2);
+          tma_load_3d(s.b[st], &tmS, &s.b_full[st], 64 * nb_issued, 0, unit * args.nC + c);
+          ++nb_issued;
+          progress = true;
+        }
+        if (!qkv_ready && mbar_test(&s.qkv_full, 0)) qkv_ready = true;
+        // intra steps (the P.V of a head must follow its first readout job)
+        if (qkv_ready && it < 2 * nh) {
+          const int hh = it >> 1, half = it & 1;
+          if (istate == 0) {
+            tc_fence_after();
+            const uint32_t qa = smem_u32(s.q[hh]);
+            const uint32_t ka = smem_u32(s.k) + half * 64 * 128;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              umma_ss(tb + kTmemS, sdesc_sw128(qa + 32 * k, 16, 1024),
+                      sdesc_sw128(ka + 32 * k, 16, 1024), id64k, k > 0);
+            umma_commit(&s.s_full);
+            istate = 1;
+            progress = true;
+          } else if (istate == 1 && jr >= nh && mbar_test(&s.p_full, it & 1)) {
+            tc_fence_after();
+            const uint32_t va = smem_u32(s.v) + half * 64 * 128;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              umma_ts(tb + kTmemD + 80 * hh, tb + kTmemS + 8 * k,
+                      sdesc_sw128(va + 2048 * k, 16, 1024), id64mn, 1u);
+            umma_commit(&s.s_free);
+            istate = 2;
+            progress = true;
+          } else if (istate == 2 && mbar_test(&s.s_free, it & 1)) {
+            ++it;
+            istate = 0;
+            progress = true;
+          }
+        }
+        // readout jobs, in order
+        if (jr < njobs) {
+          const int kb = jr / nh, hh = jr % nh;
+          const int slot = jr % kNA, st = kb % kNB;
+          bool b_ok = b_seen >= kb;
+          if (!b_ok && kb < nb_issued && mbar_test(&s.b_full[st], (kb / kNB) & 1)) {
+            b_seen = kb;
+            b_ok = true;
+          }
+          if (b_ok && mbar_test(&s.a_full[slot], (jr / kNA) & 1)) {
+            tc_fence_after();
+            const uint32_t ba = smem_u32(s.b[st]);
+            const int nk = kb == kNKB - 1 ? 1 : 4;
+            for (int k = 0; k < nk; ++k)
+              umma_ts(tb + kTmemD + 80 * hh, tb + kTmemA + 32 * slot + 8 * k,
+                      sdesc_sw128(ba + 32 * k, 16, 1024), id80, (kb > 0 || k > 0) ? 1u : 0u);
+            umma_commit(&s.a_empty[slot]);
+            if (hh == nh - 1) umma_commit(&s.b_empty[st]);
+            ++jr;
+            progress = true;
+          }
+        }
+        if (progress) {
+          t_last = globaltimer_ns();
+        } else if (globaltimer_ns() - t_last > kWaitLimitNs) {
+          *abort_flag = 1;
+          atomicCAS(args.status, 0, (int)OAL_ERR_TIMEOUT);
+        }
+      }
+      umma_commit(&s.d_full);
+      // drain before the block releases its memory: copies, then MMAs
+      mbar_wait_teardown(&s.qkv_full, 0, args.status);
+      for (int kb = max(0, nb_issued - kNB); kb < nb_issued; ++kb)
+        mbar_wait_teardown(&s.b_full[kb % kNB], (kb / kNB) & 1, args.status);
+      mbar_wait_teardown(&s.d_full, 0, args.status);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------- readout A builders: two warps per TMEM lane quarter,
+    // alternating jobs; thread = token row
+    const int m = 32 * (warp & 3) + lane;
+    const int pg = (warp - 4) >> 2;           // job parity handled by this warp
+    if (mbar_wait(&s.qkv_full, 0, abort_flag, args.status)) {
+      for (int jb = pg; jb < njobs; jb += 2) {
+        const int kb = jb / nh, hh = jb % nh, slot = jb % kNA;
+        uint32_t q[32], cw[32], out[32];
+        const uint8_t *qrow = reinterpret_cast<const uint8_t *>(s.q[hh]);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(qrow + sw128(m, cc));
+          q[4 * cc] = v.x; q[4 * cc + 1] = v.y; q[4 * cc + 2] = v.z; q[4 * cc + 3] = v.w;
+        }
+        const uint4 *cp = reinterpret_cast<const uint4 *>(s.coef[hh] + 64 * kb);
+        const int ncw = kb == kNKB - 1 ? 2 : 8;   // the H0 block holds 16 features
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (e < ncw) v = cp[e];
+          cw[4 * e] = v.x; cw[4 * e + 1] = v.y; cw[4 * e + 2] = v.z; cw[4 * e + 3] = v.w;
+        }
+        build_dispatch(kb, q, cw, out);
+        if (!mbar_wait(&s.a_empty[slot], ((jb / kNA) & 1) ^ 1, abort_flag, args.status)) break;
+        uint32_t lo[16], hi[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) { lo[e] = out[e]; hi[e] = out[16 + e]; }
+        tmem_st16(tmem_lane_addr(tb, warp, kTmemA + 32 * slot), lo);
+        tmem_st16(tmem_lane_addr(tb, warp, kTmemA + 32 * slot + 16), hi);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.a_full[slot]);
+      }
+    }
+  } else {
+    // ---------------- warps 0-3: intra-chunk kernel (thread = query row), then epilogue
+    float den_intra[kMaxNH] = {0.f, 0.f, 0.f, 0.f};
+    const bool ok = intra_worker<G>(s, args, c, nh, warp, lane, tb, den_intra);
+    const int m = tid;
+    const int i_tok = c * kC + m;
+    if (ok && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
+      tc_fence_after();
+      for (int hh = 0; hh < nh; ++hh) {
+        uint32_t d[kN];
+#pragma unroll
+        for (int q5 = 0; q5 < 5; ++q5) {
+          uint32_t r[16];
+          tmem_ld16(tmem_lane_addr(tb, warp, kTmemD + 80 * hh + 16 * q5), r);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) d[16 * q5 + e] = r[e];
+        }
+        tmem_wait_ld();
+        float den = __uint_as_float(d[64]);
+#pragma unroll
+        for (int e = 0; e < kMaxNH; ++e)
+          if (e == hh) den += den_intra[e];
+        const float inv = 1.0f / den;
+        if (i_tok < args.T) {
+          uint4 *dst = reinterpret_cast<uint4 *>(
+              args.Y + (((size_t)bidx * args.Hq + h0 + hh) * args.T + i_tok) * kDv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(d[8 * e]) * inv, __uint_as_float(d[8 * e + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(d[8 * e + 2]) * inv, __uint_as_float(d[8 * e + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(d[8 * e + 4]) * inv, __uint_as_float(d[8 * e + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(d[8 * e + 6]) * inv, __uint_as_float(d[8 * e + 7]) * inv);
+            dst[e] = v;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kCtl) {
+    tc_fence_after();
+    tmem_dealloc(tb, 512);
+  }
+}
+
+// ================================================================= host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  return fn;
+}
+
+// 3-D bf16 tensor map: x (inner, contiguous) extent nx, y extent ny (row
+// pitch ybytes), z extent nz (pitch zbytes); box {64, by, 1}, 128B swizzle.
+static bool make_map3(CUtensorMap *m, const void *ptr, uint64_t nx, uint64_t ny, uint64_t nz,
+                      uint64_t ybytes, uint64_t zbytes, uint32_t by) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {nx, ny, nz};
+  cuuint64_t strides[2] = {ybytes, zbytes};
+  cuuint32_t box[3] = {64, by, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Layout {
+  int nC, nparts, cpp, U;
+  size_t snap_off, ptot_off, coef_off, plan_off, total;
+};
+
+static Layout plan_layout(int B, int Hq, int Hkv, int T) {
+  Layout L{};
+  L.U = B * Hkv;
+  L.nC = (T + kC - 1) / kC;
+  int P = (2 * 152 + kTiles * L.U - 1) / (kTiles * L.U);
+  P = P < 1 ? 1 : (P > L.nC ? L.nC : P);
+  L.cpp = (L.nC + P - 1) / P;
+  L.nparts = (L.nC + L.cpp - 1) / L.cpp;
+  auto al = [](size_t x) { return (x + 1023) & ~size_t(1023); };
+  size_t o = 0;
+  L.snap_off = o; o = al(o + (size_t)L.U * L.nC * kSnapBytes);
+  L.ptot_off = o; o = al(o + (size_t)L.U * L.nparts * kTiles * 128 * kN * sizeof(float));
+  L.coef_off = o; o = al(o + (size_t)Hq * kKP * 2);
+  L.plan_off = o; o = al(o + (size_t)Hq * sizeof(KPlan));
+  L.total = o;
+  return L;
+}
+
+using ReadoutKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, ReadArgs);
+static ReadoutKernel readout_kernel_for(int G) {
+  switch (G) {
+    case 1: return tc_readout_kernel<1>;
+    case 2: return tc_readout_kernel<2>;
+    case 3: return tc_readout_kernel<3>;
+    case 4: return tc_readout_kernel<4>;
+    case 5: return tc_readout_kernel<5>;
+    case 6: return tc_readout_kernel<6>;
+    default: return tc_readout_kernel<7>;
+  }
+}
+
+}  // namespace tcp
+
+size_t tc_prefill_workspace_bytes(int B, int Hq, int Hkv, int T) {
+  return tcp::plan_layout(B, Hq, Hkv, T).total;
+}
+
+oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B, int Hq,
+                             int Hkv, int T, const float *L, const int32_t *group, int G,
+                             float eps, const float *a, const float *b, const float *C,
+                             int packed, float *state, int cont, void *Y, void *ws,
+                             cudaStream_t stream) {
+  using namespace tcp;
+  const Layout lay = plan_layout(B, Hq, Hkv, T);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  __nv_bfloat16 *snap = reinterpret_cast<__nv_bfloat16 *>(w + lay.snap_off);
+  float *ptot = reinterpret_cast<float *>(w + lay.ptot_off);
+  __nv_bfloat16 *coef = reinterpret_cast<__nv_bfloat16 *>(w + lay.coef_off);
+  KPlan *plans = reinterpret_cast<KPlan *>(w + lay.plan_off);
+  int *status = oal_device_status_word();
+
+  CUtensorMap tmQ, tmK, tmV, tmS;
+  const uint64_t rowb = 64 * 2;
+  if (!make_map3(&tmQ, Q, 64, T, (uint64_t)B * Hq, rowb, rowb * T, kC) ||
+      !make_map3(&tmK, K, 64, T, (uint64_t)lay.U, rowb, rowb * T, kC) ||
+      !make_map3(&tmV, V, 64, T, (uint64_t)lay.U, rowb, rowb * T, kC) ||
+      !make_map3(&tmS, snap, kKP, kN, (uint64_t)lay.U * lay.nC, (uint64_t)kKP * 2, kSnapBytes,
+                 kN))
+    return oal_fail(OAL_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+
+  tc_prep_kernel<<<dim3(Hq, (kKP + 255) / 256), 256, 0, stream>>>(a, b, C, L, group, G, eps, packed, coef, plans, status);
+  oal_status st = oal_after_launch("tc_prep_kernel", stream);
+  if (st != OAL_OK) return st;
+
+  const size_t ssmem = sizeof(StateSmem) + 1024;
+  const size_t rsmem = sizeof(ReadSmem) + 1024;
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
+    cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
+    for (int g = 1; g <= kMaxG; ++g)
+      cudaFuncSetAttribute(readout_kernel_for(g), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)rsmem);
+    attr_dev = dev;
+  }
+  StateArgs sa;
+  sa.T = T; sa.nC = lay.nC; sa.U = lay.U; sa.cpp = lay.cpp; sa.nparts = lay.nparts;
+  sa.packed = packed; sa.cont = cont; sa.state_in = state; sa.state_out = state;
+  sa.ptot = ptot; sa.snap = snap; sa.status = status;
+  if (lay.nparts > 1) {
+    sa.mode = 0;
+    dim3 g0(kTiles, lay.nparts - 1, lay.U);
+    tc_state_kernel<<<g0, kStateThreads, ssmem, stream>>>(tmK, tmV, sa);
+    st = oal_after_launch("tc_state_kernel", stream);
+    if (st != OAL_OK) return st;
+  }
+  sa.mode = 1;
+  dim3 g1(kTiles, lay.nparts, lay.U);
+  tc_state_kernel<<<g1, kStateThreads, ssmem, stream>>>(tmK, tmV, sa);
+  st = oal_after_launch("tc_state_kernel", stream);
+  if (st != OAL_OK) return st;
+
+  ReadArgs ra;
+  ra.T = T; ra.nC = lay.nC; ra.Hq = Hq; ra.Hkv = Hkv; ra.rho = Hq / Hkv;
+  ra.nh_per_block = kMaxNH;
+  ra.Y = static_cast<__nv_bfloat16 *>(Y);
+  ra.coef = coef; ra.plans = plans; ra.status = status;
+  const int nhg = (ra.rho + kMaxNH - 1) / kMaxNH;
+  dim3 g2(nhg, lay.nC, lay.U);
+  readout_kernel_for(G)<<<g2, kReadThreads, rsmem, stream>>>(tmQ, tmK, tmV, tmS, ra);
+  return oal_after_launch("tc_readout_kernel", stream);
+}
+
+}  // namespace oal
