@@ -19,7 +19,9 @@
 namespace oal {
 namespace {
 
-static __constant__ PairTable c_pairs = make_pair_table();
+// In global memory, not __constant__: threads read different entries, which
+// the constant cache would serialize.
+static __device__ const PairTable c_pairs = make_pair_table();
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
@@ -59,7 +61,8 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     s_q[n / kD][n % kD] = to_f32(q[((size_t)bidx * Hq + h0) * kD + n]);
   __syncthreads();
 
-  // per-row weights: phi_f(k) and Phi~^h_f(q^h)
+  // per-row weights: phi_f(k) and Phi~^h_f(q^h); the table loads of all
+  // heads are issued before any is used
   const size_t ctab_len = packed ? kH2Packed : kH2Full;
   for (int n = tid; n < nrows; n += kThreads) {
     const int f = f0 + n;
@@ -73,13 +76,26 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
       else { r = nn >> 6; t = nn & 63; }
     }
     s_wk[n] = kind == 0 ? 1.f : (kind == 1 ? s_k[r] : s_k[r] * s_k[t]);
-    for (int hh = 0; hh < rho; ++hh) {
-      const int h = h0 + hh;
-      float w;
-      if (kind == 0) w = a[h];
-      else if (kind == 1) w = b[(size_t)h * kD + r] * s_q[hh][r] * 0.125f;
-      else w = Ctab[(size_t)h * ctab_len + (f - 1 - kD)] * s_q[hh][r] * s_q[hh][t] * 0.015625f;
-      s_wq[hh][n] = w;
+    float coef[kMaxRho];
+#pragma unroll
+    for (int hh = 0; hh < kMaxRho; ++hh) {
+      coef[hh] = 0.f;
+      if (hh < rho) {
+        const int h = h0 + hh;
+        coef[hh] = kind == 0 ? __ldg(a + h)
+                 : (kind == 1 ? __ldg(b + (size_t)h * kD + r)
+                              : __ldg(Ctab + (size_t)h * ctab_len + (f - 1 - kD)));
+      }
+    }
+#pragma unroll
+    for (int hh = 0; hh < kMaxRho; ++hh) {
+      if (hh < rho) {
+        float w;
+        if (kind == 0) w = coef[hh];
+        else if (kind == 1) w = coef[hh] * s_q[hh][r] * 0.125f;
+        else w = coef[hh] * s_q[hh][r] * s_q[hh][t] * 0.015625f;
+        s_wq[hh][n] = w;
+      }
     }
   }
   __syncthreads();

@@ -13,7 +13,9 @@
 
 namespace oal {
 
-__constant__ PairTable c_pairs = make_pair_table();
+// In global memory, not __constant__: threads read different entries, which
+// the constant cache would serialize.
+static __device__ const PairTable c_pairs = make_pair_table();
 
 __global__ void expand_coeffs_kernel(const float *__restrict__ L,
                                      const int32_t *__restrict__ group, int G,
@@ -42,21 +44,27 @@ __global__ void expand_coeffs_kernel(const float *__restrict__ L,
     grp[r] = g;
   }
   __syncthreads();
+  // fp32 images of M and 2M (each conversion rounds once, to nearest even)
+  __shared__ float Mf[(kMaxG + 1) * (kMaxG + 1)], M2f[(kMaxG + 1) * (kMaxG + 1)];
+  for (int n = threadIdx.x; n < G1 * G1; n += blockDim.x) {
+    Mf[n] = __double2float_rn(M[n]);
+    M2f[n] = __double2float_rn(__dmul_rn(2.0, M[n]));
+  }
+  __syncthreads();
   if (threadIdx.x == 0) a[h] = __double2float_rn(__dadd_rn((double)eps, M[0]));
-  for (int r = threadIdx.x; r < kD; r += blockDim.x)
-    b[(size_t)h * kD + r] = __double2float_rn(__dmul_rn(2.0, M[grp[r]]));
+  for (int r = threadIdx.x; r < kD; r += blockDim.x) b[(size_t)h * kD + r] = M2f[grp[r]];
   if (!packed) {
     float *Ch = C + (size_t)h * kH2Full;
     for (int n = threadIdx.x; n < kH2Full; n += blockDim.x) {
       const int r = n / kD, t = n % kD;
-      Ch[n] = __double2float_rn(M[grp[r] * G1 + grp[t]]);
+      Ch[n] = Mf[grp[r] * G1 + grp[t]];
     }
   } else {
     float *Ch = C + (size_t)h * kH2Packed;
     for (int n = threadIdx.x; n < kH2Packed; n += blockDim.x) {
       const int r = c_pairs.rt[n] >> 8, t = c_pairs.rt[n] & 0xff;
-      const double m = M[grp[r] * G1 + grp[t]];
-      Ch[n] = __double2float_rn(r == t ? m : __dmul_rn(2.0, m));
+      const int idx = grp[r] * G1 + grp[t];
+      Ch[n] = r == t ? Mf[idx] : M2f[idx];
     }
   }
 }

@@ -17,7 +17,9 @@
 namespace oal {
 namespace {
 
-static __constant__ PairTable c_pairs = make_pair_table();
+// In global memory, not __constant__: threads read different entries, which
+// the constant cache would serialize.
+static __device__ const PairTable c_pairs = make_pair_table();
 
 constexpr int kThreads = 256;
 constexpr int kTile = 64;     // feature rows / query rows per block

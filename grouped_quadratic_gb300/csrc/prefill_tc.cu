@@ -57,6 +57,7 @@ constexpr int kNKB = 35;         // readout K blocks of 64 (the last one has K =
 constexpr int kTiles = 18;       // 128-feature tiles of the state kernel
 constexpr int kN = 80;           // snapshot rows: 64 value columns, the "1" column, 15 zeros
 constexpr int kMaxNH = 4;        // query heads per readout block
+constexpr int kIntraNH = 1;      // query heads per intra-chunk block
 constexpr int kMaxTailG = 6;     // tail groups (G - 1 <= 6)
 constexpr size_t kSnapBytes = (size_t)kN * kKP * 2;   // 350,720 B per (unit, chunk)
 
@@ -120,6 +121,11 @@ struct KPlan {
   float alpha[8];
   float beta[kMaxTailG][8];
   float L00, eps;
+  // kappa as a quadratic form in z = (s, tail sums), Horner order:
+  // kappa = max(eps, c0 + sum_v z_v (lin_v + sum_{w >= v} quad[v, w] z_w))
+  float c0;
+  float lin[8];
+  float quad[36];
   int ntg;                     // tail groups (G - 1)
   int nd[kMaxTailG];           // dims per tail group
   int dims[kMaxTailG][2];      // the dims when nd <= 2 (fast path)
@@ -213,6 +219,52 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
     P->eps = eps;
     P->G = G;
   }
+  // quadratic form, one entry per thread: sbar_g = sum_v A[g][v] z_v with
+  // z_0 = s, z_i = tail sum i; sbar_{g*} = (z_0 - sum_i z_i) / 8,
+  // sbar_{g_i} = z_i / 8; M = L L^T.  A[g][v] is formed on the fly.
+  __shared__ int slot_group[8];     // tail slot -> group
+  if (tid == 0) {
+    int slot = 0;
+    for (int g = 1; g <= G; ++g)
+      if (g != gstar) slot_group[++slot] = g;   // z index slot (1-based)
+  }
+  __syncthreads();
+  auto Aat = [&](int g, int v) -> double {     // d sbar_g / d z_v
+    if (v == 0) return g == gstar ? 0.125 : 0.0;
+    if (g == gstar) return -0.125;
+    return slot_group[v] == g ? 0.125 : 0.0;
+  };
+  auto Mat = [&](int g, int h2) -> double {
+    double m = 0.0;
+    for (int c = 0; c <= (g < h2 ? g : h2); ++c) m += (double)Lat(g, c) * (double)Lat(h2, c);
+    return m;
+  };
+  const int nq = G * (G + 1) / 2;
+  if (tid < nq) {
+    int v = 0, rem = tid;
+    while (rem >= G - v) { rem -= G - v; ++v; }
+    const int w2 = v + rem;
+    double q = 0.0;
+    for (int g = 1; g <= G; ++g) {
+      const double ag = Aat(g, v);
+      if (ag == 0.0) continue;
+      for (int h2 = 1; h2 <= G; ++h2) {
+        const double ah = Aat(h2, w2);
+        if (ah != 0.0) q += ag * Mat(g, h2) * ah;
+      }
+    }
+    P->quad[tid] = (float)(w2 == v ? q : 2.0 * q);
+  } else if (tid < 36) {
+    P->quad[tid] = 0.f;
+  } else if (tid >= 64 && tid < 72) {
+    const int v = tid - 64;
+    double l = 0.0;
+    if (v < G)
+      for (int g = 1; g <= G; ++g) l += 2.0 * Mat(0, g) * Aat(g, v);
+    P->lin[v] = (float)l;
+  } else if (tid == 96) {
+    P->c0 = (float)((double)eps + Mat(0, 0));
+  }
 }
 
 // ---------------------------------------------------------------- swizzle helpers
@@ -249,7 +301,8 @@ constexpr int kStateStages = 3;
 struct __align__(1024) StateSmem {
   __nv_bfloat16 kv[kStateStages][2][kC * 64];   // [stage][K | V] 128B-swizzled tiles
   __nv_bfloat16 ones[kC * 64];                  // MN-major B tile whose column 0 is 1
-  __nv_bfloat16 kT[64][kC + 8];                 // K transposed: [dim][token]
+  // K transposed, [dim][token]; the 16-byte chunk c of row r sits at c ^ (r >> 3)
+  __nv_bfloat16 kT[64][kC];
   uint64_t kv_full[kStateStages], kv_empty[kStateStages];
   uint64_t a_full[2], a_empty[2], d_full[2], d_empty[2];
   uint32_t tmem_base;
@@ -297,8 +350,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.a_full[i], 4);
-      mbar_init(&s.a_empty[i], 1);
-      mbar_init(&s.d_full[i], 1);
+      mbar_init(&s.a_empty[i], 2);   // both issuers
+      mbar_init(&s.d_full[i], 2);    // both issuers
       mbar_init(&s.d_empty[i], 4);
     }
     fence_mbar_init();
@@ -343,28 +396,28 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
         mbar_wait_teardown(&s.kv_full[i % kStateStages], (i / kStateStages) & 1, args.status);
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
     if (lane == 0) {
-      // ---------------- MMA issuer
-      const uint32_t idv = idesc_bf16_f32(128, 64, 1);
-      const uint32_t id1 = idesc_bf16_f32(128, 16, 1);
-      const uint32_t oaddr = smem_u32(s.ones);
+      // ---------------- MMA issuers: warp 1 D[:, 0:64] += A x V_c (N = 64),
+      // warp 2 D[:, 64:80] += A x [1] (N = 16); A = phi(K_c)^T as hi | lo, K = 256
+      const bool vpart = warp == 1;
+      const uint32_t idn = vpart ? idesc_bf16_f32(128, 64, 1) : idesc_bf16_f32(128, 16, 1);
+      const uint64_t vdesc0 = sdesc_sw128(smem_u32(s.kv[0][1]), 16, 1024);
+      const uint64_t odesc = sdesc_sw128(smem_u32(s.ones), 16, 1024);
+      constexpr uint64_t kKVStep = (2 * kC * 64 * 2) >> 4;   // one K|V stage
       for (int i = 0; i < nchunks; ++i) {
         const int sl = i & 1, st = i % kStateStages;
         if (!mbar_wait(&s.a_full[sl], (i >> 1) & 1, abort_flag, args.status)) break;
         if (!mbar_wait(&s.d_empty[sl], ((i >> 1) & 1) ^ 1, abort_flag, args.status)) break;
         tc_fence_after();
-        const uint32_t vaddr = smem_u32(s.kv[st][1]);
-        const uint32_t d = tb + kStateD + 128 * sl;
-        for (int k = 0; k < 16; ++k) {     // K = 256: hi half then lo half
-          const uint32_t acc = k > 0 ? 1u : 0u;
-          const uint32_t at = tb + kStateA + 128 * sl + 8 * k;
-          const uint32_t brow = 2048 * (k & 7);
-          umma_ts(d, at, sdesc_sw128(vaddr + brow, 16, 1024), idv, acc);
-          umma_ts(d + 64, at, sdesc_sw128(oaddr + brow, 16, 1024), id1, acc);
-        }
+        const uint64_t bd = vpart ? vdesc0 + kKVStep * st : odesc;
+        const uint32_t d = tb + kStateD + 128 * sl + (vpart ? 0 : 64);
+        const uint32_t a0 = tb + kStateA + 128 * sl;
+#pragma unroll
+        for (int k = 0; k < 16; ++k)       // K = 256: hi half then lo half
+          umma_ts(d, a0 + 8 * k, bd + (uint64_t)(128 * (k & 7)), idn, k > 0 ? 1u : 0u);
         umma_commit(&s.a_empty[sl]);
-        umma_commit(&s.kv_empty[st]);
+        if (vpart) umma_commit(&s.kv_empty[st]);
         umma_commit(&s.d_full[sl]);
       }
       // no MMA in flight at dealloc: drain through the accumulator barriers
@@ -383,20 +436,30 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       if (!mbar_wait(&s.kv_full[st], (i / kStateStages) & 1, abort_flag, args.status)) break;
       named_bar(1, 128);   // the previous chunk's builds are done with kT
       {
-        const uint8_t *krow = reinterpret_cast<const uint8_t *>(s.kv[st][0]);
+        // 8 x 8 block transpose: thread (tb8, db8) moves tokens 8 tb8 .. +7 x
+        // dims 8 db8 .. +7 from the K tile into kT with 16-byte accesses
+        const int tb8 = l >> 3, db8 = l & 7;
+        const uint8_t *ktile = reinterpret_cast<const uint8_t *>(s.kv[st][0]);
+        uint32_t v[8][4];
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(krow + sw128(l, cc));
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        for (int t = 0; t < 8; ++t) {
+          const uint4 x = *reinterpret_cast<const uint4 *>(ktile + sw128(8 * tb8 + t, db8));
+          v[t][0] = x.x; v[t][1] = x.y; v[t][2] = x.z; v[t][3] = x.w;
+        }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int dd = cc * 8 + 2 * e;
-            reinterpret_cast<uint16_t *>(&s.kT[dd][0])[l] = (uint16_t)(w[e] & 0xffff);
-            reinterpret_cast<uint16_t *>(&s.kT[dd + 1][0])[l] = (uint16_t)(w[e] >> 16);
-          }
+        for (int j = 0; j < 4; ++j) {          // dims 2j, 2j+1 of the block
+          uint4 lo, hi;
+          lo.x = __byte_perm(v[0][j], v[1][j], 0x5410); hi.x = __byte_perm(v[0][j], v[1][j], 0x7632);
+          lo.y = __byte_perm(v[2][j], v[3][j], 0x5410); hi.y = __byte_perm(v[2][j], v[3][j], 0x7632);
+          lo.z = __byte_perm(v[4][j], v[5][j], 0x5410); hi.z = __byte_perm(v[4][j], v[5][j], 0x7632);
+          lo.w = __byte_perm(v[6][j], v[7][j], 0x5410); hi.w = __byte_perm(v[6][j], v[7][j], 0x7632);
+          const int r0 = 8 * db8 + 2 * j;
+          *reinterpret_cast<uint4 *>(&s.kT[r0][8 * (tb8 ^ db8)]) = lo;
+          *reinterpret_cast<uint4 *>(&s.kT[r0 + 1][8 * (tb8 ^ db8)]) = hi;
         }
       }
       named_bar(1, 128);
+      // slot sl (A in tensor memory) is free once the UMMAs of chunk i - 2 are done
       if (!mbar_wait(&s.a_empty[sl], ((i >> 1) & 1) ^ 1, abort_flag, args.status)) break;
       const int nvalid = min(kC, args.T - c * kC);
       const uint32_t abase = kStateA + 128 * sl;
@@ -414,19 +477,21 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
             lo[w] = 0u;
           }
         } else if (code & 0x8000) {
-          const uint4 *kr = reinterpret_cast<const uint4 *>(&s.kT[code & 0xff][32 * q]);
+          const int rr = code & 0xff;
+          const uint4 *kr = reinterpret_cast<const uint4 *>(&s.kT[rr][0]);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const uint4 x = kr[v];
+            const uint4 x = kr[(4 * q + v) ^ (rr >> 3)];
             hi[4 * v] = x.x; hi[4 * v + 1] = x.y; hi[4 * v + 2] = x.z; hi[4 * v + 3] = x.w;
             lo[4 * v] = lo[4 * v + 1] = lo[4 * v + 2] = lo[4 * v + 3] = 0u;
           }
         } else {
-          const uint4 *kr = reinterpret_cast<const uint4 *>(&s.kT[code >> 8][32 * q]);
-          const uint4 *kt = reinterpret_cast<const uint4 *>(&s.kT[code & 0xff][32 * q]);
+          const int rr = code >> 8, tt = code & 0xff;
+          const uint4 *kr = reinterpret_cast<const uint4 *>(&s.kT[rr][0]);
+          const uint4 *kt = reinterpret_cast<const uint4 *>(&s.kT[tt][0]);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const uint4 x = kr[v], y = kt[v];
+            const uint4 x = kr[(4 * q + v) ^ (rr >> 3)], y = kt[(4 * q + v) ^ (tt >> 3)];
             const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -534,37 +599,49 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
 
 // ================================================================= readout kernel
 constexpr int kNB = 6;           // snapshot K-block stages
-constexpr int kNA = 4;           // A slots in tensor memory
+constexpr int kNA = 6;           // A slots in tensor memory
 constexpr int kTailSlots = 2 * kMaxTailG;
 
 struct __align__(1024) ReadSmem {
   __nv_bfloat16 q[kMaxNH][kC * 64];    // 128B-swizzled [token][dim]
-  __nv_bfloat16 k[kC * 64];
-  __nv_bfloat16 v[kC * 64];
   __nv_bfloat16 b[kNB][kN * 64];       // snapshot K blocks [n][64 features]
   __nv_bfloat16 coef[kMaxNH][kKP];
-  float kt[kMaxNH][kC][kTailSlots];    // tail-dim key values (fast path)
-  KPlan plan[kMaxNH];
-  uint64_t qkv_full, b_full[kNB], b_empty[kNB], a_full[kNA], a_empty[kNA];
-  uint64_t s_full, p_full, s_free, d_full;
+  uint64_t qkv_full, b_full[kNB], b_empty[kNB], a_full[kNA], a_empty[kNA], d_full;
   uint32_t tmem_base;
   int abort_flag;
 };
-
 static_assert(sizeof(ReadSmem) + 1024 <= 227 * 1024, "readout shared memory");
+
+struct __align__(1024) IntraSmem {
+  __nv_bfloat16 q[kIntraNH][kC * 64];
+  __nv_bfloat16 k[kC * 64];
+  __nv_bfloat16 v[kC * 64];
+  float kt[kIntraNH][kC][kTailSlots];  // tail-dim key values (fast path)
+  KPlan plan[kIntraNH];
+  uint64_t qkv_full, s_full[2], p_full[2], s_free[2], d_full;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(IntraSmem) + 1024 <= 56 * 1024, "four intra blocks per SM");
 
 struct ReadArgs {
   int T, nC, Hq, Hkv, rho, nh_per_block;
   __nv_bfloat16 *Y;
+  float *intra_num;            // [B*Hq][T][64] intra-chunk numerators
+  float *intra_den;            // [B*Hq][T]     intra-chunk denominators
   const __nv_bfloat16 *coef;   // [Hq][kKP]
   const KPlan *plans;          // [Hq]
   int *status;
 };
 
-constexpr int kReadThreads = 416;   // 13 warps
+constexpr int kReadThreads = 512;   // 16 warps
 constexpr int kTmemD = 0;         // D^h at [80h, 80h + 80)
-constexpr int kTmemA = 320;       // A slots [320, 448)
-constexpr int kTmemS = 448;       // s / P tile [448, 512)
+constexpr int kTmemA = 320;       // six A slots of 32 columns at [320, 512)
+constexpr uint32_t kReadTmemCols = 512;
+constexpr int kIntraThreads = 192;  // 6 warps
+constexpr int kTmemS = 0;         // intra kernel: two 32-key s / P sub-tiles at 0 and 32
+constexpr int kTmemI = 64;        // intra kernel: numerators at [64, 128)
+constexpr uint32_t kIntraTmemCols = 128;  // up to four intra blocks per SM
 
 // ---- readout A block builders (compile-time feature layout)
 template <int KB, int P>
@@ -628,26 +705,31 @@ __device__ __forceinline__ float bf16_at(const __nv_bfloat16 *tile, int row, int
 // Fast path: every tail group has <= 2 dims, constants in registers.
 template <int G>
 struct KConst {
-  float alpha[G + 1];
-  float beta[G > 1 ? G - 1 : 1][G + 1];
-  float L00, eps;
+  float c0, eps;
+  float lin[G];
+  float quad[G * (G + 1) / 2];
 };
 
+// kappa of one pair from s = q.k and the tail-group sums (fast path: every
+// tail group has <= 2 dims).  qt: this query's tail values; ktj: the key's.
 template <int G>
 __device__ __forceinline__ float kappa_g(const KConst<G> &k, float s, const float (&qt)[2 * kMaxTailG],
                                          const float *ktj) {
-  float sg[G > 1 ? G - 1 : 1];
+  float z[G];
+  z[0] = s;
 #pragma unroll
-  for (int g = 0; g < G - 1; ++g) sg[g] = fmaf(qt[2 * g], ktj[2 * g], qt[2 * g + 1] * ktj[2 * g + 1]);
-  float kap = k.eps;
+  for (int g = 1; g < G; ++g)
+    z[g] = fmaf(qt[2 * g - 2], ktj[2 * g - 2], qt[2 * g - 1] * ktj[2 * g - 1]);
+  float kap = k.c0;
+  int qi = 0;
 #pragma unroll
-  for (int c = 0; c <= G; ++c) {
-    float w = fmaf(k.alpha[c], s, c == 0 ? k.L00 : 0.f);
+  for (int v = 0; v < G; ++v) {
+    float inner = k.lin[v];
 #pragma unroll
-    for (int g = 0; g < G - 1; ++g) w = fmaf(k.beta[g][c], sg[g], w);
-    kap = fmaf(w, w, kap);
+    for (int w = v; w < G; ++w) inner = fmaf(k.quad[qi++], z[w], inner);
+    kap = fmaf(z[v], inner, kap);
   }
-  return kap;
+  return fmaxf(kap, k.eps);
 }
 
 // Generic path (a tail group with more than 2 dims): sums straight from the
@@ -671,15 +753,17 @@ __device__ float kappa_generic(const KPlan &p, float s, const __nv_bfloat16 *qti
   return kap;
 }
 
-// The intra-chunk role: for each head and each half of the key range, read
-// s = q.k for this thread's query row from tensor memory, turn it into
-// kappa (masked to keys j <= i), write P (bf16) back in place for the P.V
-// UMMA, and accumulate the denominator from the same rounded weights.
+// The intra-chunk role (warps 0-3, thread = query row): for each head and
+// each 32-key block of the chunk, read s = q.k of this row from tensor
+// memory, turn it into kappa (masked to keys j <= i), write P (bf16) back in
+// place for the P.V UMMA, and accumulate the denominator from the same
+// rounded weights.  The two 32-key sub-tiles alternate, so the UMMAs of one
+// block overlap the kappa work of the next.
 template <int G>
-__device__ bool intra_worker(ReadSmem &s, const ReadArgs &args, int c, int nh, int warp, int lane,
-                             uint32_t tb, float (&den_intra)[kMaxNH]) {
+__device__ bool intra_worker(IntraSmem &s, const ReadArgs &args, int nh, int warp, int lane,
+                             uint32_t tb, float (&den_intra)[kIntraNH]) {
   volatile int *abort_flag = &s.abort_flag;
-  const int m = threadIdx.x;                      // query row (TMEM lane), warps 0-3
+  const int m = threadIdx.x;
   if (!mbar_wait(&s.qkv_full, 0, abort_flag, args.status)) return false;
   // tail-dim key values of every head (fast path); thread = key row m
   for (int hh = 0; hh < nh; ++hh) {
@@ -695,18 +779,15 @@ __device__ bool intra_worker(ReadSmem &s, const ReadArgs &args, int c, int nh, i
   }
   named_bar(2, 128);
   const int row_max = 32 * (warp & 3) + 31;       // largest query row of this warp
-  for (int it = 0; it < 2 * nh; ++it) {
-    const int hh = it >> 1, half = it & 1;
+  for (int hh = 0; hh < nh; ++hh) {
     const KPlan &p = s.plan[hh];
     KConst<G> kc;
-#pragma unroll
-    for (int cc = 0; cc <= G; ++cc) {
-      kc.alpha[cc] = p.alpha[cc];
-#pragma unroll
-      for (int g = 0; g < G - 1; ++g) kc.beta[g][cc] = p.beta[g][cc];
-    }
-    kc.L00 = p.L00;
+    kc.c0 = p.c0;
     kc.eps = p.eps;
+#pragma unroll
+    for (int v = 0; v < G; ++v) kc.lin[v] = p.lin[v];
+#pragma unroll
+    for (int i = 0; i < G * (G + 1) / 2; ++i) kc.quad[i] = p.quad[i];
     float qt[2 * kMaxTailG];
 #pragma unroll
     for (int g = 0; g < kMaxTailG; ++g) {
@@ -714,29 +795,31 @@ __device__ bool intra_worker(ReadSmem &s, const ReadArgs &args, int c, int nh, i
       qt[2 * g + 1] = (g < p.ntg && p.nd[g] > 1) ? bf16_at(s.q[hh], m, p.dims[g][1]) : 0.f;
     }
     const bool fast = p.fast != 0;
-    if (!mbar_wait(&s.s_full, it & 1, abort_flag, args.status)) return false;
-    tc_fence_after();
     float dsum = 0.f;
-#pragma unroll 1
-    for (int sb = 0; sb < 2; ++sb) {            // 32-key sub-blocks
-      const int jbase = half * 64 + sb * 32;
+    for (int kb = 0; kb < 4; ++kb) {
+      const int it = hh * 4 + kb, buf = it & 1;
+      const uint32_t col = kTmemS + 32 * buf;
+      if (!mbar_wait(&s.s_full[buf], (it >> 1) & 1, abort_flag, args.status)) return false;
+      tc_fence_after();
+      const int jbase = 32 * kb;
       uint32_t pk[16];
       if (row_max >= jbase) {
         uint32_t sv[32];
         uint32_t r0[16], r1[16];
-        tmem_ld16(tmem_lane_addr(tb, warp, kTmemS + 32 * sb), r0);
-        tmem_ld16(tmem_lane_addr(tb, warp, kTmemS + 32 * sb + 16), r1);
+        tmem_ld16(tmem_lane_addr(tb, warp, col), r0);
+        tmem_ld16(tmem_lane_addr(tb, warp, col + 16), r1);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 16; ++e) { sv[e] = r0[e]; sv[16 + e] = r1[e]; }
         if (fast) {
+          // branch-free: every key is evaluated, the causal mask is a select,
+          // so the 32 independent evaluations interleave
 #pragma unroll
           for (int jj = 0; jj < 32; jj += 2) {
-            float kv0 = 0.f, kv1 = 0.f;
             const int j0 = jbase + jj;
-            if (j0 <= m) kv0 = kappa_g<G>(kc, __uint_as_float(sv[jj]), qt, s.kt[hh][j0]);
-            if (j0 + 1 <= m) kv1 = kappa_g<G>(kc, __uint_as_float(sv[jj + 1]), qt, s.kt[hh][j0 + 1]);
-            pk[jj >> 1] = pack_bf16x2(kv0, kv1);
+            const float k0 = kappa_g<G>(kc, __uint_as_float(sv[jj]), qt, s.kt[hh][j0]);
+            const float k1 = kappa_g<G>(kc, __uint_as_float(sv[jj + 1]), qt, s.kt[hh][j0 + 1]);
+            pk[jj >> 1] = pack_bf16x2(j0 <= m ? k0 : 0.f, j0 + 1 <= m ? k1 : 0.f);
           }
         } else {
           float sl[32];
@@ -758,59 +841,57 @@ __device__ bool intra_worker(ReadSmem &s, const ReadArgs &args, int c, int nh, i
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = 0u;
       }
-      // P for keys [jbase, jbase + 32) -> columns [16 sb, 16 sb + 16) of the
-      // tile (s of those columns has already been read)
-      tmem_st16(tmem_lane_addr(tb, warp, kTmemS + 16 * sb), pk);
+      // P for these 32 keys -> the first 16 columns of the sub-tile (their s
+      // values are already in registers)
+      tmem_st16(tmem_lane_addr(tb, warp, col), pk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.p_full[buf]);
     }
 #pragma unroll
-    for (int e = 0; e < kMaxNH; ++e)
+    for (int e = 0; e < kIntraNH; ++e)
       if (e == hh) den_intra[e] += dsum;
-    tmem_wait_st();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&s.p_full);
   }
   return true;
 }
 
+// ---------------------------------------------------------------- intra kernel
+// Intra-chunk part of Eq. (25): sum_{j in chunk, j <= i} kappa(q_i, k_j) u_j per
+// query row, written to workspace for the readout's epilogue.
+// Warps 0-3: kappa (thread = query row) and the epilogue; warp 4: UMMA issue
+// (s = Q K^T per 32-key block, then P.V) and tensor memory; warp 5: TMA.
 template <int G>
-__global__ void __launch_bounds__(kReadThreads, 1)
-tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmS,
-                  ReadArgs args) {
+__global__ void __launch_bounds__(kIntraThreads, 2)
+tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, ReadArgs args) {
   extern __shared__ uint8_t smem_raw[];
-  ReadSmem &s = *reinterpret_cast<ReadSmem *>(
+  IntraSmem &s = *reinterpret_cast<IntraSmem *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int hg = blockIdx.x, c = blockIdx.y, unit = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bidx = unit / args.Hkv, kv = unit % args.Hkv;
-  const int h0 = kv * args.rho + hg * args.nh_per_block;
-  const int nh = min(args.nh_per_block, args.rho - hg * args.nh_per_block);
-  const int njobs = kNKB * nh;
-  constexpr int kCtl = 12;        // control warp: TMEM, TMA, UMMA issue
+  const int h0 = kv * args.rho + hg * kIntraNH;
+  const int nh = min(kIntraNH, args.rho - hg * kIntraNH);
+  const int nsteps = 4 * nh;            // (head, 32-key block)
+  constexpr int kIss = 4, kTma = 5;
 
   if (tid == 0) {
     s.abort_flag = 0;
     mbar_init(&s.qkv_full, 1);
-    for (int i = 0; i < kNB; ++i) { mbar_init(&s.b_full[i], 1); mbar_init(&s.b_empty[i], 1); }
-    for (int i = 0; i < kNA; ++i) { mbar_init(&s.a_full[i], 4); mbar_init(&s.a_empty[i], 1); }
-    mbar_init(&s.s_full, 1);
-    mbar_init(&s.p_full, 4);
-    mbar_init(&s.s_free, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.p_full[i], 4);
+      mbar_init(&s.s_free[i], 1);
+    }
     mbar_init(&s.d_full, 1);
     fence_mbar_init();
   }
-  if (warp == kCtl) {
-    tmem_alloc(&s.tmem_base, 512);
+  if (warp == kIss) {
+    tmem_alloc(&s.tmem_base, kIntraTmemCols);
     tmem_relinquish();
   }
-  // per-head readout weights and kappa constants into shared memory
-  for (int n = tid; n < nh * (kKP / 8); n += kReadThreads) {
-    const int hh = n / (kKP / 8), e = n % (kKP / 8);
-    reinterpret_cast<uint4 *>(s.coef[hh])[e] =
-        reinterpret_cast<const uint4 *>(args.coef + (size_t)(h0 + hh) * kKP)[e];
-  }
-  for (int n = tid; n < nh * (int)(sizeof(KPlan) / 4); n += kReadThreads) {
+  for (int n = tid; n < nh * (int)(sizeof(KPlan) / 4); n += kIntraThreads) {
     const int hh = n / (sizeof(KPlan) / 4), e = n % (sizeof(KPlan) / 4);
     reinterpret_cast<int *>(&s.plan[hh])[e] =
         reinterpret_cast<const int *>(&args.plans[h0 + hh])[e];
@@ -821,118 +902,245 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   const uint32_t tb = s.tmem_base;
   volatile int *abort_flag = &s.abort_flag;
 
-  if (warp == kCtl) {
+  if (warp == kIss) {
     if (lane == 0) {
-      // ---------------- control: TMA loads and the UMMA issue schedule
+      const uint32_t id32k = idesc_bf16_f32(128, 32, 0);
+      const uint32_t id64mn = idesc_bf16_f32(128, 64, 1);
+      const uint64_t qdesc0 = sdesc_sw128(smem_u32(s.q[0]), 16, 1024);
+      constexpr uint64_t kQStep = (kC * 64 * 2) >> 4;       // one Q tile
+      const uint64_t kdesc0 = sdesc_sw128(smem_u32(s.k), 16, 1024);
+      const uint64_t vdesc0 = sdesc_sw128(smem_u32(s.v), 16, 1024);
+      auto issue_s = [&](int it) {
+        const int hh = it >> 2, kb = it & 3;
+        const uint64_t qd = qdesc0 + kQStep * hh;
+        const uint64_t kd = kdesc0 + (uint64_t)((32 * kb * 128) >> 4);
+        const uint32_t dt = tb + kTmemS + 32 * (it & 1);
+        umma_ss(dt, qd, kd, id32k, 0u);
+        umma_ss(dt, qd + 2, kd + 2, id32k, 1u);
+        umma_ss(dt, qd + 4, kd + 4, id32k, 1u);
+        umma_ss(dt, qd + 6, kd + 6, id32k, 1u);
+        umma_commit(&s.s_full[it & 1]);
+      };
+      bool ok = mbar_wait(&s.qkv_full, 0, abort_flag, args.status);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        if (nsteps > 1) issue_s(1);
+      }
+      for (int it = 0; it < nsteps && ok; ++it) {
+        if (!mbar_wait(&s.p_full[it & 1], (it >> 1) & 1, abort_flag, args.status)) break;
+        tc_fence_after();
+        const int hh = it >> 2, kb = it & 3;
+        const uint32_t at = tb + kTmemS + 32 * (it & 1);
+        const uint64_t vd = vdesc0 + (uint64_t)((32 * kb * 128) >> 4);
+        const uint32_t dt = tb + kTmemI + 64 * hh;
+        umma_ts(dt, at, vd, id64mn, kb > 0 ? 1u : 0u);
+        umma_ts(dt, at + 8, vd + (2048 >> 4), id64mn, 1u);
+        umma_commit(&s.s_free[it & 1]);
+        if (it + 2 < nsteps) {
+          if (!mbar_wait(&s.s_free[it & 1], (it >> 1) & 1, abort_flag, args.status)) break;
+          tc_fence_after();
+          issue_s(it + 2);
+        }
+      }
+      umma_commit(&s.d_full);
+      mbar_wait_teardown(&s.d_full, 0, args.status);   // no MMA in flight at exit
+    }
+    __syncwarp();
+  } else if (warp == kTma) {
+    if (lane == 0) {
       tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmS);
       mbar_arrive_expect_tx(&s.qkv_full, (uint32_t)(nh + 2) * kC * 64 * 2);
       for (int hh = 0; hh < nh; ++hh)
         tma_load_3d(s.q[hh], &tmQ, &s.qkv_full, 0, c * kC, bidx * args.Hq + h0 + hh);
       tma_load_3d(s.k, &tmK, &s.qkv_full, 0, c * kC, unit);
       tma_load_3d(s.v, &tmV, &s.qkv_full, 0, c * kC, unit);
+      mbar_wait_teardown(&s.qkv_full, 0, args.status);
+    }
+    __syncwarp();
+  } else {
+    // warps 0-3: kappa, then the numerators and denominators to workspace
+    float den_intra[kIntraNH] = {0.f};
+    const bool ok = intra_worker<G>(s, args, nh, warp, lane, tb, den_intra);
+    const int m = tid;
+    const int i_tok = c * kC + m;
+    if (ok && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
+      tc_fence_after();
+      for (int hh = 0; hh < nh; ++hh) {
+        uint32_t d[64];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t r[16];
+          tmem_ld16(tmem_lane_addr(tb, warp, kTmemI + 64 * hh + 16 * q4), r);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) d[16 * q4 + e] = r[e];
+        }
+        tmem_wait_ld();
+        float dsum = 0.f;
+#pragma unroll
+        for (int e = 0; e < kIntraNH; ++e)
+          if (e == hh) dsum = den_intra[e];
+        if (i_tok < args.T) {
+          const size_t row = ((size_t)bidx * args.Hq + h0 + hh) * args.T + i_tok;
+          uint4 *dst = reinterpret_cast<uint4 *>(args.intra_num + row * 64);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) dst[e] = make_uint4(d[4 * e], d[4 * e + 1], d[4 * e + 2], d[4 * e + 3]);
+          args.intra_den[row] = dsum;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kIss) {
+    tc_fence_after();
+    tmem_dealloc(tb, kIntraTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- readout kernel
+// Warp roles (16 warps):
+//   0-11   readout A builders, three warps per tensor-memory lane quarter
+//          (group g = warp / 4 builds jobs g, g + 3, ...); warps 0-3 then run
+//          the epilogue
+//   12, 13 readout UMMA issuers (jobs of even / odd index)
+//   14     tensor memory owner
+//   15     TMA producer
+// The accumulators are zeroed first and every UMMA accumulates, so the two
+// issuers need no ordering between them.
+__global__ void __launch_bounds__(kReadThreads, 1)
+tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS,
+                  ReadArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  ReadSmem &s = *reinterpret_cast<ReadSmem *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int hg = blockIdx.x, c = blockIdx.y, unit = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bidx = unit / args.Hkv, kv = unit % args.Hkv;
+  const int h0 = kv * args.rho + hg * args.nh_per_block;
+  const int nh = min(args.nh_per_block, args.rho - hg * args.nh_per_block);
+  const int njobs = kNKB * nh;
+  constexpr int kIss0 = 12, kMem = 14, kTma = 15;
+
+  if (tid == 0) {
+    s.abort_flag = 0;
+    mbar_init(&s.qkv_full, 1);
+    for (int i = 0; i < kNB; ++i) {
+      mbar_init(&s.b_full[i], 1);
+      mbar_init(&s.b_empty[i], nh >= 2 ? 2 : 1);   // one commit per readout issuer
+    }
+    for (int i = 0; i < kNA; ++i) { mbar_init(&s.a_full[i], 4); mbar_init(&s.a_empty[i], 1); }
+    mbar_init(&s.d_full, 2);                       // both issuers done
+    fence_mbar_init();
+  }
+  if (warp == kMem) {
+    tmem_alloc(&s.tmem_base, kReadTmemCols);
+    tmem_relinquish();
+  }
+  for (int n = tid; n < nh * (kKP / 8); n += kReadThreads) {
+    const int hh = n / (kKP / 8), e = n % (kKP / 8);
+    reinterpret_cast<uint4 *>(s.coef[hh])[e] =
+        reinterpret_cast<const uint4 *>(args.coef + (size_t)(h0 + hh) * kKP)[e];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = s.tmem_base;
+  if (warp < 4) {
+    // zero the accumulators D^h of this thread's lane
+    uint32_t z[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) z[e] = 0u;
+    for (int col = 0; col < 80 * nh; col += 16) tmem_st16(tmem_lane_addr(tb, warp, kTmemD + col), z);
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  volatile int *abort_flag = &s.abort_flag;
+
+  if (warp == kIss0 || warp == kIss0 + 1) {
+    if (lane == 0) {
+      // ---------------- readout UMMA issuer t: jobs t, t + 2, t + 4, ...
+      const int t = warp - kIss0;
       const uint32_t id80 = idesc_bf16_f32(128, kN, 0);
-      const uint32_t id64k = idesc_bf16_f32(128, 64, 0);
-      const uint32_t id64mn = idesc_bf16_f32(128, 64, 1);
-      int nb_issued = 0;          // snapshot K blocks requested
-      int jr = 0;                 // next readout job
-      int it = 0;                 // next intra step (head * 2 + half)
-      int istate = 0;             // 0: issue s; 1: waiting for P; 2: waiting for P.V to finish
-      bool qkv_ready = false;
-      int b_seen = -1;            // highest K block whose stage has been waited for
-      uint64_t t_last = globaltimer_ns();
-      while ((jr < njobs || it < 2 * nh) && !*abort_flag) {
-        bool progress = false;
-        // snapshot K blocks into free stages
-        while (nb_issued < kNKB) {
-          const int st = nb_issued % kNB;
-          if (!mbar_test(&s.b_empty[st], ((nb_issued / kNB) & 1) ^ 1)) break;
-          mbar_arrive_expect_tx(&s.b_full[st], kN * 64 * 2);
-          tma_load_3d(s.b[st], &tmS, &s.b_full[st], 64 * nb_issued, 0, unit * args.nC + c);
-          ++nb_issued;
-          progress = true;
+      const uint64_t bdesc0 = sdesc_sw128(smem_u32(s.b[0]), 16, 1024);
+      constexpr uint64_t kStageStep = (kN * 64 * 2) >> 4;   // one snapshot stage
+      int jr = t, kb = t / nh, hh = t % nh;
+      int st = kb % kNB, sph = (kb / kNB) & 1;               // stage and its phase
+      int slot = t, aph = 0;                                 // A slot and its phase
+      int kb_seen = -1;
+      while (jr < njobs) {
+        if (kb != kb_seen) {
+          if (!mbar_wait(&s.b_full[st], sph, abort_flag, args.status)) break;
+          kb_seen = kb;
         }
-        if (!qkv_ready && mbar_test(&s.qkv_full, 0)) qkv_ready = true;
-        // intra steps (the P.V of a head must follow its first readout job)
-        if (qkv_ready && it < 2 * nh) {
-          const int hh = it >> 1, half = it & 1;
-          if (istate == 0) {
-            tc_fence_after();
-            const uint32_t qa = smem_u32(s.q[hh]);
-            const uint32_t ka = smem_u32(s.k) + half * 64 * 128;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              umma_ss(tb + kTmemS, sdesc_sw128(qa + 32 * k, 16, 1024),
-                      sdesc_sw128(ka + 32 * k, 16, 1024), id64k, k > 0);
-            umma_commit(&s.s_full);
-            istate = 1;
-            progress = true;
-          } else if (istate == 1 && jr >= nh && mbar_test(&s.p_full, it & 1)) {
-            tc_fence_after();
-            const uint32_t va = smem_u32(s.v) + half * 64 * 128;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              umma_ts(tb + kTmemD + 80 * hh, tb + kTmemS + 8 * k,
-                      sdesc_sw128(va + 2048 * k, 16, 1024), id64mn, 1u);
-            umma_commit(&s.s_free);
-            istate = 2;
-            progress = true;
-          } else if (istate == 2 && mbar_test(&s.s_free, it & 1)) {
-            ++it;
-            istate = 0;
-            progress = true;
-          }
+        if (!mbar_wait(&s.a_full[slot], aph, abort_flag, args.status)) break;
+        tc_fence_after();
+        const uint64_t bd = bdesc0 + kStageStep * st;
+        const uint32_t at = tb + kTmemA + 32 * slot;
+        const uint32_t dt = tb + kTmemD + 80 * hh;
+        umma_ts(dt, at, bd, id80, 1u);
+        if (kb != kNKB - 1) {
+          umma_ts(dt, at + 8, bd + 2, id80, 1u);
+          umma_ts(dt, at + 16, bd + 4, id80, 1u);
+          umma_ts(dt, at + 24, bd + 6, id80, 1u);
         }
-        // readout jobs, in order
-        if (jr < njobs) {
-          const int kb = jr / nh, hh = jr % nh;
-          const int slot = jr % kNA, st = kb % kNB;
-          bool b_ok = b_seen >= kb;
-          if (!b_ok && kb < nb_issued && mbar_test(&s.b_full[st], (kb / kNB) & 1)) {
-            b_seen = kb;
-            b_ok = true;
-          }
-          if (b_ok && mbar_test(&s.a_full[slot], (jr / kNA) & 1)) {
-            tc_fence_after();
-            const uint32_t ba = smem_u32(s.b[st]);
-            const int nk = kb == kNKB - 1 ? 1 : 4;
-            for (int k = 0; k < nk; ++k)
-              umma_ts(tb + kTmemD + 80 * hh, tb + kTmemA + 32 * slot + 8 * k,
-                      sdesc_sw128(ba + 32 * k, 16, 1024), id80, (kb > 0 || k > 0) ? 1u : 0u);
-            umma_commit(&s.a_empty[slot]);
-            if (hh == nh - 1) umma_commit(&s.b_empty[st]);
-            ++jr;
-            progress = true;
-          }
-        }
-        if (progress) {
-          t_last = globaltimer_ns();
-        } else if (globaltimer_ns() - t_last > kWaitLimitNs) {
-          *abort_flag = 1;
-          atomicCAS(args.status, 0, (int)OAL_ERR_TIMEOUT);
+        umma_commit(&s.a_empty[slot]);
+        // advance to this issuer's next job
+        jr += 2;
+        slot += 2;
+        if (slot >= kNA) { slot -= kNA; aph ^= 1; }
+        hh += 2;
+        int nkb = kb;
+        while (hh >= nh) { hh -= nh; ++nkb; }
+        if (nkb != kb || jr >= njobs) {
+          umma_commit(&s.b_empty[st]);        // this issuer is done with the stage
+          for (; kb < nkb; ++kb)
+            if (++st == kNB) { st = 0; sph ^= 1; }
         }
       }
       umma_commit(&s.d_full);
-      // drain before the block releases its memory: copies, then MMAs
-      mbar_wait_teardown(&s.qkv_full, 0, args.status);
-      for (int kb = max(0, nb_issued - kNB); kb < nb_issued; ++kb)
-        mbar_wait_teardown(&s.b_full[kb % kNB], (kb / kNB) & 1, args.status);
-      mbar_wait_teardown(&s.d_full, 0, args.status);
+      mbar_wait_teardown(&s.d_full, 0, args.status);   // no MMA in flight at exit
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    // ---------------- readout A builders: two warps per TMEM lane quarter,
-    // alternating jobs; thread = token row
+  } else if (warp == kTma) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmS);
+      mbar_arrive_expect_tx(&s.qkv_full, (uint32_t)nh * kC * 64 * 2);
+      for (int hh = 0; hh < nh; ++hh)
+        tma_load_3d(s.q[hh], &tmQ, &s.qkv_full, 0, c * kC, bidx * args.Hq + h0 + hh);
+      int issued = 0, st = 0, sph = 0;
+      for (int kb = 0; kb < kNKB; ++kb) {
+        if (!mbar_wait(&s.b_empty[st], sph ^ 1, abort_flag, args.status)) break;
+        mbar_arrive_expect_tx(&s.b_full[st], kN * 64 * 2);
+        tma_load_3d(s.b[st], &tmS, &s.b_full[st], 64 * kb, 0, unit * args.nC + c);
+        issued = kb + 1;
+        if (++st == kNB) { st = 0; sph ^= 1; }
+      }
+      // copies still in flight must land before the block exits
+      mbar_wait_teardown(&s.qkv_full, 0, args.status);
+      for (int kb = max(0, issued - kNB); kb < issued; ++kb)
+        mbar_wait_teardown(&s.b_full[kb % kNB], (kb / kNB) & 1, args.status);
+    }
+    __syncwarp();
+  } else if (warp < 12) {
+    // ---------------- readout A builders: thread = token row
     const int m = 32 * (warp & 3) + lane;
-    const int pg = (warp - 4) >> 2;           // job parity handled by this warp
+    const int g3 = warp >> 2;                 // builds jobs g3, g3 + 3, ...
     if (mbar_wait(&s.qkv_full, 0, abort_flag, args.status)) {
-      for (int jb = pg; jb < njobs; jb += 2) {
-        const int kb = jb / nh, hh = jb % nh, slot = jb % kNA;
+      const uint8_t *qbase = reinterpret_cast<const uint8_t *>(s.q[0]) + m * 128;
+      const int m7 = m & 7;
+      int kb = g3 / nh, hh = g3 % nh;
+      int slot = g3, aph = 0;
+      for (int jb = g3; jb < njobs; jb += 3) {
         uint32_t q[32], cw[32], out[32];
-        const uint8_t *qrow = reinterpret_cast<const uint8_t *>(s.q[hh]);
+        const uint8_t *qrow = qbase + hh * (kC * 64 * 2);
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(qrow + sw128(m, cc));
+          const uint4 v = *reinterpret_cast<const uint4 *>(qrow + ((cc ^ m7) << 4));
           q[4 * cc] = v.x; q[4 * cc + 1] = v.y; q[4 * cc + 2] = v.z; q[4 * cc + 3] = v.w;
         }
         const uint4 *cp = reinterpret_cast<const uint4 *>(s.coef[hh] + 64 * kb);
@@ -944,62 +1152,78 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           cw[4 * e] = v.x; cw[4 * e + 1] = v.y; cw[4 * e + 2] = v.z; cw[4 * e + 3] = v.w;
         }
         build_dispatch(kb, q, cw, out);
-        if (!mbar_wait(&s.a_empty[slot], ((jb / kNA) & 1) ^ 1, abort_flag, args.status)) break;
-        uint32_t lo[16], hi[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) { lo[e] = out[e]; hi[e] = out[16 + e]; }
-        tmem_st16(tmem_lane_addr(tb, warp, kTmemA + 32 * slot), lo);
-        tmem_st16(tmem_lane_addr(tb, warp, kTmemA + 32 * slot + 16), hi);
+        if (!mbar_wait(&s.a_empty[slot], aph ^ 1, abort_flag, args.status)) break;
+        tmem_st16(tmem_lane_addr(tb, warp, kTmemA + 32 * slot),
+                  *reinterpret_cast<const uint32_t(*)[16]>(&out[0]));
+        tmem_st16(tmem_lane_addr(tb, warp, kTmemA + 32 * slot + 16),
+                  *reinterpret_cast<const uint32_t(*)[16]>(&out[16]));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.a_full[slot]);
+        slot += 3;
+        if (slot >= kNA) { slot -= kNA; aph ^= 1; }
+        hh += 3;
+        while (hh >= nh) { hh -= nh; ++kb; }
       }
     }
-  } else {
-    // ---------------- warps 0-3: intra-chunk kernel (thread = query row), then epilogue
-    float den_intra[kMaxNH] = {0.f, 0.f, 0.f, 0.f};
-    const bool ok = intra_worker<G>(s, args, c, nh, warp, lane, tb, den_intra);
-    const int m = tid;
-    const int i_tok = c * kC + m;
-    if (ok && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
-      tc_fence_after();
-      for (int hh = 0; hh < nh; ++hh) {
-        uint32_t d[kN];
+    if (warp < 4) {
+      // ---------------- epilogue: y = (u~ + intra)[0:64] / (u~ + intra)[64].
+      // The intra-chunk rows of every head are loaded before the wait so the
+      // global-memory latency overlaps the last UMMAs; one head at a time
+      // keeps the registers in bounds.
+      const int i_tok = c * kC + m;
+      const bool row_ok = i_tok < args.T;
+      const size_t row0 = ((size_t)bidx * args.Hq + h0) * args.T + i_tok;
+      float4 inum[16];
+      float iden = 0.f;
+      auto load_intra = [&](int hh) {
+        if (row_ok) {
+          const size_t row = row0 + (size_t)hh * args.T;
+          const float4 *src = reinterpret_cast<const float4 *>(args.intra_num + row * 64);
 #pragma unroll
-        for (int q5 = 0; q5 < 5; ++q5) {
-          uint32_t r[16];
-          tmem_ld16(tmem_lane_addr(tb, warp, kTmemD + 80 * hh + 16 * q5), r);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) d[16 * q5 + e] = r[e];
+          for (int e = 0; e < 16; ++e) inum[e] = __ldg(src + e);
+          iden = __ldg(args.intra_den + row);
         }
-        tmem_wait_ld();
-        float den = __uint_as_float(d[64]);
+      };
+      load_intra(0);
+      if (!*abort_flag && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
+        tc_fence_after();
+        for (int hh = 0; hh < nh; ++hh) {
+          // denominator column first, then the values 16 columns at a time
+          uint32_t r[16];
+          tmem_ld16(tmem_lane_addr(tb, warp, kTmemD + 80 * hh + 64), r);
+          tmem_wait_ld();
+          const float inv = 1.0f / (__uint_as_float(r[0]) + iden);
+          uint4 *dst = reinterpret_cast<uint4 *>(args.Y + (row0 + (size_t)hh * args.T) * kDv);
 #pragma unroll
-        for (int e = 0; e < kMaxNH; ++e)
-          if (e == hh) den += den_intra[e];
-        const float inv = 1.0f / den;
-        if (i_tok < args.T) {
-          uint4 *dst = reinterpret_cast<uint4 *>(
-              args.Y + (((size_t)bidx * args.Hq + h0 + hh) * args.T + i_tok) * kDv);
+          for (int q4 = 0; q4 < 4; ++q4) {
+            tmem_ld16(tmem_lane_addr(tb, warp, kTmemD + 80 * hh + 16 * q4), r);
+            tmem_wait_ld();
+            uint32_t pk[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(d[8 * e]) * inv, __uint_as_float(d[8 * e + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(d[8 * e + 2]) * inv, __uint_as_float(d[8 * e + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(d[8 * e + 4]) * inv, __uint_as_float(d[8 * e + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(d[8 * e + 6]) * inv, __uint_as_float(d[8 * e + 7]) * inv);
-            dst[e] = v;
+            for (int e = 0; e < 4; ++e) {
+              const float4 n4 = inum[4 * q4 + e];
+              pk[2 * e] = pack_bf16x2((__uint_as_float(r[4 * e]) + n4.x) * inv,
+                                      (__uint_as_float(r[4 * e + 1]) + n4.y) * inv);
+              pk[2 * e + 1] = pack_bf16x2((__uint_as_float(r[4 * e + 2]) + n4.z) * inv,
+                                          (__uint_as_float(r[4 * e + 3]) + n4.w) * inv);
+            }
+            if (row_ok) {
+              dst[2 * q4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              dst[2 * q4 + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
           }
+          if (hh + 1 < nh) load_intra(hh + 1);
         }
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kCtl) {
+  if (warp == kMem) {
     tc_fence_after();
-    tmem_dealloc(tb, 512);
+    tmem_dealloc(tb, kReadTmemCols);
   }
 }
 
@@ -1034,7 +1258,7 @@ static bool make_map3(CUtensorMap *m, const void *ptr, uint64_t nx, uint64_t ny,
 
 struct Layout {
   int nC, nparts, cpp, U;
-  size_t snap_off, ptot_off, coef_off, plan_off, total;
+  size_t snap_off, ptot_off, coef_off, plan_off, inum_off, iden_off, total;
 };
 
 static Layout plan_layout(int B, int Hq, int Hkv, int T) {
@@ -1051,20 +1275,22 @@ static Layout plan_layout(int B, int Hq, int Hkv, int T) {
   L.ptot_off = o; o = al(o + (size_t)L.U * L.nparts * kTiles * 128 * kN * sizeof(float));
   L.coef_off = o; o = al(o + (size_t)Hq * kKP * 2);
   L.plan_off = o; o = al(o + (size_t)Hq * sizeof(KPlan));
+  L.inum_off = o; o = al(o + (size_t)B * Hq * T * 64 * sizeof(float));
+  L.iden_off = o; o = al(o + (size_t)B * Hq * T * sizeof(float));
   L.total = o;
   return L;
 }
 
-using ReadoutKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, ReadArgs);
-static ReadoutKernel readout_kernel_for(int G) {
+using IntraKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, ReadArgs);
+static IntraKernel intra_kernel_for(int G) {
   switch (G) {
-    case 1: return tc_readout_kernel<1>;
-    case 2: return tc_readout_kernel<2>;
-    case 3: return tc_readout_kernel<3>;
-    case 4: return tc_readout_kernel<4>;
-    case 5: return tc_readout_kernel<5>;
-    case 6: return tc_readout_kernel<6>;
-    default: return tc_readout_kernel<7>;
+    case 1: return tc_intra_kernel<1>;
+    case 2: return tc_intra_kernel<2>;
+    case 3: return tc_intra_kernel<3>;
+    case 4: return tc_intra_kernel<4>;
+    case 5: return tc_intra_kernel<5>;
+    case 6: return tc_intra_kernel<6>;
+    default: return tc_intra_kernel<7>;
   }
 }
 
@@ -1103,14 +1329,17 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
 
   const size_t ssmem = sizeof(StateSmem) + 1024;
   const size_t rsmem = sizeof(ReadSmem) + 1024;
+  const size_t ismem = sizeof(IntraSmem) + 1024;
   static int attr_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_dev != dev) {
     cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
+    cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)rsmem);
     for (int g = 1; g <= kMaxG; ++g)
-      cudaFuncSetAttribute(readout_kernel_for(g), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)rsmem);
+      cudaFuncSetAttribute(intra_kernel_for(g), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)ismem);
     attr_dev = dev;
   }
   StateArgs sa;
@@ -1135,9 +1364,14 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   ra.nh_per_block = kMaxNH;
   ra.Y = static_cast<__nv_bfloat16 *>(Y);
   ra.coef = coef; ra.plans = plans; ra.status = status;
-  const int nhg = (ra.rho + kMaxNH - 1) / kMaxNH;
-  dim3 g2(nhg, lay.nC, lay.U);
-  readout_kernel_for(G)<<<g2, kReadThreads, rsmem, stream>>>(tmQ, tmK, tmV, tmS, ra);
+  ra.intra_num = reinterpret_cast<float *>(w + lay.inum_off);
+  ra.intra_den = reinterpret_cast<float *>(w + lay.iden_off);
+  dim3 gi((ra.rho + kIntraNH - 1) / kIntraNH, lay.nC, lay.U);
+  intra_kernel_for(G)<<<gi, kIntraThreads, ismem, stream>>>(tmQ, tmK, tmV, ra);
+  st = oal_after_launch("tc_intra_kernel", stream);
+  if (st != OAL_OK) return st;
+  dim3 g2((ra.rho + kMaxNH - 1) / kMaxNH, lay.nC, lay.U);
+  tc_readout_kernel<<<g2, kReadThreads, rsmem, stream>>>(tmQ, tmS, ra);
   return oal_after_launch("tc_readout_kernel", stream);
 }
 

@@ -15,11 +15,10 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
+// SM cycle counter; cheap to read, unlike %globaltimer, so it is the clock of
+// every bounded wait.  Limits are in cycles (2^32 cycles is about 2 s at the
+// GB300's 2.07 GHz maximum SM clock, longer at lower clocks).
+__device__ __forceinline__ uint64_t cycles_now() { return (uint64_t)clock64(); }
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
@@ -44,14 +43,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                : "memory");
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes (or the hint, in ns, runs out) instead of spinning and
+// taking issue slots from the warps that do the work.
+constexpr uint32_t kSuspendHintNs = 200000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -73,15 +76,15 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 
 // Bounded wait for the phase with the given parity.  `abort` is a block-wide
 // flag in shared memory; `status` the device status word (may be null).
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kWaitLimitCycles = 1ull << 32;  // about 2 s
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           volatile int *abort, int *status) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const uint64_t t0 = cycles_now();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (cycles_now() - t0 > kWaitLimitCycles) {
       *abort = 1;
       if (status) atomicCAS(status, 0, 4 /* OAL_ERR_TIMEOUT */);
       return false;
@@ -91,11 +94,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
 
 // Teardown wait: ignores the abort flag (used to drain copies and MMAs that
 // are already in flight before a block releases its memory); bounded.
-constexpr uint64_t kTeardownLimitNs = 200000000ull;  // 0.2 s
+constexpr uint64_t kTeardownLimitCycles = 1ull << 29;  // about 0.25 s
 __device__ __forceinline__ bool mbar_wait_teardown(uint64_t *bar, uint32_t parity, int *status) {
-  const uint64_t t0 = globaltimer_ns();
+  const uint64_t t0 = cycles_now();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kTeardownLimitNs) {
+    if (cycles_now() - t0 > kTeardownLimitCycles) {
       if (status) atomicCAS(status, 0, 4 /* OAL_ERR_TIMEOUT */);
       return false;
     }
