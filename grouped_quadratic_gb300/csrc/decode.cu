@@ -1,6 +1,6 @@
 // decode.cu -- one decode token of OAL ([OAL] = "Not All Dimensions Are
 // Equal: Outlier-Aware Attention Linearization with Grouped Quadratic
-// Kernels", Algorithm 1 lines 7-10).
+// Kernels", Algorithm 1, its per-token state update and readout).
 //
 // For each (batch, KV head) the fp32 state S [F][65] is streamed once:
 //     S[f][c] += phi_f(k) u_c              (Eq. 5 update, u = [v; 1])

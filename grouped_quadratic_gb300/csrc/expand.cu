@@ -1,4 +1,4 @@
-// expand.cu -- coefficient expansion of [OAL] Sec. 4.3 (Algorithm 1, line 5).
+// expand.cu -- coefficient expansion of [OAL] Sec. 4.3 (Algorithm 1, the coefficient step).
 //
 //   M = L L^T,  a = eps + M_00,  b_r = 2 M_{0,g(r)},  C_rt = M_{g(r),g(t)}
 //

@@ -74,7 +74,7 @@ size_t oal_coeff_table_elems(int d, oal_state_layout layout);
 
 /*
  * oal_expand_coeffs -- coefficient map of [OAL] Sec. 4.3 ("Positive
- * group-aware kernel"), Algorithm 1 line 5:  M = L L^T,
+ * group-aware kernel"), the coefficient step of Algorithm 1:  M = L L^T,
  *     a = eps + M_00,  b_r = 2 M_{0,g(r)},  C_rt = M_{g(r),g(t)}.
  *  L      [Hq][G+1][G+1] fp32, row-major; only the lower triangle is read.
  *  group  [Hq][d] int32, the group of each dimension, values 1..G.
@@ -95,7 +95,7 @@ oal_status oal_expand_coeffs(const float *L, const int32_t *group, int Hq,
 
 /*
  * oal_prefill -- causal OAL attention over T tokens ([OAL] Algorithm 1,
- * causal-evaluation stage, lines 5-12), evaluated in chunks of `chunk`
+ * causal-evaluation stage), evaluated in chunks of `chunk`
  * tokens: inter-chunk terms through the prefix states (Eqs. 5-6),
  * intra-chunk terms pair by pair from the group sums (Eq. 7).  Exact in
  * real arithmetic ([OAL] App. D, Eq. (25)).
@@ -129,7 +129,7 @@ oal_status oal_prefill(const void *Q, const void *K, const void *V,
                        cudaStream_t stream);
 
 /*
- * oal_decode_step -- one token of [OAL] Algorithm 1 (lines 7-10) for every
+ * oal_decode_step -- one token of [OAL] Algorithm 1 (state update and readout) for every
  * sequence: u = [v; 1]; H0 += u; H1_r += k_r u; H2_rt += k_r k_t u; then the
  * Eq. (6) readout for each query head of the KV head (inclusive: the new
  * token attends to itself).
