@@ -57,6 +57,9 @@ def load_library(path: str = LIB_PATH):
     lib.oal_prefill.argtypes = ([vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, vp, vp, ci, cf,
                                  vp, vp, vp, ci, vp, ci, vp, ci, vp, sz, vp])
     lib.oal_prefill.restype = ci
+    lib.oal_prefill_noalloc.argtypes = ([vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, vp, vp, ci,
+                                         cf, vp, vp, vp, ci, vp, ci, vp, ci, vp])
+    lib.oal_prefill_noalloc.restype = ci
     lib.oal_decode_workspace_bytes.argtypes = [ci] * 5 + [ci]
     lib.oal_decode_workspace_bytes.restype = sz
     lib.oal_decode_step.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, ci,
@@ -174,6 +177,31 @@ def oal_prefill(Q, K, V, L, group, eps, a, b, C, layout=OAL_STATE_FULL, state=No
                            _ptr(state), int(bool(continue_from_state)), _ptr(Y), chunk,
                            _ptr(workspace), workspace.numel() * workspace.element_size(),
                            _stream(stream)))
+    return Y, state
+
+
+# Size of the library's fixed prefill scratch (OAL_PREFILL_NOALLOC_SCRATCH_BYTES).
+OAL_PREFILL_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def oal_prefill_noalloc(Q, K, V, L, group, eps, a, b, C, state, Y, layout=OAL_STATE_FULL,
+                        continue_from_state=False, chunk=0, stream=None):
+    """oal_prefill with the library's fixed scratch instead of a workspace.
+
+    For callers that cannot allocate device memory: `state` and `Y` must be
+    passed in, and this wrapper allocates nothing either.  Problems whose
+    workspace would exceed OAL_PREFILL_NOALLOC_SCRATCH_BYTES are rejected.
+    """
+    lib = load_library()
+    B, Hq, T, d = Q.shape
+    Hkv, dv = K.shape[1], V.shape[3]
+    G = L.shape[1] - 1
+    _need_cuda(Q, K, V, L, group, a, b, C, state, Y)
+    _check(lib.oal_prefill_noalloc(_ptr(Q), _ptr(K), _ptr(V), _dtype_code(Q), B, Hq, Hkv, T,
+                                   d, dv, _ptr(L), _ptr(group), G, float(eps), _ptr(a),
+                                   _ptr(b), _ptr(C), layout, _ptr(state),
+                                   int(bool(continue_from_state)), _ptr(Y), chunk,
+                                   _stream(stream)))
     return Y, state
 
 

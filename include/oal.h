@@ -129,6 +129,45 @@ oal_status oal_prefill(const void *Q, const void *K, const void *V,
                        cudaStream_t stream);
 
 /*
+ * oal_prefill_noalloc -- oal_prefill without a caller workspace.  The paper
+ * has no counterpart: this is a deployment convenience of this library.
+ *
+ * Some callers cannot allocate device memory at the point where they run a
+ * prefill: code that must not call cudaMalloc or a caching allocator (for
+ * instance inside a framework that owns all device memory, or a runtime that
+ * forbids allocation after start-up), or code that has no allocator handle
+ * at all.  This entry point takes the same arguments as oal_prefill minus
+ * `workspace` / `workspace_bytes`; its scratch lives in one fixed array of
+ * OAL_PREFILL_NOALLOC_SCRATCH_BYTES bytes inside the library, which every
+ * GPU that loads the library keeps until the process exits.  It makes no
+ * cudaMalloc / cudaFree call and calls no allocating library routine.
+ *  Limit: a problem whose oal_prefill_workspace_bytes(...) exceeds
+ *    OAL_PREFILL_NOALLOC_SCRATCH_BYTES is rejected with OAL_ERR_INVALID_ARG
+ *    and a message giving both sizes (bf16 with B = 1, Hq = 14, Hkv = 2
+ *    fits up to T = 6016); use oal_prefill with a workspace beyond that.
+ *  First call on a device: looks up the array's device address with
+ *    cudaGetSymbolAddress on the current device (this may load the
+ *    library's device code on that device) and caches it per device.
+ *    Make that first call before any stream capture begins.
+ *  Sharing: all calls in the process share the one array per device.  Two
+ *    calls whose kernels overlap on the GPU (different streams without an
+ *    ordering between them, or different host threads) race on it and give
+ *    wrong results; order them on one stream.  Nothing in the array needs to
+ *    start at zero: each call writes every scratch byte before reading it.
+ *  Everything else (arguments, layouts, errors, arithmetic) is as for
+ *    oal_prefill.
+ */
+#define OAL_PREFILL_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+oal_status oal_prefill_noalloc(const void *Q, const void *K, const void *V,
+                               oal_dtype dtype, int B, int Hq, int Hkv, int T,
+                               int d, int dv, const float *L,
+                               const int32_t *group, int G, float eps,
+                               const float *a, const float *b, const float *C,
+                               oal_state_layout layout, float *state,
+                               int continue_from_state, void *Y, int chunk,
+                               cudaStream_t stream);
+
+/*
  * oal_decode_step -- one token of [OAL] Algorithm 1 (state update and readout) for every
  * sequence: u = [v; 1]; H0 += u; H1_r += k_r u; H2_rt += k_r k_t u; then the
  * Eq. (6) readout for each query head of the KV head (inclusive: the new
