@@ -8,13 +8,16 @@
 //                                           h sharing the KV head)
 // and y^h = u~^h[0:64] / u~^h[64].  The kernel is bound by HBM: 8 bytes
 // (read + write) per state element.  Rows of the state are split into
-// slices, one block per (slice, batch x KV head); inside a block each warp
-// walks rows (lane l owns columns l and l+32, lane 0 also column 64), so
-// every load and store is a coalesced 128-byte warp access and the readout
-// accumulators stay in registers.  Per-slice partial readouts go to the
-// workspace; the last block of a (batch, KV head) to finish (atomic ticket)
-// sums them in slice order and divides.
+// slices, one block per (slice, batch x KV head).  A block first copies its
+// whole slice into shared memory with asynchronous 4-byte copies (rows of 65
+// floats are not 16-byte aligned), forms the per-row weights meanwhile, then
+// each warp walks rows (lane l owns columns l and l+32, lane 0 also column
+// 64): coalesced 128-byte stores of the updated rows and readout accumulators
+// in registers.  Per-slice partial readouts go to the workspace; the last
+// block of a (batch, KV head) to finish (atomic ticket) sums them in a fixed
+// order and divides.
 #include "oal_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace oal {
 namespace {
@@ -25,9 +28,21 @@ static __device__ const PairTable c_pairs = make_pair_table();
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRowsPerBlock = 256;
+constexpr int kMaxRowsPerBlock = 128;   // rows of one slice
+constexpr int kMinRowsPerBlock = 128;
 constexpr int kMaxRho = 8;
-constexpr int kUnroll = 4;
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {   // a * b + c, two lanes
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+constexpr int kGroups = 4;             // row groups of a slice, each with its own bulk copy
 
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
@@ -35,24 +50,57 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
               const Tin *__restrict__ v, Tin *__restrict__ y,
               const float *__restrict__ a, const float *__restrict__ b,
               const float *__restrict__ Ctab, float *__restrict__ state, int Hq,
-              int Hkv, int F, int packed, int nslices,
-              float *__restrict__ partial, unsigned *__restrict__ tickets) {
+              int Hkv, int F, int packed, int rows_per_block, int nslices,
+              float *__restrict__ partial, unsigned *__restrict__ tickets, int *status) {
   const int rho = Hq / Hkv;
   const int slice = blockIdx.x;
   const int unit = blockIdx.y;              // b * Hkv + kv
   const int bidx = unit / Hkv, kv = unit % Hkv;
   const int h0 = kv * rho;
-  const int f0 = slice * kRowsPerBlock;
-  const int nrows = min(kRowsPerBlock, F - f0);
+  const int f0 = slice * rows_per_block;
+  const int nrows = min(rows_per_block, F - f0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+  extern __shared__ __align__(16) float s_buf[];   // decode_smem_floats(rows_per_block)
   __shared__ float s_k[kD];
   __shared__ float s_u[kU];
   __shared__ float s_q[kMaxRho][kD];
-  __shared__ float s_wk[kRowsPerBlock];
-  __shared__ float s_wq[kMaxRho][kRowsPerBlock];
-  __shared__ float s_red[kWarps][kMaxRho][kU];
+  __shared__ __align__(16) float s_wk[kMaxRowsPerBlock];
+  __shared__ __align__(16) float s_wq[kMaxRho][kMaxRowsPerBlock];
+  __shared__ __align__(8) uint64_t s_bar[kGroups];
+  __shared__ int s_abort;
   __shared__ bool s_last;
+
+  // The slice (nrows rows of 65 floats) is contiguous in memory but not
+  // 16-byte aligned in general.  Its aligned interior is fetched by kGroups
+  // bulk copies (one per group of rows, boundaries rounded up to 16 bytes)
+  // issued before anything else; the at most 3 + 3 floats outside it are
+  // read with plain loads.  s_rows[i] holds float i of the slice.
+  float *S = state + ((size_t)unit * F + f0) * kU;
+  const size_t sf0 = ((size_t)unit * F + f0) * kU;     // float index of the slice
+  const int nel = nrows * kU;
+  const int head = (int)((4 - (sf0 & 3)) & 3);
+  const int tail = (int)((sf0 + nel) & 3);
+  float *s_rows = s_buf + ((4 - head) & 3);            // s_rows + head is 16-byte aligned
+  const int rows_per_group = (((nrows + kGroups - 1) / kGroups) + 3) & ~3;   // whole steps of 4
+  auto copy_begin = [&](int g) {                      // float offset where copy g starts
+    if (g == 0) return min(head, nel - tail);
+    const int x = min(nrows, g * rows_per_group) * kU;
+    return min(nel - tail, head + ((x - head + 3) & ~3));
+  };
+  if (tid == 0) {
+    s_abort = 0;
+    for (int g = 0; g < kGroups; ++g) oal::tc::mbar_init(&s_bar[g], 1);
+    oal::tc::fence_mbar_init();
+    for (int g = 0; g < kGroups; ++g) {
+      const int c0 = copy_begin(g), c1 = copy_begin(g + 1 < kGroups ? g + 1 : kGroups);
+      const int n = (g + 1 < kGroups ? c1 : nel - tail) - c0;
+      oal::tc::mbar_arrive_expect_tx(&s_bar[g], n > 0 ? (uint32_t)n * 4u : 0u);
+      if (n > 0) oal::tc::bulk_load(s_rows + c0, S + c0, (uint32_t)n * 4u, &s_bar[g]);
+    }
+  }
+  if (tid < head) s_rows[tid] = __ldcs(S + tid);
+  if (tid >= 32 && tid < 32 + tail) s_rows[nel - tail + tid - 32] = __ldcs(S + nel - tail + tid - 32);
 
   for (int n = tid; n < kD; n += kThreads) s_k[n] = to_f32(k[(size_t)unit * kD + n]);
   for (int n = tid; n < kU; n += kThreads)
@@ -100,56 +148,71 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
   }
   __syncthreads();
 
-  float acc[kMaxRho][3];
+  // Value columns: each warp takes 4 consecutive rows per step (lane l owns
+  // columns l and l + 32) and accumulates the readout of every head with
+  // packed fp32 FMAs.  Column 64 (the normaliser) follows, one row per thread.
+  float2 acc[kMaxRho];
 #pragma unroll
-  for (int hh = 0; hh < kMaxRho; ++hh) acc[hh][0] = acc[hh][1] = acc[hh][2] = 0.f;
-  const float u0 = s_u[lane], u1 = s_u[lane + 32], u2 = s_u[64];
-  float *S = state + ((size_t)unit * F + f0) * kU;
-
-  for (int rb = warp * kUnroll; rb < nrows; rb += kWarps * kUnroll) {
-    float x0[kUnroll], x1[kUnroll], x2[kUnroll];
+  for (int hh = 0; hh < kMaxRho; ++hh) acc[hh] = make_float2(0.f, 0.f);
+  const float2 u01 = make_float2(s_u[lane], s_u[lane + 32]);
+  // (the __syncthreads above also publishes the head and tail floats)
+  for (int g = 0; g < kGroups; ++g) {
+    if (!oal::tc::mbar_wait(&s_bar[g], 0, &s_abort, status)) break;
+    const int r1 = min(nrows, (g + 1) * rows_per_group);
+    for (int rb = g * rows_per_group + 4 * warp; rb < r1; rb += 4 * kWarps) {
+      const float4 wk4 = *reinterpret_cast<const float4 *>(&s_wk[rb]);
+      const float wk[4] = {wk4.x, wk4.y, wk4.z, wk4.w};
+      float2 nv[4];
 #pragma unroll
-    for (int uu = 0; uu < kUnroll; ++uu) {
-      const int rr = rb + uu;
-      if (rr < nrows) {
-        const float *src = S + (size_t)rr * kU;
-        x0[uu] = __ldcs(src + lane);
-        x1[uu] = __ldcs(src + lane + 32);
-        x2[uu] = lane == 0 ? __ldcs(src + 64) : 0.f;
+      for (int u = 0; u < 4; ++u) {
+        const int rr = rb + u;
+        nv[u] = make_float2(0.f, 0.f);
+        if (rr < r1) {
+          const float *src = s_rows + rr * kU;
+          nv[u] = make_float2(fmaf(wk[u], u01.x, src[lane]), fmaf(wk[u], u01.y, src[lane + 32]));
+          float *dst = S + (size_t)rr * kU;
+          __stcs(dst + lane, nv[u].x);
+          __stcs(dst + lane + 32, nv[u].y);
+        }
       }
-    }
 #pragma unroll
-    for (int uu = 0; uu < kUnroll; ++uu) {
-      const int rr = rb + uu;
-      if (rr < nrows) {
-        const float wk = s_wk[rr];
-        const float n0 = fmaf(wk, u0, x0[uu]);
-        const float n1 = fmaf(wk, u1, x1[uu]);
-        const float n2 = fmaf(wk, u2, x2[uu]);
-        float *dst = S + (size_t)rr * kU;
-        __stcs(dst + lane, n0);
-        __stcs(dst + lane + 32, n1);
-        if (lane == 0) __stcs(dst + 64, n2);
-#pragma unroll
-        for (int hh = 0; hh < kMaxRho; ++hh) {
-          if (hh < rho) {
-            const float wq = s_wq[hh][rr];
-            acc[hh][0] = fmaf(wq, n0, acc[hh][0]);
-            acc[hh][1] = fmaf(wq, n1, acc[hh][1]);
-            acc[hh][2] = fmaf(wq, n2, acc[hh][2]);
-          }
+      for (int hh = 0; hh < kMaxRho; ++hh) {
+        if (hh < rho) {
+          const float4 wq = *reinterpret_cast<const float4 *>(&s_wq[hh][rb]);
+          acc[hh] = ffma2(make_float2(wq.x, wq.x), nv[0], acc[hh]);
+          acc[hh] = ffma2(make_float2(wq.y, wq.y), nv[1], acc[hh]);
+          acc[hh] = ffma2(make_float2(wq.z, wq.z), nv[2], acc[hh]);
+          acc[hh] = ffma2(make_float2(wq.w, wq.w), nv[3], acc[hh]);
         }
       }
     }
   }
+  // every copy has landed (or timed out) before the buffer is read again
+  for (int g = 0; g < kGroups; ++g) oal::tc::mbar_wait_teardown(&s_bar[g], 0, status);
+  float den[kMaxRho];
+#pragma unroll
+  for (int hh = 0; hh < kMaxRho; ++hh) den[hh] = 0.f;
+  for (int rr = tid; rr < nrows; rr += kThreads) {
+    const float n2 = s_rows[rr * kU + kDv] + s_wk[rr];   // u_64 = 1
+    __stcs(S + (size_t)rr * kU + kDv, n2);
+#pragma unroll
+    for (int hh = 0; hh < kMaxRho; ++hh)
+      if (hh < rho) den[hh] = fmaf(s_wq[hh][rr], n2, den[hh]);
+  }
+#pragma unroll
+  for (int hh = 0; hh < kMaxRho; ++hh)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den[hh] += __shfl_xor_sync(0xffffffffu, den[hh], o);
+  __syncthreads();   // the slice buffer is reused for the block reduction
+  float(*s_red)[kMaxRho][kU] = reinterpret_cast<float(*)[kMaxRho][kU]>(s_buf);
 
   // block reduction (fixed order) -> partial[unit][slice][rho][65]
 #pragma unroll
   for (int hh = 0; hh < kMaxRho; ++hh) {
     if (hh < rho) {
-      s_red[warp][hh][lane] = acc[hh][0];
-      s_red[warp][hh][lane + 32] = acc[hh][1];
-      if (lane == 0) s_red[warp][hh][64] = acc[hh][2];
+      s_red[warp][hh][lane] = acc[hh].x;
+      s_red[warp][hh][lane + 32] = acc[hh].y;
+      if (lane == 0) s_red[warp][hh][64] = den[hh];
     }
   }
   __syncthreads();
@@ -174,9 +237,21 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
   const float *pu = partial + (size_t)unit * nslices * kMaxRho * kU;
   for (int n = tid; n < rho * kU; n += kThreads) {
     const int hh = n / kU, c = n % kU;
-    float s = 0.f;
-    for (int sl = 0; sl < nslices; ++sl) s += __ldcg(pu + (size_t)sl * kMaxRho * kU + hh * kU + c);
-    s_tot[hh][c] = s;
+    // sixteen interleaved partial sums (loads in flight together), combined
+    // in a fixed order
+    float p16[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) p16[j] = 0.f;
+    for (int sl0 = 0; sl0 < nslices; sl0 += 16) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (sl0 + j < nslices) p16[j] += __ldcg(pu + (size_t)(sl0 + j) * kMaxRho * kU + hh * kU + c);
+    }
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+      for (int j = 0; j < w; ++j) p16[j] += p16[j + w];
+    s_tot[hh][c] = p16[0];
   }
   __syncthreads();
   for (int n = tid; n < rho * kDv; n += kThreads) {
@@ -188,13 +263,31 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 
 }  // namespace
 
-int decode_slices(int packed) {
-  return (state_rows(packed) + kRowsPerBlock - 1) / kRowsPerBlock;
+// Dynamic shared memory of a block: the slice (+ alignment slack), reused
+// afterwards for the per-warp readout partials.
+static size_t decode_smem_floats(int rpb) {
+  const size_t rows = (size_t)rpb * kU + 8, red = (size_t)kWarps * kMaxRho * kU;
+  return rows > red ? rows : red;
+}
+
+// Rows per block: small enough that small batches of sequences still spread
+// over the SMs (at least ~2 blocks per SM), a multiple of 32.
+static int decode_rows_per_block(size_t units, int packed) {
+  int rpb = kMaxRowsPerBlock;
+  while (rpb > kMinRowsPerBlock &&
+         units * (size_t)((state_rows(packed) + rpb - 1) / rpb) < 2 * 152)
+    rpb /= 2;
+  return rpb;
+}
+
+static int decode_slices(size_t units, int packed) {
+  const int rpb = decode_rows_per_block(units, packed);
+  return (state_rows(packed) + rpb - 1) / rpb;
 }
 
 size_t decode_workspace_bytes(int B, int Hkv, int packed) {
   const size_t units = (size_t)B * Hkv;
-  const size_t part = units * decode_slices(packed) * kMaxRho * kU * sizeof(float);
+  const size_t part = units * decode_slices(units, packed) * kMaxRho * kU * sizeof(float);
   const size_t tick = units * sizeof(unsigned);
   return ((part + 255) / 256) * 256 + ((tick + 255) / 256) * 256;
 }
@@ -206,8 +299,9 @@ oal_status launch_decode(const void *q, const void *k, const void *v, int is_bf1
                          const float *C, int packed, float *state, void *y,
                          void *ws, cudaStream_t stream) {
   const int F = state_rows(packed);
-  const int nslices = decode_slices(packed);
   const size_t units = (size_t)B * Hkv;
+  const int rpb = decode_rows_per_block(units, packed);
+  const int nslices = decode_slices(units, packed);
   const size_t part_bytes =
       ((units * nslices * kMaxRho * kU * sizeof(float) + 255) / 256) * 256;
   float *partial = (float *)ws;
@@ -215,14 +309,29 @@ oal_status launch_decode(const void *q, const void *k, const void *v, int is_bf1
   if (cudaMemsetAsync(tickets, 0, units * sizeof(unsigned), stream) != cudaSuccess)
     return oal_check_launch("decode ticket reset");
   dim3 grid(nslices, (unsigned)units);
+  const size_t smem = decode_smem_floats(rpb) * sizeof(float);
+  static bool attr_set[256] = {};   // per device: the slice buffer is above 48 KB
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256)
+    return oal_check_launch("decode: cudaGetDevice");
+  if (!attr_set[dev]) {
+    const int bytes = (int)(decode_smem_floats(kMaxRowsPerBlock) * sizeof(float));
+    if (cudaFuncSetAttribute(decode_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes) != cudaSuccess)
+      return oal_check_launch("decode: shared memory attribute");
+    attr_set[dev] = true;
+  }
   if (is_bf16)
-    decode_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
+    decode_kernel<__nv_bfloat16><<<grid, kThreads, smem, stream>>>(
         (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
-        (__nv_bfloat16 *)y, a, b, C, state, Hq, Hkv, F, packed, nslices, partial, tickets);
+        (__nv_bfloat16 *)y, a, b, C, state, Hq, Hkv, F, packed, rpb, nslices, partial, tickets,
+        oal_device_status_word());
   else
-    decode_kernel<float><<<grid, kThreads, 0, stream>>>(
+    decode_kernel<float><<<grid, kThreads, smem, stream>>>(
         (const float *)q, (const float *)k, (const float *)v, (float *)y, a, b, C, state,
-        Hq, Hkv, F, packed, nslices, partial, tickets);
+        Hq, Hkv, F, packed, rpb, nslices, partial, tickets, oal_device_status_word());
   return oal_after_launch("decode_kernel", stream);
 }
 

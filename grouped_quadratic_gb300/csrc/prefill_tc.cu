@@ -221,49 +221,55 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
   }
   // quadratic form, one entry per thread: sbar_g = sum_v A[g][v] z_v with
   // z_0 = s, z_i = tail sum i; sbar_{g*} = (z_0 - sum_i z_i) / 8,
-  // sbar_{g_i} = z_i / 8; M = L L^T.  A[g][v] is formed on the fly.
+  // sbar_{g_i} = z_i / 8; M = L L^T.  A[g][v] has at most two non-zero
+  // rows per column, so every entry is a sum of at most four terms of M.
   __shared__ int slot_group[8];     // tail slot -> group
+  __shared__ double sM[8][8];       // M = L L^T in fp64, one entry per thread
   if (tid == 0) {
     int slot = 0;
     for (int g = 1; g <= G; ++g)
       if (g != gstar) slot_group[++slot] = g;   // z index slot (1-based)
   }
-  __syncthreads();
-  auto Aat = [&](int g, int v) -> double {     // d sbar_g / d z_v
-    if (v == 0) return g == gstar ? 0.125 : 0.0;
-    if (g == gstar) return -0.125;
-    return slot_group[v] == g ? 0.125 : 0.0;
-  };
-  auto Mat = [&](int g, int h2) -> double {
+  if (tid < G1 * G1) {
+    const int g = tid / G1, h2 = tid % G1;
     double m = 0.0;
     for (int c = 0; c <= (g < h2 ? g : h2); ++c) m += (double)Lat(g, c) * (double)Lat(h2, c);
-    return m;
+    sM[g][h2] = m;
+  }
+  __syncthreads();
+  // the (at most two) groups g with d sbar_g / d z_v != 0, and those values
+  auto deps = [&](int v, int (&gs)[2], double (&as)[2]) -> int {
+    if (v == 0) { gs[0] = gstar; as[0] = 0.125; return 1; }
+    gs[0] = gstar; as[0] = -0.125;
+    gs[1] = slot_group[v]; as[1] = 0.125;
+    return 2;
   };
   const int nq = G * (G + 1) / 2;
   if (tid < nq) {
     int v = 0, rem = tid;
     while (rem >= G - v) { rem -= G - v; ++v; }
     const int w2 = v + rem;
+    int gv[2], gw[2];
+    double av[2], aw[2];
+    const int nv = deps(v, gv, av), nw = deps(w2, gw, aw);
     double q = 0.0;
-    for (int g = 1; g <= G; ++g) {
-      const double ag = Aat(g, v);
-      if (ag == 0.0) continue;
-      for (int h2 = 1; h2 <= G; ++h2) {
-        const double ah = Aat(h2, w2);
-        if (ah != 0.0) q += ag * Mat(g, h2) * ah;
-      }
-    }
+    for (int i = 0; i < nv; ++i)
+      for (int j = 0; j < nw; ++j) q += av[i] * sM[gv[i]][gw[j]] * aw[j];
     P->quad[tid] = (float)(w2 == v ? q : 2.0 * q);
   } else if (tid < 36) {
     P->quad[tid] = 0.f;
   } else if (tid >= 64 && tid < 72) {
     const int v = tid - 64;
     double l = 0.0;
-    if (v < G)
-      for (int g = 1; g <= G; ++g) l += 2.0 * Mat(0, g) * Aat(g, v);
+    if (v < G) {
+      int gv[2];
+      double av[2];
+      const int nv = deps(v, gv, av);
+      for (int i = 0; i < nv; ++i) l += 2.0 * sM[0][gv[i]] * av[i];
+    }
     P->lin[v] = (float)l;
   } else if (tid == 96) {
-    P->c0 = (float)((double)eps + Mat(0, 0));
+    P->c0 = (float)((double)eps + sM[0][0]);
   }
 }
 
@@ -301,7 +307,7 @@ constexpr int kStateStages = 3;
 struct __align__(1024) StateSmem {
   __nv_bfloat16 kv[kStateStages][2][kC * 64];   // [stage][K | V] 128B-swizzled tiles
   __nv_bfloat16 ones[kC * 64];                  // MN-major B tile whose column 0 is 1
-  // K transposed, [dim][token]; the 16-byte chunk c of row r sits at c ^ (r >> 3)
+  // K transposed, [dim][token]; the 16-byte chunk c of row r sits at c ^ kt_swz(r)
   __nv_bfloat16 kT[64][kC];
   uint64_t kv_full[kStateStages], kv_empty[kStateStages];
   uint64_t a_full[2], a_empty[2], d_full[2], d_empty[2];
@@ -328,6 +334,11 @@ __device__ __forceinline__ uint32_t hfma2_bf16(uint32_t a, uint32_t b, uint32_t 
   asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
   return r;
 }
+
+// Swizzle of the transposed K tile: conflict-free for the transpose's writes
+// (8 rows 8 apart, same chunk) and at most 2-way for the builders' reads (8
+// consecutive rows, same chunk).
+__device__ __forceinline__ int kt_swz(int r) { return (r & 7) ^ ((r >> 3) & 7); }
 
 __global__ void __launch_bounds__(kStateThreads, 1)
 tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -454,8 +465,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           lo.z = __byte_perm(v[4][j], v[5][j], 0x5410); hi.z = __byte_perm(v[4][j], v[5][j], 0x7632);
           lo.w = __byte_perm(v[6][j], v[7][j], 0x5410); hi.w = __byte_perm(v[6][j], v[7][j], 0x7632);
           const int r0 = 8 * db8 + 2 * j;
-          *reinterpret_cast<uint4 *>(&s.kT[r0][8 * (tb8 ^ db8)]) = lo;
-          *reinterpret_cast<uint4 *>(&s.kT[r0 + 1][8 * (tb8 ^ db8)]) = hi;
+          *reinterpret_cast<uint4 *>(&s.kT[r0][8 * (tb8 ^ kt_swz(r0))]) = lo;
+          *reinterpret_cast<uint4 *>(&s.kT[r0 + 1][8 * (tb8 ^ kt_swz(r0 + 1))]) = hi;
         }
       }
       named_bar(1, 128);
@@ -481,7 +492,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           const uint4 *kr = reinterpret_cast<const uint4 *>(&s.kT[rr][0]);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const uint4 x = kr[(4 * q + v) ^ (rr >> 3)];
+            const uint4 x = kr[(4 * q + v) ^ kt_swz(rr)];
             hi[4 * v] = x.x; hi[4 * v + 1] = x.y; hi[4 * v + 2] = x.z; hi[4 * v + 3] = x.w;
             lo[4 * v] = lo[4 * v + 1] = lo[4 * v + 2] = lo[4 * v + 3] = 0u;
           }
@@ -491,7 +502,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           const uint4 *kt = reinterpret_cast<const uint4 *>(&s.kT[tt][0]);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const uint4 x = kr[(4 * q + v) ^ (rr >> 3)], y = kt[(4 * q + v) ^ (tt >> 3)];
+            const uint4 x = kr[(4 * q + v) ^ kt_swz(rr)], y = kt[(4 * q + v) ^ kt_swz(tt)];
             const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -1167,11 +1178,11 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         while (hh >= nh) { hh -= nh; ++kb; }
       }
     }
-    if (warp < 4) {
+    {
       // ---------------- epilogue: y = (u~ + intra)[0:64] / (u~ + intra)[64].
-      // The intra-chunk rows of every head are loaded before the wait so the
-      // global-memory latency overlaps the last UMMAs; one head at a time
-      // keeps the registers in bounds.
+      // Builder group g3 finishes the heads g3, g3 + 3, ...  The intra-chunk
+      // rows of a head are loaded before they are needed so the global-memory
+      // latency overlaps the last UMMAs (first head) or the previous head.
       const int i_tok = c * kC + m;
       const bool row_ok = i_tok < args.T;
       const size_t row0 = ((size_t)bidx * args.Hq + h0) * args.T + i_tok;
@@ -1186,10 +1197,10 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           iden = __ldg(args.intra_den + row);
         }
       };
-      load_intra(0);
-      if (!*abort_flag && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
+      if (g3 < nh) load_intra(g3);
+      if (g3 < nh && !*abort_flag && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
         tc_fence_after();
-        for (int hh = 0; hh < nh; ++hh) {
+        for (int hh = g3; hh < nh; hh += 3) {
           // denominator column first, then the values 16 columns at a time
           uint32_t r[16];
           tmem_ld16(tmem_lane_addr(tb, warp, kTmemD + 80 * hh + 64), r);
@@ -1214,7 +1225,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
               dst[2 * q4 + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
           }
-          if (hh + 1 < nh) load_intra(hh + 1);
+          if (hh + 3 < nh) load_intra(hh + 3);
         }
       }
     }
