@@ -295,22 +295,25 @@ __device__ __forceinline__ void named_bar(int id, int n) {
 
 // ================================================================= state kernel
 // One block per (128-feature tile, part of the sequence, batch x KV head).
-// Per chunk c of the part: Delta S_c = phi(K_c)^T [V_c | 1] by UMMA into one
-// of two tensor-memory accumulators; phi is split exactly into two bf16
-// terms (hi = bf16(k_r k_t), lo = k_r k_t - hi; the product of two bf16
-// values has at most 16 significant bits), so the fp32 state is exact up to
-// fp32 accumulation.  The epilogue warps keep the running fp32 state of their
+// Per chunk c of the part: Delta S_c = phi(K_c)^T V_c by UMMA into one of two
+// tensor-memory accumulators; phi is split exactly into two bf16 terms
+// (hi = bf16(k_r k_t), lo = k_r k_t - hi; the product of two bf16 values has
+// at most 16 significant bits), so the fp32 state is exact up to fp32
+// accumulation.  The "1" column, sum_j phi(k_j), is summed in fp32 by the
+// builders (an N = 16 UMMA for one column costs as much tensor time as the
+// value columns).  The epilogue warps keep the running fp32 state of their
 // feature row in registers, add each Delta S_c, and (mode 1) write the bf16
 // snapshot S_{c-1} that the readout of chunk c consumes.
 constexpr int kStateStages = 3;
 
 struct __align__(1024) StateSmem {
   __nv_bfloat16 kv[kStateStages][2][kC * 64];   // [stage][K | V] 128B-swizzled tiles
-  __nv_bfloat16 ones[kC * 64];                  // MN-major B tile whose column 0 is 1
   // K transposed, [dim][token]; the 16-byte chunk c of row r sits at c ^ kt_swz(r)
   __nv_bfloat16 kT[64][kC];
   uint64_t kv_full[kStateStages], kv_empty[kStateStages];
   uint64_t a_full[2], a_empty[2], d_full[2], d_empty[2];
+  uint64_t sum_full[4];                          // "1"-column sums of a chunk are ready
+  float osum[4][2][128];                         // [chunk & 3][builder group][feature]
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -325,9 +328,21 @@ struct StateArgs {
   int *status;
 };
 
-constexpr int kStateThreads = 384;
-constexpr int kStateD = 0;          // accumulators at cols 0 and 128 (80 wide)
+constexpr int kStateThreads = 512;
+constexpr int kStateD = 0;          // accumulators at cols 0 and 128 (64 wide)
 constexpr int kStateA = 256;        // A slots at 256 and 384: [hi 64 | lo 64]
+
+__device__ __forceinline__ float bf16lo_f32(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16hi_f32(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {   // a * b + c, two lanes
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
 
 __device__ __forceinline__ uint32_t hfma2_bf16(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t r;
@@ -360,26 +375,17 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       mbar_init(&s.kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.a_full[i], 4);
-      mbar_init(&s.a_empty[i], 2);   // both issuers
-      mbar_init(&s.d_full[i], 2);    // both issuers
+      mbar_init(&s.a_full[i], 8);    // every builder warp
+      mbar_init(&s.a_empty[i], 1);
+      mbar_init(&s.d_full[i], 1);
       mbar_init(&s.d_empty[i], 4);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(&s.sum_full[i], 8);
     fence_mbar_init();
   }
   if (warp == 1) {
     tmem_alloc(&s.tmem_base, 512);
     tmem_relinquish();
-  }
-  if (warp >= 4 && warp < 8) {
-    // ones tile (MN-major B of the "1" column): row j = token j, element 0 = 1
-    const int j = tid - 128;
-    for (int c = 0; c < 8; ++c) {
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (c == 0) v.x = 0x3F80u;
-      *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(s.ones) + sw128(j, c)) = v;
-    }
-    fence_proxy_async();
   }
   tc_fence_before();
   __syncthreads();
@@ -407,28 +413,26 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
         mbar_wait_teardown(&s.kv_full[i % kStateStages], (i / kStateStages) & 1, args.status);
     }
     __syncwarp();
-  } else if (warp == 1 || warp == 2) {
+  } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------- MMA issuers: warp 1 D[:, 0:64] += A x V_c (N = 64),
-      // warp 2 D[:, 64:80] += A x [1] (N = 16); A = phi(K_c)^T as hi | lo, K = 256
-      const bool vpart = warp == 1;
-      const uint32_t idn = vpart ? idesc_bf16_f32(128, 64, 1) : idesc_bf16_f32(128, 16, 1);
+      // ---------------- MMA issuer: D[:, 0:64] += A x V_c (N = 64), A = phi(K_c)^T
+      // as hi | lo, K = 256; V read MN-major straight from the TMA stage
+      const uint32_t idn = idesc_bf16_f32(128, 64, 1);
       const uint64_t vdesc0 = sdesc_sw128(smem_u32(s.kv[0][1]), 16, 1024);
-      const uint64_t odesc = sdesc_sw128(smem_u32(s.ones), 16, 1024);
       constexpr uint64_t kKVStep = (2 * kC * 64 * 2) >> 4;   // one K|V stage
       for (int i = 0; i < nchunks; ++i) {
         const int sl = i & 1, st = i % kStateStages;
         if (!mbar_wait(&s.a_full[sl], (i >> 1) & 1, abort_flag, args.status)) break;
         if (!mbar_wait(&s.d_empty[sl], ((i >> 1) & 1) ^ 1, abort_flag, args.status)) break;
         tc_fence_after();
-        const uint64_t bd = vpart ? vdesc0 + kKVStep * st : odesc;
-        const uint32_t d = tb + kStateD + 128 * sl + (vpart ? 0 : 64);
+        const uint64_t bd = vdesc0 + kKVStep * st;
+        const uint32_t d = tb + kStateD + 128 * sl;
         const uint32_t a0 = tb + kStateA + 128 * sl;
 #pragma unroll
         for (int k = 0; k < 16; ++k)       // K = 256: hi half then lo half
           umma_ts(d, a0 + 8 * k, bd + (uint64_t)(128 * (k & 7)), idn, k > 0 ? 1u : 0u);
         umma_commit(&s.a_empty[sl]);
-        if (vpart) umma_commit(&s.kv_empty[st]);
+        umma_commit(&s.kv_empty[st]);
         umma_commit(&s.d_full[sl]);
       }
       // no MMA in flight at dealloc: drain through the accumulator barriers
@@ -436,17 +440,19 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
         mbar_wait_teardown(&s.d_full[i & 1], (i >> 1) & 1, args.status);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 8) {
-    // ---------------- builders: transpose K, then A = phi(K_c)^T (hi | lo)
-    const int l = tid - 128;                 // TMEM lane = feature row, = token when transposing
+  } else if (warp >= 4 && warp < 12) {
+    // ---------------- builders: group 0 (warps 4-7) transposes K; then group
+    // bg builds tokens 64 bg .. 64 bg + 63 of A = phi(K_c)^T (hi | lo)
+    const int bg = (warp - 4) >> 2;
+    const int l = 32 * (warp & 3) + lane;    // TMEM lane = feature row, = token when transposing
     const int f = tile * 128 + l;
     const uint16_t code = f < kKP ? g_feat.code[f] : (uint16_t)0xFFFF;
     for (int i = 0; i < nchunks; ++i) {
       const int sl = i & 1, st = i % kStateStages;
       const int c = c0 + i;
       if (!mbar_wait(&s.kv_full[st], (i / kStateStages) & 1, abort_flag, args.status)) break;
-      named_bar(1, 128);   // the previous chunk's builds are done with kT
-      {
+      named_bar(1, 256);   // the previous chunk's builds are done with kT
+      if (bg == 0) {
         // 8 x 8 block transpose: thread (tb8, db8) moves tokens 8 tb8 .. +7 x
         // dims 8 db8 .. +7 from the K tile into kT with 16-byte accesses
         const int tb8 = l >> 3, db8 = l & 7;
@@ -469,13 +475,15 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           *reinterpret_cast<uint4 *>(&s.kT[r0 + 1][8 * (tb8 ^ kt_swz(r0 + 1))]) = hi;
         }
       }
-      named_bar(1, 128);
+      named_bar(1, 256);
       // slot sl (A in tensor memory) is free once the UMMAs of chunk i - 2 are done
       if (!mbar_wait(&s.a_empty[sl], ((i >> 1) & 1) ^ 1, abort_flag, args.status)) break;
       const int nvalid = min(kC, args.T - c * kC);
       const uint32_t abase = kStateA + 128 * sl;
+      float2 osum = make_float2(0.f, 0.f);    // sum over this group's tokens of phi_f(k_j)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int qq = 0; qq < 2; ++qq) {
+        const int q = 2 * bg + qq;           // 32-token block
         uint32_t hi[16], lo[16];
         if (code == 0xFFFF) {
 #pragma unroll
@@ -487,6 +495,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
             hi[w] = (j < nvalid ? 0x3F80u : 0u) | (j + 1 < nvalid ? 0x3F800000u : 0u);
             lo[w] = 0u;
           }
+          osum.x += (float)min(32, max(0, nvalid - 32 * q));
         } else if (code & 0x8000) {
           const int rr = code & 0xff;
           const uint4 *kr = reinterpret_cast<const uint4 *>(&s.kT[rr][0]);
@@ -495,6 +504,11 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
             const uint4 x = kr[(4 * q + v) ^ kt_swz(rr)];
             hi[4 * v] = x.x; hi[4 * v + 1] = x.y; hi[4 * v + 2] = x.z; hi[4 * v + 3] = x.w;
             lo[4 * v] = lo[4 * v + 1] = lo[4 * v + 2] = lo[4 * v + 3] = 0u;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              osum.x += bf16lo_f32(hi[4 * v + e]);
+              osum.y += bf16hi_f32(hi[4 * v + e]);
+            }
           }
         } else {
           const int rr = code >> 8, tt = code & 0xff;
@@ -509,20 +523,28 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
               const uint32_t h2 = hmul2(xs[e], ys[e]);
               hi[4 * v + e] = h2;
               lo[4 * v + e] = hfma2_bf16(xs[e], ys[e], h2 ^ 0x80008000u);   // exact residual
+              // the products of bf16 values are exact in fp32
+              osum = ffma2(make_float2(bf16lo_f32(xs[e]), bf16hi_f32(xs[e])),
+                           make_float2(bf16lo_f32(ys[e]), bf16hi_f32(ys[e])), osum);
             }
           }
         }
         tmem_st16(tmem_lane_addr(tb, warp, abase + 16 * q), hi);
         tmem_st16(tmem_lane_addr(tb, warp, abase + 64 + 16 * q), lo);
       }
+      // rows with t < r (duplicates) still carry their sum: the epilogue drops them
+      s.osum[i & 3][bg][l] = osum.x + osum.y;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.a_full[sl]);
+      if (lane == 0) {
+        mbar_arrive(&s.a_full[sl]);
+        mbar_arrive(&s.sum_full[i & 3]);
+      }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ---------------- epilogue: running fp32 state of this feature row
-    const int l = tid - 256;
+    const int l = tid - 384;
     const int f = tile * 128 + l;
     const uint16_t code = f < kKP ? g_feat.code[f] : (uint16_t)0xFFFF;
     int mirror;
@@ -565,14 +587,17 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       if (!mbar_wait(&s.d_full[sl], (i >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
-      for (int q = 0; q < kN / 16; ++q) {
+      for (int q = 0; q < kDv / 16; ++q) {
         uint32_t r[16];
         tmem_ld16(tmem_lane_addr(tb, warp, kStateD + 128 * sl + 16 * q), r);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          if (16 * q + e < kU) S[16 * q + e] += __uint_as_float(r[e]);
+        for (int e = 0; e < 16; ++e) S[16 * q + e] += __uint_as_float(r[e]);
       }
+      // the "1" column from the builders' sums (read before d_empty is
+      // released: the slot is rewritten four chunks later)
+      if (!mbar_wait(&s.sum_full[i & 3], (i >> 2) & 1, abort_flag, args.status)) { ok = false; break; }
+      S[kDv] += s.osum[i & 3][0][l] + s.osum[i & 3][1][l];
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.d_empty[sl]);
@@ -1276,7 +1301,7 @@ static Layout plan_layout(int B, int Hq, int Hkv, int T) {
   Layout L{};
   L.U = B * Hkv;
   L.nC = (T + kC - 1) / kC;
-  int P = (2 * 152 + kTiles * L.U - 1) / (kTiles * L.U);
+  int P = 152 / (kTiles * L.U);   // one wave: every CTA walks its part once
   P = P < 1 ? 1 : (P > L.nC ? L.nC : P);
   L.cpp = (L.nC + P - 1) / P;
   L.nparts = (L.nC + L.cpp - 1) / L.cpp;

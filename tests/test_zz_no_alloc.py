@@ -68,10 +68,13 @@ def test_noalloc_matches_prefill_on_two_calls(oal, dtype, layout):
 
 
 def test_noalloc_rejects_problems_above_its_scratch(oal):
-    B, Hq, Hkv, T = 1, 14, 2, 6017     # bf16 needs just over 64 MiB of scratch here
-    need = oal.oal_prefill_workspace_bytes(B, Hq, Hkv, T, dtype=oal.OAL_BF16,
-                                           layout=PACKED)
-    assert need > oal.OAL_PREFILL_NOALLOC_SCRATCH_BYTES
+    B, Hq, Hkv = 1, 14, 2
+    # the shortest sequence whose scratch need is above the fixed array
+    T = 128
+    while oal.oal_prefill_workspace_bytes(B, Hq, Hkv, T, dtype=oal.OAL_BF16,
+                                          layout=PACKED) <= oal.OAL_PREFILL_NOALLOC_SCRATCH_BYTES:
+        T += 128
+    need = oal.oal_prefill_workspace_bytes(B, Hq, Hkv, T, dtype=oal.OAL_BF16, layout=PACKED)
     z = lambda *shape, dt=torch.bfloat16: torch.zeros(*shape, dtype=dt, device="cuda")
     Q, K, V = z(B, Hq, T, 64), z(B, Hkv, T, 64), z(B, Hkv, T, 64)
     L = torch.eye(5, dtype=torch.float32, device="cuda")[None].repeat(Hq, 1, 1)
