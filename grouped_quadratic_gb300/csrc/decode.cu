@@ -52,6 +52,8 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
               const float *__restrict__ Ctab, float *__restrict__ state, int Hq,
               int Hkv, int F, int packed, int rows_per_block, int nslices,
               float *__restrict__ partial, unsigned *__restrict__ tickets, int *status) {
+  pdl_trigger();
+  pdl_wait();
   const int rho = Hq / Hkv;
   const int slice = blockIdx.x;
   const int unit = blockIdx.y;              // b * Hkv + kv
@@ -324,14 +326,14 @@ oal_status launch_decode(const void *q, const void *k, const void *v, int is_bf1
     attr_set[dev] = true;
   }
   if (is_bf16)
-    decode_kernel<__nv_bfloat16><<<grid, kThreads, smem, stream>>>(
-        (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
-        (__nv_bfloat16 *)y, a, b, C, state, Hq, Hkv, F, packed, rpb, nslices, partial, tickets,
-        oal_device_status_word());
+    launch_pdl(decode_kernel<__nv_bfloat16>, grid, dim3(kThreads), smem, stream,
+               (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
+               (__nv_bfloat16 *)y, a, b, C, state, Hq, Hkv, F, packed, rpb, nslices, partial,
+               tickets, oal_device_status_word());
   else
-    decode_kernel<float><<<grid, kThreads, smem, stream>>>(
-        (const float *)q, (const float *)k, (const float *)v, (float *)y, a, b, C, state,
-        Hq, Hkv, F, packed, rpb, nslices, partial, tickets, oal_device_status_word());
+    launch_pdl(decode_kernel<float>, grid, dim3(kThreads), smem, stream, (const float *)q,
+               (const float *)k, (const float *)v, (float *)y, a, b, C, state, Hq, Hkv, F, packed,
+               rpb, nslices, partial, tickets, oal_device_status_word());
   return oal_after_launch("decode_kernel", stream);
 }
 

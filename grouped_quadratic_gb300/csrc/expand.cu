@@ -22,6 +22,8 @@ __global__ void expand_coeffs_kernel(const float *__restrict__ L,
                                      float eps, int packed, float *__restrict__ a,
                                      float *__restrict__ b, float *__restrict__ C,
                                      int *status) {
+  pdl_trigger();
+  pdl_wait();
   const int h = blockIdx.x;
   const int G1 = G + 1;
   __shared__ double M[(kMaxG + 1) * (kMaxG + 1)];
@@ -51,17 +53,21 @@ __global__ void expand_coeffs_kernel(const float *__restrict__ L,
     M2f[n] = __double2float_rn(__dmul_rn(2.0, M[n]));
   }
   __syncthreads();
-  if (threadIdx.x == 0) a[h] = __double2float_rn(__dadd_rn((double)eps, M[0]));
-  for (int r = threadIdx.x; r < kD; r += blockDim.x) b[(size_t)h * kD + r] = M2f[grp[r]];
+  // blockIdx.y splits the C table; block 0 also writes a and b
+  const int n0 = blockIdx.y * blockDim.x + threadIdx.x, nstep = blockDim.x * gridDim.y;
+  if (blockIdx.y == 0) {
+    if (threadIdx.x == 0) a[h] = __double2float_rn(__dadd_rn((double)eps, M[0]));
+    for (int r = threadIdx.x; r < kD; r += blockDim.x) b[(size_t)h * kD + r] = M2f[grp[r]];
+  }
   if (!packed) {
     float *Ch = C + (size_t)h * kH2Full;
-    for (int n = threadIdx.x; n < kH2Full; n += blockDim.x) {
+    for (int n = n0; n < kH2Full; n += nstep) {
       const int r = n / kD, t = n % kD;
       Ch[n] = Mf[grp[r] * G1 + grp[t]];
     }
   } else {
     float *Ch = C + (size_t)h * kH2Packed;
-    for (int n = threadIdx.x; n < kH2Packed; n += blockDim.x) {
+    for (int n = n0; n < kH2Packed; n += nstep) {
       const int r = c_pairs.rt[n] >> 8, t = c_pairs.rt[n] & 0xff;
       const int idx = grp[r] * G1 + grp[t];
       Ch[n] = r == t ? Mf[idx] : M2f[idx];
@@ -72,8 +78,8 @@ __global__ void expand_coeffs_kernel(const float *__restrict__ L,
 oal_status launch_expand_coeffs(const float *L, const int32_t *group, int Hq,
                                 int G, float eps, int packed, float *a, float *b,
                                 float *C, cudaStream_t stream) {
-  expand_coeffs_kernel<<<Hq, 256, 0, stream>>>(L, group, G, eps, packed, a, b, C,
-                                               oal_device_status_word());
+  launch_pdl(expand_coeffs_kernel, dim3(Hq, 4), dim3(256), 0, stream, L, group, G, eps, packed,
+             a, b, C, oal_device_status_word());
   return oal_after_launch("expand_coeffs_kernel", stream);
 }
 

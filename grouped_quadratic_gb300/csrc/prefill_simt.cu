@@ -48,6 +48,8 @@ template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
 chunk_delta_kernel(const Tin *__restrict__ K, const Tin *__restrict__ V, int T,
                    int C, int nC, int F, int packed, float *__restrict__ ws) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float sm[];
   float *ks = sm;                     // [64 tokens][kP]
   float *us = ks + kTile * kP;        // [64 tokens][kP]  (u = [v; 1])
@@ -103,6 +105,8 @@ chunk_delta_kernel(const Tin *__restrict__ K, const Tin *__restrict__ V, int T,
 // Exclusive prefix over chunks, in place: ws[c] <- S0 + sum_{c' < c} Delta S_c'.
 __global__ void chunk_scan_kernel(float *__restrict__ ws, int nC, size_t FU,
                                   float *__restrict__ state, int cont) {
+  pdl_trigger();
+  pdl_wait();
   const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t unit = blockIdx.y;
   if (e >= FU) return;
@@ -125,6 +129,8 @@ readout_kernel(const Tin *__restrict__ Q, const Tin *__restrict__ K,
                const float *__restrict__ L, const int32_t *__restrict__ group,
                int G, float eps, int Hq, int Hkv, int T, int C, int nC, int F,
                int packed, int *status) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float sm[];
   float *qs = sm;                        // [64 rows][kP]  q (natural order)
   float *qp = qs + kTile * kP;           // [64 rows][kP]  q (group order)
@@ -332,19 +338,18 @@ static oal_status launch_simt(const Tin *Q, const Tin *K, const Tin *V, int B,
     attr_done = true;
   }
   dim3 g1((F + kTile - 1) / kTile, nC, B * Hkv);
-  chunk_delta_kernel<Tin><<<g1, kThreads, delta_smem(), stream>>>(K, V, T, chunk, nC, F,
-                                                                  packed, ws);
+  launch_pdl(chunk_delta_kernel<Tin>, g1, dim3(kThreads), delta_smem(), stream, K, V, T, chunk,
+             nC, F, packed, ws);
   oal_status st = oal_after_launch("chunk_delta_kernel", stream);
   if (st != OAL_OK) return st;
   const size_t FU = (size_t)F * kU;
   dim3 g2((unsigned)((FU + 255) / 256), B * Hkv);
-  chunk_scan_kernel<<<g2, 256, 0, stream>>>(ws, nC, FU, state, cont);
+  launch_pdl(chunk_scan_kernel, g2, dim3(256), 0, stream, ws, nC, FU, state, cont);
   st = oal_after_launch("chunk_scan_kernel", stream);
   if (st != OAL_OK) return st;
   dim3 g3(nC * (chunk / kTile), B * Hq);
-  readout_kernel<Tin><<<g3, kThreads, readout_smem(), stream>>>(
-      Q, K, V, Y, ws, a, b, C, L, group, G, eps, Hq, Hkv, T, chunk, nC, F, packed,
-      oal_device_status_word());
+  launch_pdl(readout_kernel<Tin>, g3, dim3(kThreads), readout_smem(), stream, Q, K, V, Y, ws, a, b,
+             C, L, group, G, eps, Hq, Hkv, T, chunk, nC, F, packed, oal_device_status_word());
   return oal_after_launch("readout_kernel", stream);
 }
 

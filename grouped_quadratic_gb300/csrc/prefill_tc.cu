@@ -141,6 +141,8 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
                const float *__restrict__ Ctab, const float *__restrict__ L,
                const int32_t *__restrict__ group, int G, float eps, int packed,
                __nv_bfloat16 *__restrict__ coef, KPlan *__restrict__ plans, int *status) {
+  pdl_trigger();
+  pdl_wait();
   const int h = blockIdx.x;
   const int tid = threadIdx.x;
   const int G1 = G + 1;
@@ -156,9 +158,12 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
     sgrp[tid] = g;
     atomicAdd(&scnt[g], 1);
   }
-  // readout weights in the internal feature order (blockIdx.y splits the rows)
+  // readout weights in the internal feature order (blockIdx.y < gridDim.y - 1
+  // split the rows); the last block row forms the kappa plan meanwhile
+  const int ncoef = gridDim.y - 1;
   const float *Ch = Ctab + (size_t)h * (packed ? kH2Packed : kH2Full);
-  for (int f = blockIdx.y * blockDim.x + tid; f < kKP; f += blockDim.x * gridDim.y) {
+  for (int f = blockIdx.y * blockDim.x + tid; blockIdx.y < ncoef && f < kKP;
+       f += blockDim.x * ncoef) {
     const uint16_t code = g_feat.code[f];
     float w = 0.f;
     if (code == 0xC000) {
@@ -176,7 +181,7 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
     coef[(size_t)h * kKP + f] = __float2bfloat16_rn(w);
   }
   __syncthreads();
-  if (blockIdx.y != 0) return;
+  if (blockIdx.y != ncoef) return;
   // kappa constants: the bulk group g* is the largest; the others are tail groups
   int gstar = 1;
   for (int g = 2; g <= G; ++g)
@@ -367,6 +372,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
   const int c1 = min(args.nC, c0 + args.cpp);
   const int nchunks = c1 - c0;
   const int mode = args.mode;
+  pdl_trigger();
 
   if (tid == 0) {
     s.abort_flag = 0;
@@ -392,6 +398,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
   tc_fence_after();
   const uint32_t tb = s.tmem_base;
   volatile int *abort_flag = &s.abort_flag;
+  pdl_wait();   // inputs, part totals and snapshots of the previous kernels
 
   if (warp == 0) {
     if (lane == 0) {
@@ -652,7 +659,7 @@ struct __align__(1024) IntraSmem {
   __nv_bfloat16 q[kIntraNH][kC * 64];
   __nv_bfloat16 k[kC * 64];
   __nv_bfloat16 v[kC * 64];
-  float kt[kIntraNH][kC][kTailSlots];  // tail-dim key values (fast path)
+  float kt[kIntraNH][kTailSlots][kC];  // tail-dim key values (fast path), key-major
   KPlan plan[kIntraNH];
   uint64_t qkv_full, s_full[2], p_full[2], s_free[2], d_full;
   uint32_t tmem_base;
@@ -670,7 +677,7 @@ struct ReadArgs {
   int *status;
 };
 
-constexpr int kReadThreads = 512;   // 16 warps
+constexpr int kReadThreads = 640;   // 20 warps
 constexpr int kTmemD = 0;         // D^h at [80h, 80h + 80)
 constexpr int kTmemA = 320;       // six A slots of 32 columns at [320, 512)
 constexpr uint32_t kReadTmemCols = 512;
@@ -689,33 +696,46 @@ __device__ __forceinline__ uint32_t h2_pair(const uint32_t (&q)[32], uint32_t cw
   return hmul2(hmul2(qr, q[t >> 1]), cw);
 }
 
-template <int KB, int... P>
-__device__ __forceinline__ void h2_block(const uint32_t (&q)[32], const uint32_t (&cw)[32],
-                                         uint32_t (&out)[32], std::integer_sequence<int, P...>) {
-  ((out[P] = h2_pair<KB, P>(q, cw[P])), ...);
+template <int KB, int H, int... P>
+__device__ __forceinline__ void h2_half(const uint32_t (&q)[32], const uint32_t (&cw)[16],
+                                        uint32_t (&out)[16], std::integer_sequence<int, P...>) {
+  ((out[P] = h2_pair<KB, 16 * H + P>(q, cw[P])), ...);
 }
 
-template <int KB>
-__device__ __forceinline__ void build_block(const uint32_t (&q)[32], const uint32_t (&cw)[32],
-                                            uint32_t (&out)[32]) {
-  if constexpr (KB < 33) {
-    h2_block<KB>(q, cw, out, std::make_integer_sequence<int, 32>{});
-  } else if constexpr (KB == 33) {
+// Words 16 H .. 16 H + 15 of K block KB of one A row (token row of Phi~(Q)):
+// the weights come from this head's table in shared memory (cp = block KB).
+template <int KB, int H>
+__device__ __forceinline__ void build_half(const uint32_t (&q)[32], const uint4 *cp,
+                                           uint32_t (&out)[16]) {
+  if constexpr (KB < kNKB - 1) {
+    uint32_t cw[16];
 #pragma unroll
-    for (int p = 0; p < 32; ++p) out[p] = hmul2(q[p], cw[p]);
+    for (int e = 0; e < 4; ++e) {
+      const uint4 v = cp[4 * H + e];
+      cw[4 * e] = v.x; cw[4 * e + 1] = v.y; cw[4 * e + 2] = v.z; cw[4 * e + 3] = v.w;
+    }
+    if constexpr (KB < 33) {
+      h2_half<KB, H>(q, cw, out, std::make_integer_sequence<int, 16>{});
+    } else {
+#pragma unroll
+      for (int p = 0; p < 16; ++p) out[p] = hmul2(q[16 * H + p], cw[p]);
+    }
   } else {
+    // H0 block: feature 2176 carries a, the 15 after it are zero
 #pragma unroll
-    for (int p = 0; p < 32; ++p) out[p] = p == 0 ? (cw[0] & 0xffffu) : 0u;
+    for (int p = 0; p < 16; ++p) out[p] = 0u;
+    if constexpr (H == 0) out[0] = cp[0].x & 0xffffu;
   }
 }
 
 #define OAL_BUILD_CASE(n) \
   case n:                 \
-    build_block<n>(q, cw, out); \
+    build_half<n, H>(q, cp, out); \
     break;
 
-__device__ __forceinline__ void build_dispatch(int kb, const uint32_t (&q)[32],
-                                               const uint32_t (&cw)[32], uint32_t (&out)[32]) {
+template <int H>
+__device__ __forceinline__ void build_dispatch(int kb, const uint32_t (&q)[32], const uint4 *cp,
+                                               uint32_t (&out)[16]) {
   switch (kb) {
     OAL_BUILD_CASE(0) OAL_BUILD_CASE(1) OAL_BUILD_CASE(2) OAL_BUILD_CASE(3)
     OAL_BUILD_CASE(4) OAL_BUILD_CASE(5) OAL_BUILD_CASE(6) OAL_BUILD_CASE(7)
@@ -768,6 +788,35 @@ __device__ __forceinline__ float kappa_g(const KConst<G> &k, float s, const floa
   return fmaxf(kap, k.eps);
 }
 
+// kappa of two keys (j, j + 1) for one query row, two lanes per packed fp32
+// instruction.  kt: this head's key-major tail values, offset to key j.
+template <int G>
+__device__ __forceinline__ float2 kappa2_g(const KConst<G> &k, float2 s,
+                                          const float (&qt)[2 * kMaxTailG], const float *kt) {
+  float2 z[G];
+  z[0] = s;
+#pragma unroll
+  for (int g = 1; g < G; ++g) {
+    const float2 a = *reinterpret_cast<const float2 *>(kt + (2 * g - 2) * kC);
+    const float2 b = *reinterpret_cast<const float2 *>(kt + (2 * g - 1) * kC);
+    z[g] = ffma2(make_float2(qt[2 * g - 2], qt[2 * g - 2]), a,
+                 make_float2(qt[2 * g - 1] * b.x, qt[2 * g - 1] * b.y));
+  }
+  float2 kap = make_float2(k.c0, k.c0);
+  int qi = 0;
+#pragma unroll
+  for (int v = 0; v < G; ++v) {
+    float2 inner = make_float2(k.lin[v], k.lin[v]);
+#pragma unroll
+    for (int w = v; w < G; ++w) {
+      inner = ffma2(make_float2(k.quad[qi], k.quad[qi]), z[w], inner);
+      ++qi;
+    }
+    kap = ffma2(z[v], inner, kap);
+  }
+  return make_float2(fmaxf(kap.x, k.eps), fmaxf(kap.y, k.eps));
+}
+
 // Generic path (a tail group with more than 2 dims): sums straight from the
 // Q and K tiles, constants from shared memory.
 __device__ float kappa_generic(const KPlan &p, float s, const __nv_bfloat16 *qtile,
@@ -809,8 +858,8 @@ __device__ bool intra_worker(IntraSmem &s, const ReadArgs &args, int nh, int war
       float k0 = 0.f, k1 = 0.f;
       if (g < p.ntg && p.nd[g] > 0) k0 = bf16_at(s.k, m, p.dims[g][0]);
       if (g < p.ntg && p.nd[g] > 1) k1 = bf16_at(s.k, m, p.dims[g][1]);
-      s.kt[hh][m][2 * g] = k0;
-      s.kt[hh][m][2 * g + 1] = k1;
+      s.kt[hh][2 * g][m] = k0;
+      s.kt[hh][2 * g + 1][m] = k1;
     }
   }
   named_bar(2, 128);
@@ -840,24 +889,31 @@ __device__ bool intra_worker(IntraSmem &s, const ReadArgs &args, int nh, int war
       const int jbase = 32 * kb;
       uint32_t pk[16];
       if (row_max >= jbase) {
-        uint32_t sv[32];
-        uint32_t r0[16], r1[16];
-        tmem_ld16(tmem_lane_addr(tb, warp, col), r0);
-        tmem_ld16(tmem_lane_addr(tb, warp, col + 16), r1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) { sv[e] = r0[e]; sv[16 + e] = r1[e]; }
         if (fast) {
-          // branch-free: every key is evaluated, the causal mask is a select,
-          // so the 32 independent evaluations interleave
+          // branch-free: every key is evaluated (two per packed instruction),
+          // the causal mask is a select; 16 keys per tensor-memory load
 #pragma unroll
-          for (int jj = 0; jj < 32; jj += 2) {
-            const int j0 = jbase + jj;
-            const float k0 = kappa_g<G>(kc, __uint_as_float(sv[jj]), qt, s.kt[hh][j0]);
-            const float k1 = kappa_g<G>(kc, __uint_as_float(sv[jj + 1]), qt, s.kt[hh][j0 + 1]);
-            pk[jj >> 1] = pack_bf16x2(j0 <= m ? k0 : 0.f, j0 + 1 <= m ? k1 : 0.f);
+          for (int half = 0; half < 2; ++half) {
+            uint32_t sv[16];
+            tmem_ld16(tmem_lane_addr(tb, warp, col + 16 * half), sv);
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 2) {
+              const int j0 = jbase + 16 * half + jj;
+              const float2 kp = kappa2_g<G>(
+                  kc, make_float2(__uint_as_float(sv[jj]), __uint_as_float(sv[jj + 1])), qt,
+                  &s.kt[hh][0][j0]);
+              pk[8 * half + (jj >> 1)] = pack_bf16x2(j0 <= m ? kp.x : 0.f, j0 + 1 <= m ? kp.y : 0.f);
+            }
           }
         } else {
+          uint32_t sv[32];
+          uint32_t r0[16], r1[16];
+          tmem_ld16(tmem_lane_addr(tb, warp, col), r0);
+          tmem_ld16(tmem_lane_addr(tb, warp, col + 16), r1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) { sv[e] = r0[e]; sv[16 + e] = r1[e]; }
           float sl[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) sl[e] = __uint_as_float(sv[e]);
@@ -897,8 +953,10 @@ __device__ bool intra_worker(IntraSmem &s, const ReadArgs &args, int nh, int war
 // query row, written to workspace for the readout's epilogue.
 // Warps 0-3: kappa (thread = query row) and the epilogue; warp 4: UMMA issue
 // (s = Q K^T per 32-key block, then P.V) and tensor memory; warp 5: TMA.
+// Blocks per SM by register need: four for small G (the whole grid of a
+// 4096-token, 14-head chunking fits one wave from three up).
 template <int G>
-__global__ void __launch_bounds__(kIntraThreads, 2)
+__global__ void __launch_bounds__(kIntraThreads, G <= 3 ? 4 : (G <= 5 ? 3 : 2))
 tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, ReadArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -911,6 +969,7 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int nh = min(kIntraNH, args.rho - hg * kIntraNH);
   const int nsteps = 4 * nh;            // (head, 32-key block)
   constexpr int kIss = 4, kTma = 5;
+  pdl_trigger();
 
   if (tid == 0) {
     s.abort_flag = 0;
@@ -927,6 +986,7 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tmem_alloc(&s.tmem_base, kIntraTmemCols);
     tmem_relinquish();
   }
+  pdl_wait();   // plans of the prep kernel; the intra rows of the previous call
   for (int n = tid; n < nh * (int)(sizeof(KPlan) / 4); n += kIntraThreads) {
     const int hh = n / (sizeof(KPlan) / 4), e = n % (sizeof(KPlan) / 4);
     reinterpret_cast<int *>(&s.plan[hh])[e] =
@@ -1035,15 +1095,15 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 }
 
 // ---------------------------------------------------------------- readout kernel
-// Warp roles (16 warps):
-//   0-11   readout A builders, three warps per tensor-memory lane quarter
-//          (group g = warp / 4 builds jobs g, g + 3, ...); warps 0-3 then run
-//          the epilogue
-//   12, 13 readout UMMA issuers (jobs of even / odd index)
-//   14     tensor memory owner
-//   15     TMA producer
-// The accumulators are zeroed first and every UMMA accumulates, so the two
-// issuers need no ordering between them.
+// Warp roles (20 warps):
+//   0-15   readout A builders: group h = warp / 4 builds every K block of the
+//          block's query head h (its Q row stays in registers), then runs the
+//          epilogue of head h
+//   16, 17 readout UMMA issuers (jobs of even / odd index)
+//   18     tensor memory owner
+//   19     TMA producer
+// Job j = 35-block index kb * nh + head; the accumulators are zeroed first and
+// every UMMA accumulates, so the two issuers need no ordering between them.
 __global__ void __launch_bounds__(kReadThreads, 1)
 tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS,
                   ReadArgs args) {
@@ -1056,7 +1116,8 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   const int h0 = kv * args.rho + hg * args.nh_per_block;
   const int nh = min(args.nh_per_block, args.rho - hg * args.nh_per_block);
   const int njobs = kNKB * nh;
-  constexpr int kIss0 = 12, kMem = 14, kTma = 15;
+  constexpr int kIss0 = 16, kMem = 18, kTma = 19;
+  pdl_trigger();
 
   if (tid == 0) {
     s.abort_flag = 0;
@@ -1073,6 +1134,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     tmem_alloc(&s.tmem_base, kReadTmemCols);
     tmem_relinquish();
   }
+  pdl_wait();   // weights, snapshots and intra rows of the previous kernels
   for (int n = tid; n < nh * (kKP / 8); n += kReadThreads) {
     const int hh = n / (kKP / 8), e = n % (kKP / 8);
     reinterpret_cast<uint4 *>(s.coef[hh])[e] =
@@ -1162,95 +1224,79 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         mbar_wait_teardown(&s.b_full[kb % kNB], (kb / kNB) & 1, args.status);
     }
     __syncwarp();
-  } else if (warp < 12) {
-    // ---------------- readout A builders: thread = token row
+  } else if (warp < 16) {
+    // ---------------- readout A builders: group hh builds head hh; thread = token row
     const int m = 32 * (warp & 3) + lane;
-    const int g3 = warp >> 2;                 // builds jobs g3, g3 + 3, ...
-    if (mbar_wait(&s.qkv_full, 0, abort_flag, args.status)) {
-      const uint8_t *qbase = reinterpret_cast<const uint8_t *>(s.q[0]) + m * 128;
-      const int m7 = m & 7;
-      int kb = g3 / nh, hh = g3 % nh;
-      int slot = g3, aph = 0;
-      for (int jb = g3; jb < njobs; jb += 3) {
-        uint32_t q[32], cw[32], out[32];
-        const uint8_t *qrow = qbase + hh * (kC * 64 * 2);
+    const int hh = warp >> 2;
+    if (hh < nh && mbar_wait(&s.qkv_full, 0, abort_flag, args.status)) {
+      uint32_t q[32];
+      const uint8_t *qrow = reinterpret_cast<const uint8_t *>(s.q[hh]) + m * 128;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(qrow + ((cc ^ m7) << 4));
-          q[4 * cc] = v.x; q[4 * cc + 1] = v.y; q[4 * cc + 2] = v.z; q[4 * cc + 3] = v.w;
-        }
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(qrow + ((cc ^ (m & 7)) << 4));
+        q[4 * cc] = v.x; q[4 * cc + 1] = v.y; q[4 * cc + 2] = v.z; q[4 * cc + 3] = v.w;
+      }
+      for (int kb = 0; kb < kNKB; ++kb) {
+        const int jr = kb * nh + hh;
+        const int slot = jr % kNA, aph = (jr / kNA) & 1;
         const uint4 *cp = reinterpret_cast<const uint4 *>(s.coef[hh] + 64 * kb);
-        const int ncw = kb == kNKB - 1 ? 2 : 8;   // the H0 block holds 16 features
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (e < ncw) v = cp[e];
-          cw[4 * e] = v.x; cw[4 * e + 1] = v.y; cw[4 * e + 2] = v.z; cw[4 * e + 3] = v.w;
-        }
-        build_dispatch(kb, q, cw, out);
+        uint32_t out[16];
+        build_dispatch<0>(kb, q, cp, out);
         if (!mbar_wait(&s.a_empty[slot], aph ^ 1, abort_flag, args.status)) break;
-        tmem_st16(tmem_lane_addr(tb, warp, kTmemA + 32 * slot),
-                  *reinterpret_cast<const uint32_t(*)[16]>(&out[0]));
-        tmem_st16(tmem_lane_addr(tb, warp, kTmemA + 32 * slot + 16),
-                  *reinterpret_cast<const uint32_t(*)[16]>(&out[16]));
+        tmem_st16(tmem_lane_addr(tb, warp, kTmemA + 32 * slot), out);
+        build_dispatch<1>(kb, q, cp, out);
+        tmem_st16(tmem_lane_addr(tb, warp, kTmemA + 32 * slot + 16), out);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.a_full[slot]);
-        slot += 3;
-        if (slot >= kNA) { slot -= kNA; aph ^= 1; }
-        hh += 3;
-        while (hh >= nh) { hh -= nh; ++kb; }
       }
     }
-    {
-      // ---------------- epilogue: y = (u~ + intra)[0:64] / (u~ + intra)[64].
-      // Builder group g3 finishes the heads g3, g3 + 3, ...  The intra-chunk
-      // rows of a head are loaded before they are needed so the global-memory
-      // latency overlaps the last UMMAs (first head) or the previous head.
+    if (hh < nh) {
+      // ---------------- epilogue of head hh: y = (u~ + intra)[0:64] / (u~ + intra)[64],
+      // 16 columns at a time; the intra-chunk rows of the next 16 columns are
+      // loaded while the current ones are finished
       const int i_tok = c * kC + m;
       const bool row_ok = i_tok < args.T;
-      const size_t row0 = ((size_t)bidx * args.Hq + h0) * args.T + i_tok;
-      float4 inum[16];
+      const size_t row = ((size_t)bidx * args.Hq + h0 + hh) * args.T + i_tok;
+      const float4 *src = reinterpret_cast<const float4 *>(args.intra_num + row * 64);
+      float4 cur[4], nxt[4];
       float iden = 0.f;
-      auto load_intra = [&](int hh) {
-        if (row_ok) {
-          const size_t row = row0 + (size_t)hh * args.T;
-          const float4 *src = reinterpret_cast<const float4 *>(args.intra_num + row * 64);
+      if (row_ok) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) inum[e] = __ldg(src + e);
-          iden = __ldg(args.intra_den + row);
-        }
-      };
-      if (g3 < nh) load_intra(g3);
-      if (g3 < nh && !*abort_flag && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
+        for (int e = 0; e < 4; ++e) cur[e] = __ldg(src + e);
+        iden = __ldg(args.intra_den + row);
+      }
+      if (!*abort_flag && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
         tc_fence_after();
-        for (int hh = g3; hh < nh; hh += 3) {
-          // denominator column first, then the values 16 columns at a time
-          uint32_t r[16];
-          tmem_ld16(tmem_lane_addr(tb, warp, kTmemD + 80 * hh + 64), r);
-          tmem_wait_ld();
-          const float inv = 1.0f / (__uint_as_float(r[0]) + iden);
-          uint4 *dst = reinterpret_cast<uint4 *>(args.Y + (row0 + (size_t)hh * args.T) * kDv);
+        uint32_t r[16];
+        tmem_ld16(tmem_lane_addr(tb, warp, kTmemD + 80 * hh + 64), r);
+        tmem_wait_ld();
+        const float inv = 1.0f / (__uint_as_float(r[0]) + iden);
+        uint4 *dst = reinterpret_cast<uint4 *>(args.Y + row * kDv);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            tmem_ld16(tmem_lane_addr(tb, warp, kTmemD + 80 * hh + 16 * q4), r);
-            tmem_wait_ld();
-            uint32_t pk[8];
+        for (int q4 = 0; q4 < 4; ++q4) {
+          if (q4 < 3 && row_ok) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float4 n4 = inum[4 * q4 + e];
-              pk[2 * e] = pack_bf16x2((__uint_as_float(r[4 * e]) + n4.x) * inv,
-                                      (__uint_as_float(r[4 * e + 1]) + n4.y) * inv);
-              pk[2 * e + 1] = pack_bf16x2((__uint_as_float(r[4 * e + 2]) + n4.z) * inv,
-                                          (__uint_as_float(r[4 * e + 3]) + n4.w) * inv);
-            }
-            if (row_ok) {
-              dst[2 * q4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              dst[2 * q4 + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            }
+            for (int e = 0; e < 4; ++e) nxt[e] = __ldg(src + 4 * (q4 + 1) + e);
           }
-          if (hh + 3 < nh) load_intra(hh + 3);
+          tmem_ld16(tmem_lane_addr(tb, warp, kTmemD + 80 * hh + 16 * q4), r);
+          tmem_wait_ld();
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 n4 = cur[e];
+            pk[2 * e] = pack_bf16x2((__uint_as_float(r[4 * e]) + n4.x) * inv,
+                                    (__uint_as_float(r[4 * e + 1]) + n4.y) * inv);
+            pk[2 * e + 1] = pack_bf16x2((__uint_as_float(r[4 * e + 2]) + n4.z) * inv,
+                                        (__uint_as_float(r[4 * e + 3]) + n4.w) * inv);
+          }
+          if (row_ok) {
+            dst[2 * q4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[2 * q4 + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) cur[e] = nxt[e];
         }
       }
     }
@@ -1359,7 +1405,8 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
                  kN))
     return oal_fail(OAL_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
-  tc_prep_kernel<<<dim3(Hq, (kKP + 255) / 256), 256, 0, stream>>>(a, b, C, L, group, G, eps, packed, coef, plans, status);
+  launch_pdl(tc_prep_kernel, dim3(Hq, (kKP + 255) / 256 + 1), dim3(256), 0, stream, a, b, C, L, group,
+             G, eps, packed, coef, plans, status);
   oal_status st = oal_after_launch("tc_prep_kernel", stream);
   if (st != OAL_OK) return st;
 
@@ -1385,13 +1432,13 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   if (lay.nparts > 1) {
     sa.mode = 0;
     dim3 g0(kTiles, lay.nparts - 1, lay.U);
-    tc_state_kernel<<<g0, kStateThreads, ssmem, stream>>>(tmK, tmV, sa);
+    launch_pdl(tc_state_kernel, g0, dim3(kStateThreads), ssmem, stream, tmK, tmV, sa);
     st = oal_after_launch("tc_state_kernel", stream);
     if (st != OAL_OK) return st;
   }
   sa.mode = 1;
   dim3 g1(kTiles, lay.nparts, lay.U);
-  tc_state_kernel<<<g1, kStateThreads, ssmem, stream>>>(tmK, tmV, sa);
+  launch_pdl(tc_state_kernel, g1, dim3(kStateThreads), ssmem, stream, tmK, tmV, sa);
   st = oal_after_launch("tc_state_kernel", stream);
   if (st != OAL_OK) return st;
 
@@ -1403,11 +1450,11 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   ra.intra_num = reinterpret_cast<float *>(w + lay.inum_off);
   ra.intra_den = reinterpret_cast<float *>(w + lay.iden_off);
   dim3 gi((ra.rho + kIntraNH - 1) / kIntraNH, lay.nC, lay.U);
-  intra_kernel_for(G)<<<gi, kIntraThreads, ismem, stream>>>(tmQ, tmK, tmV, ra);
+  launch_pdl(intra_kernel_for(G), gi, dim3(kIntraThreads), ismem, stream, tmQ, tmK, tmV, ra);
   st = oal_after_launch("tc_intra_kernel", stream);
   if (st != OAL_OK) return st;
   dim3 g2((ra.rho + kMaxNH - 1) / kMaxNH, lay.nC, lay.U);
-  tc_readout_kernel<<<g2, kReadThreads, rsmem, stream>>>(tmQ, tmS, ra);
+  launch_pdl(tc_readout_kernel, g2, dim3(kReadThreads), rsmem, stream, tmQ, tmS, ra);
   return oal_after_launch("tc_readout_kernel", stream);
 }
 
