@@ -300,25 +300,25 @@ __device__ __forceinline__ void named_bar(int id, int n) {
 
 // ================================================================= state kernel
 // One block per (128-feature tile, part of the sequence, batch x KV head).
-// Per chunk c of the part: Delta S_c = phi(K_c)^T V_c by UMMA into one of two
+// Per chunk c of the part: Delta S_c = phi(K_c)^T [V_c | 1] by UMMA into one of two
 // tensor-memory accumulators; phi is split exactly into two bf16 terms
 // (hi = bf16(k_r k_t), lo = k_r k_t - hi; the product of two bf16 values has
 // at most 16 significant bits), so the fp32 state is exact up to fp32
-// accumulation.  The "1" column, sum_j phi(k_j), is summed in fp32 by the
-// builders (an N = 16 UMMA for one column costs as much tensor time as the
-// value columns).  The epilogue warps keep the running fp32 state of their
+// accumulation.  B = [V_c | 1] is MN-major with N = 80: the V tile as loaded
+// by TMA is its first 128-byte atom and one constant tile whose column 0 is 1
+// its second (the descriptor's atom stride differs per stage).  The epilogue
+// warps keep the running fp32 state of their
 // feature row in registers, add each Delta S_c, and (mode 1) write the bf16
 // snapshot S_{c-1} that the readout of chunk c consumes.
 constexpr int kStateStages = 3;
 
 struct __align__(1024) StateSmem {
   __nv_bfloat16 kv[kStateStages][2][kC * 64];   // [stage][K | V] 128B-swizzled tiles
+  __nv_bfloat16 ones[kC * 64];                  // second atom of B: column 0 is 1
   // K transposed, [dim][token]; the 16-byte chunk c of row r sits at c ^ kt_swz(r)
   __nv_bfloat16 kT[64][kC];
   uint64_t kv_full[kStateStages], kv_empty[kStateStages];
   uint64_t a_full[2], a_empty[2], d_full[2], d_empty[2];
-  uint64_t sum_full[4];                          // "1"-column sums of a chunk are ready
-  float osum[4][2][128];                         // [chunk & 3][builder group][feature]
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -334,7 +334,7 @@ struct StateArgs {
 };
 
 constexpr int kStateThreads = 512;
-constexpr int kStateD = 0;          // accumulators at cols 0 and 128 (64 wide)
+constexpr int kStateD = 0;          // accumulators at cols 0 and 128 (80 wide)
 constexpr int kStateA = 256;        // A slots at 256 and 384: [hi 64 | lo 64]
 
 __device__ __forceinline__ float bf16lo_f32(uint32_t x) { return __uint_as_float(x << 16); }
@@ -386,12 +386,22 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       mbar_init(&s.d_full[i], 1);
       mbar_init(&s.d_empty[i], 4);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&s.sum_full[i], 8);
     fence_mbar_init();
   }
   if (warp == 1) {
     tmem_alloc(&s.tmem_base, 512);
     tmem_relinquish();
+  }
+  if (warp >= 4 && warp < 8) {
+    // the constant atom of B: row j (token) holds 1 in column 0, 0 elsewhere
+    const int j = tid - 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (c == 0) v.x = 0x3F80u;
+      *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(s.ones) + sw128(j, c)) = v;
+    }
+    fence_proxy_async();
   }
   tc_fence_before();
   __syncthreads();
@@ -422,17 +432,21 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------- MMA issuer: D[:, 0:64] += A x V_c (N = 64), A = phi(K_c)^T
-      // as hi | lo, K = 256; V read MN-major straight from the TMA stage
-      const uint32_t idn = idesc_bf16_f32(128, 64, 1);
-      const uint64_t vdesc0 = sdesc_sw128(smem_u32(s.kv[0][1]), 16, 1024);
-      constexpr uint64_t kKVStep = (2 * kC * 64 * 2) >> 4;   // one K|V stage
+      // ---------------- MMA issuer: D[:, 0:80] += A x [V_c | 1] (N = 80), A =
+      // phi(K_c)^T as hi | lo, K = 256; B read MN-major: the V atom straight
+      // from the TMA stage, the constant atom at the stage's atom stride
+      const uint32_t idn = idesc_bf16_f32(128, kN, 1);
+      uint64_t vdesc[kStateStages];
+#pragma unroll
+      for (int st = 0; st < kStateStages; ++st)
+        vdesc[st] = sdesc_sw128(smem_u32(s.kv[st][1]), smem_u32(s.ones) - smem_u32(s.kv[st][1]),
+                                1024);
       for (int i = 0; i < nchunks; ++i) {
         const int sl = i & 1, st = i % kStateStages;
         if (!mbar_wait(&s.a_full[sl], (i >> 1) & 1, abort_flag, args.status)) break;
         if (!mbar_wait(&s.d_empty[sl], ((i >> 1) & 1) ^ 1, abort_flag, args.status)) break;
         tc_fence_after();
-        const uint64_t bd = vdesc0 + kKVStep * st;
+        const uint64_t bd = vdesc[st];
         const uint32_t d = tb + kStateD + 128 * sl;
         const uint32_t a0 = tb + kStateA + 128 * sl;
 #pragma unroll
@@ -487,7 +501,6 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       if (!mbar_wait(&s.a_empty[sl], ((i >> 1) & 1) ^ 1, abort_flag, args.status)) break;
       const int nvalid = min(kC, args.T - c * kC);
       const uint32_t abase = kStateA + 128 * sl;
-      float2 osum = make_float2(0.f, 0.f);    // sum over this group's tokens of phi_f(k_j)
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
         const int q = 2 * bg + qq;           // 32-token block
@@ -502,7 +515,6 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
             hi[w] = (j < nvalid ? 0x3F80u : 0u) | (j + 1 < nvalid ? 0x3F800000u : 0u);
             lo[w] = 0u;
           }
-          osum.x += (float)min(32, max(0, nvalid - 32 * q));
         } else if (code & 0x8000) {
           const int rr = code & 0xff;
           const uint4 *kr = reinterpret_cast<const uint4 *>(&s.kT[rr][0]);
@@ -511,11 +523,6 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
             const uint4 x = kr[(4 * q + v) ^ kt_swz(rr)];
             hi[4 * v] = x.x; hi[4 * v + 1] = x.y; hi[4 * v + 2] = x.z; hi[4 * v + 3] = x.w;
             lo[4 * v] = lo[4 * v + 1] = lo[4 * v + 2] = lo[4 * v + 3] = 0u;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              osum.x += bf16lo_f32(hi[4 * v + e]);
-              osum.y += bf16hi_f32(hi[4 * v + e]);
-            }
           }
         } else {
           const int rr = code >> 8, tt = code & 0xff;
@@ -530,24 +537,16 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
               const uint32_t h2 = hmul2(xs[e], ys[e]);
               hi[4 * v + e] = h2;
               lo[4 * v + e] = hfma2_bf16(xs[e], ys[e], h2 ^ 0x80008000u);   // exact residual
-              // the products of bf16 values are exact in fp32
-              osum = ffma2(make_float2(bf16lo_f32(xs[e]), bf16hi_f32(xs[e])),
-                           make_float2(bf16lo_f32(ys[e]), bf16hi_f32(ys[e])), osum);
             }
           }
         }
         tmem_st16(tmem_lane_addr(tb, warp, abase + 16 * q), hi);
         tmem_st16(tmem_lane_addr(tb, warp, abase + 64 + 16 * q), lo);
       }
-      // rows with t < r (duplicates) still carry their sum: the epilogue drops them
-      s.osum[i & 3][bg][l] = osum.x + osum.y;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&s.a_full[sl]);
-        mbar_arrive(&s.sum_full[i & 3]);
-      }
+      if (lane == 0) mbar_arrive(&s.a_full[sl]);
     }
   } else if (warp >= 12) {
     // ---------------- epilogue: running fp32 state of this feature row
@@ -594,17 +593,14 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       if (!mbar_wait(&s.d_full[sl], (i >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
-      for (int q = 0; q < kDv / 16; ++q) {
+      for (int q = 0; q < kN / 16; ++q) {
         uint32_t r[16];
         tmem_ld16(tmem_lane_addr(tb, warp, kStateD + 128 * sl + 16 * q), r);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) S[16 * q + e] += __uint_as_float(r[e]);
+        for (int e = 0; e < 16; ++e)
+          if (16 * q + e < kU) S[16 * q + e] += __uint_as_float(r[e]);
       }
-      // the "1" column from the builders' sums (read before d_empty is
-      // released: the slot is rewritten four chunks later)
-      if (!mbar_wait(&s.sum_full[i & 3], (i >> 2) & 1, abort_flag, args.status)) { ok = false; break; }
-      S[kDv] += s.osum[i & 3][0][l] + s.osum[i & 3][1][l];
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.d_empty[sl]);
