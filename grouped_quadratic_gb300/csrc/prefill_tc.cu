@@ -40,6 +40,7 @@
 //                       FMA), P.V by UMMA, then normalisation.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <utility>
 
 #include "oal_internal.cuh"
@@ -136,13 +137,55 @@ struct KPlan {
 };
 
 // ---------------------------------------------------------------- prep
+struct KtArgs {
+  const __nv_bfloat16 *K;    // [U][T][64]
+  __nv_bfloat16 *Kt;         // [U][64][Tpad]
+  int T, Tpad, U, nC;
+};
+
 __global__ void __launch_bounds__(256)
 tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
                const float *__restrict__ Ctab, const float *__restrict__ L,
                const int32_t *__restrict__ group, int G, float eps, int packed,
-               __nv_bfloat16 *__restrict__ coef, KPlan *__restrict__ plans, int *status) {
+               __nv_bfloat16 *__restrict__ coef, KPlan *__restrict__ plans, int *status,
+               KtArgs kt) {
   pdl_trigger();
   pdl_wait();
+  const int ncoef = (kKP + 255) / 256;
+  if ((int)blockIdx.y > ncoef) {
+    // ---- K^T for the state kernel: [unit][64 dims][nC * 128 tokens], zero past T
+    __shared__ __nv_bfloat16 ks[kC][64 + 2];      // padded: column reads hit distinct banks
+    const int ntr = (gridDim.y - ncoef - 1) * gridDim.x;
+    for (int tile = blockIdx.x + gridDim.x * (blockIdx.y - ncoef - 1); tile < kt.U * kt.nC;
+         tile += ntr) {
+      const int u = tile / kt.nC, c = tile % kt.nC;
+      __syncthreads();
+      // 16-byte loads, all in flight before any is stored (blockDim.x == 256)
+      uint4 v[kC * 8 / 256];
+#pragma unroll
+      for (int k = 0; k < kC * 8 / 256; ++k) {   // token j, 8-dim chunk
+        const int e = threadIdx.x + 256 * k, j = e >> 3, d8 = e & 7, tok = c * kC + j;
+        v[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (tok < kt.T)
+          v[k] = *reinterpret_cast<const uint4 *>(kt.K + ((size_t)u * kt.T + tok) * 64 + 8 * d8);
+      }
+#pragma unroll
+      for (int k = 0; k < kC * 8 / 256; ++k) {
+        const int e = threadIdx.x + 256 * k, j = e >> 3, d8 = e & 7;
+        uint32_t *row = reinterpret_cast<uint32_t *>(&ks[j][8 * d8]);
+        row[0] = v[k].x; row[1] = v[k].y; row[2] = v[k].z; row[3] = v[k].w;
+      }
+      __syncthreads();
+      __nv_bfloat16 *dst = kt.Kt + (size_t)u * 64 * kt.Tpad + (size_t)c * kC;
+      for (int e = threadIdx.x; e < 64 * (kC / 2); e += blockDim.x) {   // dim d, token pair
+        const int d = e / (kC / 2), jp = e % (kC / 2);
+        const uint32_t lo = *reinterpret_cast<const uint16_t *>(&ks[2 * jp][d]);
+        const uint32_t hi = *reinterpret_cast<const uint16_t *>(&ks[2 * jp + 1][d]);
+        *reinterpret_cast<uint32_t *>(dst + (size_t)d * kt.Tpad + 2 * jp) = lo | (hi << 16);
+      }
+    }
+    return;
+  }
   const int h = blockIdx.x;
   const int tid = threadIdx.x;
   const int G1 = G + 1;
@@ -158,9 +201,8 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
     sgrp[tid] = g;
     atomicAdd(&scnt[g], 1);
   }
-  // readout weights in the internal feature order (blockIdx.y < gridDim.y - 1
-  // split the rows); the last block row forms the kappa plan meanwhile
-  const int ncoef = gridDim.y - 1;
+  // readout weights in the internal feature order (blockIdx.y < ncoef split
+  // the rows); block row ncoef forms the kappa plan meanwhile
   const float *Ch = Ctab + (size_t)h * (packed ? kH2Packed : kH2Full);
   for (int f = blockIdx.y * blockDim.x + tid; blockIdx.y < ncoef && f < kKP;
        f += blockDim.x * ncoef) {
@@ -313,10 +355,10 @@ __device__ __forceinline__ void named_bar(int id, int n) {
 constexpr int kStateStages = 3;
 
 struct __align__(1024) StateSmem {
-  __nv_bfloat16 kv[kStateStages][2][kC * 64];   // [stage][K | V] 128B-swizzled tiles
+  // [stage][K^T | V]: K^T as two [64 dims][64 tokens] halves, V as [128 tokens][64
+  // dims]; every tile 128B-swizzled (16-byte chunk c of row r at c ^ (r & 7))
+  __nv_bfloat16 kv[kStateStages][2][kC * 64];
   __nv_bfloat16 ones[kC * 64];                  // second atom of B: column 0 is 1
-  // K transposed, [dim][token]; the 16-byte chunk c of row r sits at c ^ kt_swz(r)
-  __nv_bfloat16 kT[64][kC];
   uint64_t kv_full[kStateStages], kv_empty[kStateStages];
   uint64_t a_full[2], a_empty[2], d_full[2], d_empty[2];
   uint32_t tmem_base;
@@ -354,11 +396,6 @@ __device__ __forceinline__ uint32_t hfma2_bf16(uint32_t a, uint32_t b, uint32_t 
   asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
   return r;
 }
-
-// Swizzle of the transposed K tile: conflict-free for the transpose's writes
-// (8 rows 8 apart, same chunk) and at most 2-way for the builders' reads (8
-// consecutive rows, same chunk).
-__device__ __forceinline__ int kt_swz(int r) { return (r & 7) ^ ((r >> 3) & 7); }
 
 __global__ void __launch_bounds__(kStateThreads, 1)
 tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -421,7 +458,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
         if (!mbar_wait(&s.kv_empty[st], ((i / kStateStages) & 1) ^ 1, abort_flag, args.status))
           break;
         mbar_arrive_expect_tx(&s.kv_full[st], 2 * kC * 64 * 2);
-        tma_load_3d(s.kv[st][0], &tmK, &s.kv_full[st], 0, (c0 + i) * kC, unit);
+        tma_load_3d(s.kv[st][0], &tmK, &s.kv_full[st], (c0 + i) * kC, 0, unit);
+        tma_load_3d(s.kv[st][0] + 64 * 64, &tmK, &s.kv_full[st], (c0 + i) * kC + 64, 0, unit);
         tma_load_3d(s.kv[st][1], &tmV, &s.kv_full[st], 0, (c0 + i) * kC, unit);
         issued = i + 1;
       }
@@ -462,45 +500,21 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
-    // ---------------- builders: group 0 (warps 4-7) transposes K; then group
-    // bg builds tokens 64 bg .. 64 bg + 63 of A = phi(K_c)^T (hi | lo)
+    // ---------------- builders: group bg builds tokens 64 bg .. 64 bg + 63 of
+    // A = phi(K_c)^T (hi | lo) from the K^T half bg of the stage
     const int bg = (warp - 4) >> 2;
-    const int l = 32 * (warp & 3) + lane;    // TMEM lane = feature row, = token when transposing
+    const int l = 32 * (warp & 3) + lane;    // TMEM lane = feature row
     const int f = tile * 128 + l;
     const uint16_t code = f < kKP ? g_feat.code[f] : (uint16_t)0xFFFF;
     for (int i = 0; i < nchunks; ++i) {
       const int sl = i & 1, st = i % kStateStages;
       const int c = c0 + i;
       if (!mbar_wait(&s.kv_full[st], (i / kStateStages) & 1, abort_flag, args.status)) break;
-      named_bar(1, 256);   // the previous chunk's builds are done with kT
-      if (bg == 0) {
-        // 8 x 8 block transpose: thread (tb8, db8) moves tokens 8 tb8 .. +7 x
-        // dims 8 db8 .. +7 from the K tile into kT with 16-byte accesses
-        const int tb8 = l >> 3, db8 = l & 7;
-        const uint8_t *ktile = reinterpret_cast<const uint8_t *>(s.kv[st][0]);
-        uint32_t v[8][4];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const uint4 x = *reinterpret_cast<const uint4 *>(ktile + sw128(8 * tb8 + t, db8));
-          v[t][0] = x.x; v[t][1] = x.y; v[t][2] = x.z; v[t][3] = x.w;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {          // dims 2j, 2j+1 of the block
-          uint4 lo, hi;
-          lo.x = __byte_perm(v[0][j], v[1][j], 0x5410); hi.x = __byte_perm(v[0][j], v[1][j], 0x7632);
-          lo.y = __byte_perm(v[2][j], v[3][j], 0x5410); hi.y = __byte_perm(v[2][j], v[3][j], 0x7632);
-          lo.z = __byte_perm(v[4][j], v[5][j], 0x5410); hi.z = __byte_perm(v[4][j], v[5][j], 0x7632);
-          lo.w = __byte_perm(v[6][j], v[7][j], 0x5410); hi.w = __byte_perm(v[6][j], v[7][j], 0x7632);
-          const int r0 = 8 * db8 + 2 * j;
-          *reinterpret_cast<uint4 *>(&s.kT[r0][8 * (tb8 ^ kt_swz(r0))]) = lo;
-          *reinterpret_cast<uint4 *>(&s.kT[r0 + 1][8 * (tb8 ^ kt_swz(r0 + 1))]) = hi;
-        }
-      }
-      named_bar(1, 256);
       // slot sl (A in tensor memory) is free once the UMMAs of chunk i - 2 are done
       if (!mbar_wait(&s.a_empty[sl], ((i >> 1) & 1) ^ 1, abort_flag, args.status)) break;
       const int nvalid = min(kC, args.T - c * kC);
       const uint32_t abase = kStateA + 128 * sl;
+      const uint8_t *kth = reinterpret_cast<const uint8_t *>(s.kv[st][0]) + bg * (64 * 128);
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
         const int q = 2 * bg + qq;           // 32-token block
@@ -517,20 +531,20 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           }
         } else if (code & 0x8000) {
           const int rr = code & 0xff;
-          const uint4 *kr = reinterpret_cast<const uint4 *>(&s.kT[rr][0]);
+          const uint4 *kr = reinterpret_cast<const uint4 *>(kth + rr * 128);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const uint4 x = kr[(4 * q + v) ^ kt_swz(rr)];
+            const uint4 x = kr[(4 * qq + v) ^ (rr & 7)];
             hi[4 * v] = x.x; hi[4 * v + 1] = x.y; hi[4 * v + 2] = x.z; hi[4 * v + 3] = x.w;
             lo[4 * v] = lo[4 * v + 1] = lo[4 * v + 2] = lo[4 * v + 3] = 0u;
           }
         } else {
           const int rr = code >> 8, tt = code & 0xff;
-          const uint4 *kr = reinterpret_cast<const uint4 *>(&s.kT[rr][0]);
-          const uint4 *kt = reinterpret_cast<const uint4 *>(&s.kT[tt][0]);
+          const uint4 *kr = reinterpret_cast<const uint4 *>(kth + rr * 128);
+          const uint4 *kt = reinterpret_cast<const uint4 *>(kth + tt * 128);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const uint4 x = kr[(4 * q + v) ^ kt_swz(rr)], y = kt[(4 * q + v) ^ kt_swz(tt)];
+            const uint4 x = kr[(4 * qq + v) ^ (rr & 7)], y = kt[(4 * qq + v) ^ (tt & 7)];
             const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -1336,7 +1350,7 @@ static bool make_map3(CUtensorMap *m, const void *ptr, uint64_t nx, uint64_t ny,
 
 struct Layout {
   int nC, nparts, cpp, U;
-  size_t snap_off, ptot_off, coef_off, plan_off, inum_off, iden_off, total;
+  size_t snap_off, ptot_off, coef_off, plan_off, inum_off, iden_off, kt_off, total;
 };
 
 static Layout plan_layout(int B, int Hq, int Hkv, int T) {
@@ -1355,6 +1369,7 @@ static Layout plan_layout(int B, int Hq, int Hkv, int T) {
   L.plan_off = o; o = al(o + (size_t)Hq * sizeof(KPlan));
   L.inum_off = o; o = al(o + (size_t)B * Hq * T * 64 * sizeof(float));
   L.iden_off = o; o = al(o + (size_t)B * Hq * T * sizeof(float));
+  L.kt_off = o; o = al(o + (size_t)L.U * 64 * L.nC * kC * 2);
   L.total = o;
   return L;
 }
@@ -1392,17 +1407,26 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   KPlan *plans = reinterpret_cast<KPlan *>(w + lay.plan_off);
   int *status = oal_device_status_word();
 
-  CUtensorMap tmQ, tmK, tmV, tmS;
+  CUtensorMap tmQ, tmK, tmKn, tmV, tmS;
+  const int Tpad = lay.nC * kC;
+  __nv_bfloat16 *Kt = reinterpret_cast<__nv_bfloat16 *>(w + lay.kt_off);
   const uint64_t rowb = 64 * 2;
   if (!make_map3(&tmQ, Q, 64, T, (uint64_t)B * Hq, rowb, rowb * T, kC) ||
-      !make_map3(&tmK, K, 64, T, (uint64_t)lay.U, rowb, rowb * T, kC) ||
+      !make_map3(&tmKn, K, 64, T, (uint64_t)lay.U, rowb, rowb * T, kC) ||
+      !make_map3(&tmK, Kt, (uint64_t)Tpad, 64, (uint64_t)lay.U, (uint64_t)Tpad * 2,
+                 (uint64_t)Tpad * 2 * 64, 64) ||
       !make_map3(&tmV, V, 64, T, (uint64_t)lay.U, rowb, rowb * T, kC) ||
       !make_map3(&tmS, snap, kKP, kN, (uint64_t)lay.U * lay.nC, (uint64_t)kKP * 2, kSnapBytes,
                  kN))
     return oal_fail(OAL_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
-  launch_pdl(tc_prep_kernel, dim3(Hq, (kKP + 255) / 256 + 1), dim3(256), 0, stream, a, b, C, L, group,
-             G, eps, packed, coef, plans, status);
+  KtArgs kta;
+  kta.K = static_cast<const __nv_bfloat16 *>(K); kta.Kt = Kt;
+  kta.T = T; kta.Tpad = Tpad; kta.U = lay.U; kta.nC = lay.nC;
+  const int ntiles = lay.U * lay.nC;
+  const int ntr = (std::min(ntiles, 2 * 152) + Hq - 1) / Hq;   // block rows of transposes
+  launch_pdl(tc_prep_kernel, dim3(Hq, (kKP + 255) / 256 + 1 + ntr), dim3(256), 0, stream, a, b, C,
+             L, group, G, eps, packed, coef, plans, status, kta);
   oal_status st = oal_after_launch("tc_prep_kernel", stream);
   if (st != OAL_OK) return st;
 
@@ -1446,7 +1470,7 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   ra.intra_num = reinterpret_cast<float *>(w + lay.inum_off);
   ra.intra_den = reinterpret_cast<float *>(w + lay.iden_off);
   dim3 gi((ra.rho + kIntraNH - 1) / kIntraNH, lay.nC, lay.U);
-  launch_pdl(intra_kernel_for(G), gi, dim3(kIntraThreads), ismem, stream, tmQ, tmK, tmV, ra);
+  launch_pdl(intra_kernel_for(G), gi, dim3(kIntraThreads), ismem, stream, tmQ, tmKn, tmV, ra);
   st = oal_after_launch("tc_intra_kernel", stream);
   if (st != OAL_OK) return st;
   dim3 g2((ra.rho + kMaxNH - 1) / kMaxNH, lay.nC, lay.U);
