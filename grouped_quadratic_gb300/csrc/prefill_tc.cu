@@ -359,6 +359,9 @@ struct __align__(1024) StateSmem {
   // dims]; every tile 128B-swizzled (16-byte chunk c of row r at c ^ (r & 7))
   __nv_bfloat16 kv[kStateStages][2][kC * 64];
   __nv_bfloat16 ones[kC * 64];                  // second atom of B: column 0 is 1
+  // walk: the part's starting state, then (last part) the final state, one
+  // row per feature of the tile (odd pitch: row reads are conflict-free)
+  float rows[128][kU];
   uint64_t kv_full[kStateStages], kv_empty[kStateStages];
   uint64_t a_full[2], a_empty[2], d_full[2], d_empty[2];
   uint32_t tmem_base;
@@ -409,7 +412,12 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
   const int c1 = min(args.nC, c0 + args.cpp);
   const int nchunks = c1 - c0;
   const int mode = args.mode;
-  pdl_trigger();
+  // Mode 0 signals its dependents only after its own wait, so the walk
+  // (mode 1) can never start before the prep kernel's K^T is complete; the
+  // walk's part 0 needs no part totals and skips the wait, running on the SMs
+  // mode 0 leaves idle.  Every other walk block waits, so the walk still
+  // completes after mode 0.
+  if (mode == 1) pdl_trigger();
 
   if (tid == 0) {
     s.abort_flag = 0;
@@ -445,7 +453,50 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
   tc_fence_after();
   const uint32_t tb = s.tmem_base;
   volatile int *abort_flag = &s.abort_flag;
-  pdl_wait();   // inputs, part totals and snapshots of the previous kernels
+  if (mode == 0 || part > 0 || args.nparts == 1) pdl_wait();   // see above
+  if (mode == 0) pdl_trigger();
+  if (mode == 1 && part > 0) {
+    // Starting state of this part: the totals of parts 0 .. part-1 for this
+    // tile, summed in part order.  Every thread owns fixed float4s of the
+    // tile's [128][80] block and keeps up to four parts' loads in flight.
+    constexpr int kV4 = 128 * kN / 4;                     // float4s per part and tile
+    constexpr int kPer = (kV4 + kStateThreads - 1) / kStateThreads;
+    float4 acc[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = 0; p0 < part; p0 += 4) {
+      float4 v[4][kPer];
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp)
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int e = tid + kStateThreads * k;
+          v[pp][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (p0 + pp < part && e < kV4)
+            v[pp][k] = reinterpret_cast<const float4 *>(
+                args.ptot + (((size_t)unit * args.nparts + p0 + pp) * kTiles + tile) * 128 * kN)[e];
+        }
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp)
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          acc[k].x += v[pp][k].x; acc[k].y += v[pp][k].y;
+          acc[k].z += v[pp][k].z; acc[k].w += v[pp][k].w;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = tid + kStateThreads * k;
+      if (e < kV4) {
+        const int row = e / (kN / 4), c4 = 4 * (e % (kN / 4));
+        const float a4[4] = {acc[k].x, acc[k].y, acc[k].z, acc[k].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (c4 + j < kU) s.rows[row][c4 + j] = a4[j];
+      }
+    }
+    __syncthreads();
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -579,15 +630,9 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
 #pragma unroll
         for (int n = 0; n < kU; ++n) S[n] = src[n];
       }
-      for (int p = 0; p < part; ++p) {
-        const float4 *src = reinterpret_cast<const float4 *>(
-            args.ptot + ((((size_t)unit * args.nparts + p) * kTiles + tile) * 128 + l) * kN);
+      if (part > 0) {
 #pragma unroll
-        for (int n4 = 0; n4 < 16; ++n4) {
-          const float4 v = src[n4];
-          S[4 * n4] += v.x; S[4 * n4 + 1] += v.y; S[4 * n4 + 2] += v.z; S[4 * n4 + 3] += v.w;
-        }
-        S[64] += src[16].x;
+        for (int n = 0; n < kU; ++n) S[n] += s.rows[l][n];
       }
     }
     __nv_bfloat16 *snap_row =
@@ -630,11 +675,31 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
         dst[16] = make_float4(S[64], 0.f, 0.f, 0.f);
 #pragma unroll
         for (int n4 = 17; n4 < kN / 4; ++n4) dst[n4] = make_float4(0.f, 0.f, 0.f, 0.f);
-      } else if (part == args.nparts - 1 && erow >= 0 && !is_duplicate(code)) {
-        float *dst = args.state_out + (size_t)unit * FU + (size_t)erow * kU;
+      } else if (part == args.nparts - 1) {
+        // final state: this warp's 32 feature rows go through shared memory
+        // and out as runs of consecutive external rows, each run written by
+        // the whole warp with consecutive addresses
+        const bool mine = erow >= 0 && !is_duplicate(code);
 #pragma unroll
-        for (int n = 0; n < kU; ++n) dst[n] = S[n];
-        if (mirror >= 0) {
+        for (int n = 0; n < kU; ++n) s.rows[l][n] = S[n];
+        __syncwarp();
+        const int prev = __shfl_up_sync(0xffffffffu, mine ? erow : -2, 1);
+        const bool start = mine && (lane == 0 || prev != erow - 1);
+        unsigned starts = __ballot_sync(0xffffffffu, start);
+        const unsigned mask_mine = __ballot_sync(0xffffffffu, mine);
+        while (starts) {
+          const int a = __ffs(starts) - 1;
+          starts &= starts - 1;
+          // the run goes on while rows are mine and consecutive
+          const unsigned after = ~((2u << a) - 1u);
+          const unsigned breaks = (starts | ~mask_mine) & after;
+          const int b = breaks ? __ffs(breaks) - 1 : 32;
+          const int e0 = __shfl_sync(0xffffffffu, erow, a);
+          float *dst = args.state_out + (size_t)unit * FU + (size_t)e0 * kU;
+          const float *src = &s.rows[32 * (warp & 3) + a][0];
+          for (int idx = lane; idx < (b - a) * kU; idx += 32) dst[idx] = src[idx];
+        }
+        if (mine && mirror >= 0) {
           float *dm = args.state_out + (size_t)unit * FU + (size_t)mirror * kU;
 #pragma unroll
           for (int n = 0; n < kU; ++n) dm[n] = S[n];
