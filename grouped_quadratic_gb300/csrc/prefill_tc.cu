@@ -136,6 +136,13 @@ struct KPlan {
   int G;
 };
 
+// The dynamic shared memory rounded up to a 1024-byte boundary (swizzled
+// tiles need it), by pointer arithmetic on the shared array itself so the
+// compiler keeps the shared address space (shared loads, not generic ones).
+__device__ __forceinline__ uint8_t *smem_align1024(uint8_t *raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
 // ---------------------------------------------------------------- prep
 struct KtArgs {
   const __nv_bfloat16 *K;    // [U][T][64]
@@ -404,8 +411,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 StateArgs args) {
   extern __shared__ uint8_t smem_raw[];
-  StateSmem &s = *reinterpret_cast<StateSmem *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  StateSmem &s = *reinterpret_cast<StateSmem *>(smem_align1024(smem_raw));
   const int tile = blockIdx.x, part = blockIdx.y, unit = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c0 = part * args.cpp;
@@ -1035,8 +1041,7 @@ __global__ void __launch_bounds__(kIntraThreads, G <= 3 ? 4 : (G <= 5 ? 3 : 2))
 tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, ReadArgs args) {
   extern __shared__ uint8_t smem_raw[];
-  IntraSmem &s = *reinterpret_cast<IntraSmem *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  IntraSmem &s = *reinterpret_cast<IntraSmem *>(smem_align1024(smem_raw));
   const int hg = blockIdx.x, c = blockIdx.y, unit = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bidx = unit / args.Hkv, kv = unit % args.Hkv;
@@ -1183,8 +1188,7 @@ __global__ void __launch_bounds__(kReadThreads, 1)
 tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS,
                   ReadArgs args) {
   extern __shared__ uint8_t smem_raw[];
-  ReadSmem &s = *reinterpret_cast<ReadSmem *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  ReadSmem &s = *reinterpret_cast<ReadSmem *>(smem_align1024(smem_raw));
   const int hg = blockIdx.x, c = blockIdx.y, unit = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bidx = unit / args.Hkv, kv = unit % args.Hkv;
