@@ -9,13 +9,19 @@
 // and y^h = u~^h[0:64] / u~^h[64].  The kernel is bound by HBM: 8 bytes
 // (read + write) per state element.  Rows of the state are split into
 // slices, one block per (slice, batch x KV head).  A block first copies its
-// whole slice into shared memory with asynchronous 4-byte copies (rows of 65
-// floats are not 16-byte aligned), forms the per-row weights meanwhile, then
+// whole slice into shared memory with bulk copies (rows of 65 floats are not
+// 16-byte aligned: the ends are read with plain loads), forms the per-row
+// weights meanwhile, then
 // each warp walks rows (lane l owns columns l and l+32, lane 0 also column
 // 64): coalesced 128-byte stores of the updated rows and readout accumulators
-// in registers.  Per-slice partial readouts go to the workspace; the last
-// block of a (batch, KV head) to finish (atomic ticket) sums them in a fixed
-// order and divides.
+// in registers.  The partial readouts of the slices are combined in one of two
+// ways.  Few sequences: the slices of one (batch, KV head) form a thread-block
+// cluster and meet in distributed shared memory, where the first block sums
+// them in rank order and divides (no scratch, no extra launch).  Many
+// sequences: 128-row slices, partials in the workspace, and the last block of
+// a (batch, KV head) to finish (atomic ticket) sums them in a fixed order.
+#include <cooperative_groups.h>
+
 #include "oal_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -28,8 +34,8 @@ static __device__ const PairTable c_pairs = make_pair_table();
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxRowsPerBlock = 128;   // rows of one slice
-constexpr int kMinRowsPerBlock = 128;
+constexpr int kTicketRows = 128;        // rows of a slice, many-sequence kernel
+constexpr int kClusterRows = 528;       // rows of a slice, cluster kernel (state rows / 8)
 constexpr int kMaxRho = 8;
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {   // a * b + c, two lanes
@@ -44,19 +50,20 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {   // a *
 
 constexpr int kGroups = 4;             // row groups of a slice, each with its own bulk copy
 
-template <typename Tin>
-__global__ void __launch_bounds__(kThreads)
-decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
-              const Tin *__restrict__ v, Tin *__restrict__ y,
-              const float *__restrict__ a, const float *__restrict__ b,
-              const float *__restrict__ Ctab, float *__restrict__ state, int Hq,
-              int Hkv, int F, int packed, int rows_per_block, int nslices,
-              float *__restrict__ partial, unsigned *__restrict__ tickets, int *status) {
+// One slice of rows of one (batch, KV head): state update in place and this
+// block's partial readout of every head in s_part (rho x 65, fixed order).
+template <typename Tin, int kRows>
+__device__ __forceinline__ void decode_slice(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                                             const Tin *__restrict__ v,
+                                             const float *__restrict__ a,
+                                             const float *__restrict__ b,
+                                             const float *__restrict__ Ctab,
+                                             float *__restrict__ state, int Hq, int Hkv, int F,
+                                             int packed, int rows_per_block, int slice, int unit,
+                                             int *status, float (&s_part)[kMaxRho][kU]) {
   pdl_trigger();
   pdl_wait();
   const int rho = Hq / Hkv;
-  const int slice = blockIdx.x;
-  const int unit = blockIdx.y;              // b * Hkv + kv
   const int bidx = unit / Hkv, kv = unit % Hkv;
   const int h0 = kv * rho;
   const int f0 = slice * rows_per_block;
@@ -67,11 +74,10 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
   __shared__ float s_k[kD];
   __shared__ float s_u[kU];
   __shared__ float s_q[kMaxRho][kD];
-  __shared__ __align__(16) float s_wk[kMaxRowsPerBlock];
-  __shared__ __align__(16) float s_wq[kMaxRho][kMaxRowsPerBlock];
+  __shared__ __align__(16) float s_wk[kRows];
+  __shared__ __align__(16) float s_wq[kMaxRho][kRows];
   __shared__ __align__(8) uint64_t s_bar[kGroups];
   __shared__ int s_abort;
-  __shared__ bool s_last;
 
   // The slice (nrows rows of 65 floats) is contiguous in memory but not
   // 16-byte aligned in general.  Its aligned interior is fetched by kGroups
@@ -208,7 +214,7 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
   __syncthreads();   // the slice buffer is reused for the block reduction
   float(*s_red)[kMaxRho][kU] = reinterpret_cast<float(*)[kMaxRho][kU]>(s_buf);
 
-  // block reduction (fixed order) -> partial[unit][slice][rho][65]
+  // block reduction (fixed order) -> this block's partial readout
 #pragma unroll
   for (int hh = 0; hh < kMaxRho; ++hh) {
     if (hh < rho) {
@@ -218,13 +224,65 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     }
   }
   __syncthreads();
-  float *part = partial + ((size_t)unit * nslices + slice) * kMaxRho * kU;
   for (int n = tid; n < rho * kU; n += kThreads) {
     const int hh = n / kU, c = n % kU;
-    float s = 0.f;
-    for (int w = 0; w < kWarps; ++w) s += s_red[w][hh][c];
-    part[hh * kU + c] = s;
+    float sum = 0.f;
+    for (int w = 0; w < kWarps; ++w) sum += s_red[w][hh][c];
+    s_part[hh][c] = sum;
   }
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+decode_cluster_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                      const Tin *__restrict__ v, Tin *__restrict__ y,
+                      const float *__restrict__ a, const float *__restrict__ b,
+                      const float *__restrict__ Ctab, float *__restrict__ state, int Hq,
+                      int Hkv, int F, int packed, int rows_per_block, int *status) {
+  __shared__ float s_part[kMaxRho][kU];
+  const int unit = blockIdx.y, bidx = unit / Hkv, kv = unit % Hkv, rho = Hq / Hkv;
+  const int h0 = kv * rho, tid = threadIdx.x;
+  decode_slice<Tin, kClusterRows>(q, k, v, a, b, Ctab, state, Hq, Hkv, F, packed, rows_per_block,
+                                  blockIdx.x, unit, status, s_part);
+  // the first block sums every block's partial from distributed shared
+  // memory, in rank order, and divides
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  if (cluster.block_rank() == 0) {
+    __shared__ float s_tot[kMaxRho][kU];
+    const int nblk = (int)cluster.num_blocks();
+    for (int n = tid; n < rho * kU; n += kThreads) {
+      const int hh = n / kU, c = n % kU;
+      float sum = 0.f;
+      for (int r = 0; r < nblk; ++r) sum += cluster.map_shared_rank(&s_part[hh][c], r)[0];
+      s_tot[hh][c] = sum;
+    }
+    __syncthreads();
+    for (int n = tid; n < rho * kDv; n += kThreads) {
+      const int hh = n / kDv, c = n % kDv;
+      y[((size_t)bidx * Hq + h0 + hh) * kDv + c] = from_f32<Tin>(s_tot[hh][c] / s_tot[hh][kDv]);
+    }
+  }
+  cluster.sync();   // no block leaves while the first one reads its partial
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+decode_ticket_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                     const Tin *__restrict__ v, Tin *__restrict__ y,
+                     const float *__restrict__ a, const float *__restrict__ b,
+                     const float *__restrict__ Ctab, float *__restrict__ state, int Hq, int Hkv,
+                     int F, int packed, int rows_per_block, int nslices,
+                     float *__restrict__ partial, unsigned *__restrict__ tickets, int *status) {
+  __shared__ float s_part[kMaxRho][kU];
+  __shared__ bool s_last;
+  const int unit = blockIdx.y, slice = blockIdx.x, bidx = unit / Hkv, kv = unit % Hkv;
+  const int rho = Hq / Hkv, h0 = kv * rho, tid = threadIdx.x;
+  decode_slice<Tin, kTicketRows>(q, k, v, a, b, Ctab, state, Hq, Hkv, F, packed, rows_per_block,
+                                 slice, unit, status, s_part);
+  float *part = partial + ((size_t)unit * nslices + slice) * kMaxRho * kU;
+  for (int n = tid; n < rho * kU; n += kThreads) part[(n / kU) * kU + n % kU] = s_part[n / kU][n % kU];
   __threadfence();
   __syncthreads();
   if (tid == 0) {
@@ -234,14 +292,12 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // last block of this (batch, KV head): sum the slices in order, divide.
+  // last block of this (batch, KV head): sum the slices in a fixed order, divide
   __shared__ float s_tot[kMaxRho][kU];
   const float *pu = partial + (size_t)unit * nslices * kMaxRho * kU;
   for (int n = tid; n < rho * kU; n += kThreads) {
     const int hh = n / kU, c = n % kU;
-    // sixteen interleaved partial sums (loads in flight together), combined
-    // in a fixed order
-    float p16[16];
+    float p16[16];   // sixteen interleaved sums: the loads are in flight together
 #pragma unroll
     for (int j = 0; j < 16; ++j) p16[j] = 0.f;
     for (int sl0 = 0; sl0 < nslices; sl0 += 16) {
@@ -272,69 +328,118 @@ static size_t decode_smem_floats(int rpb) {
   return rows > red ? rows : red;
 }
 
-// Rows per block: small enough that small batches of sequences still spread
-// over the SMs (at least ~2 blocks per SM), a multiple of 32.
-static int decode_rows_per_block(size_t units, int packed) {
-  int rpb = kMaxRowsPerBlock;
-  while (rpb > kMinRowsPerBlock &&
-         units * (size_t)((state_rows(packed) + rpb - 1) / rpb) < 2 * 152)
-    rpb /= 2;
-  return rpb;
-}
+// The cluster kernel serves batches whose clusters (one per batch x KV
+// head) all fit the GPU at once.
+static bool use_clusters(size_t units) { return units * 16 <= 2 * 152; }
 
-static int decode_slices(size_t units, int packed) {
-  const int rpb = decode_rows_per_block(units, packed);
-  return (state_rows(packed) + rpb - 1) / rpb;
-}
+static int ticket_slices(int packed) { return (state_rows(packed) + kTicketRows - 1) / kTicketRows; }
 
 size_t decode_workspace_bytes(int B, int Hkv, int packed) {
   const size_t units = (size_t)B * Hkv;
-  const size_t part = units * decode_slices(units, packed) * kMaxRho * kU * sizeof(float);
+  if (use_clusters(units)) return 256;
+  const size_t part = units * ticket_slices(packed) * kMaxRho * kU * sizeof(float);
   const size_t tick = units * sizeof(unsigned);
   return ((part + 255) / 256) * 256 + ((tick + 255) / 256) * 256;
 }
 
 int decode_max_rho() { return kMaxRho; }
 
-oal_status launch_decode(const void *q, const void *k, const void *v, int is_bf16,
-                         int B, int Hq, int Hkv, const float *a, const float *b,
-                         const float *C, int packed, float *state, void *y,
-                         void *ws, cudaStream_t stream) {
+// Blocks per (batch, KV head) of the cluster kernel: 16 where the device can
+// schedule such clusters, else the portable 8.
+template <typename Tin>
+static int decode_cluster_size(int packed) {
+  static int cs[2] = {0, 0};
+  int &c = cs[packed != 0];
+  if (c) return c;
+  c = 8;
+  if (cudaFuncSetAttribute(decode_cluster_kernel<Tin>,
+                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    const int rpb = ((state_rows(packed) + 15) / 16 + 3) & ~3;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = decode_smem_floats(rpb) * sizeof(float);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel<Tin>, &cfg) == cudaSuccess &&
+        n > 0)
+      c = 16;
+  }
+  cudaGetLastError();   // a refused query is not an error of the next launch
+  return c;
+}
+
+template <typename Tin>
+static oal_status launch_decode_t(const Tin *q, const Tin *k, const Tin *v, int B, int Hq, int Hkv,
+                                  const float *a, const float *b, const float *C, int packed,
+                                  float *state, Tin *y, void *ws, cudaStream_t stream) {
   const int F = state_rows(packed);
   const size_t units = (size_t)B * Hkv;
-  const int rpb = decode_rows_per_block(units, packed);
-  const int nslices = decode_slices(units, packed);
-  const size_t part_bytes =
-      ((units * nslices * kMaxRho * kU * sizeof(float) + 255) / 256) * 256;
-  float *partial = (float *)ws;
-  unsigned *tickets = (unsigned *)((char *)ws + part_bytes);
-  if (cudaMemsetAsync(tickets, 0, units * sizeof(unsigned), stream) != cudaSuccess)
-    return oal_check_launch("decode ticket reset");
-  dim3 grid(nslices, (unsigned)units);
-  const size_t smem = decode_smem_floats(rpb) * sizeof(float);
-  static bool attr_set[256] = {};   // per device: the slice buffer is above 48 KB
+  static bool attr_set[256] = {};   // per device: the slice buffers are above 48 KB
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256)
     return oal_check_launch("decode: cudaGetDevice");
   if (!attr_set[dev]) {
-    const int bytes = (int)(decode_smem_floats(kMaxRowsPerBlock) * sizeof(float));
-    if (cudaFuncSetAttribute(decode_kernel<__nv_bfloat16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
-        cudaFuncSetAttribute(decode_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(decode_cluster_kernel<Tin>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(decode_smem_floats(kClusterRows) * sizeof(float))) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(decode_ticket_kernel<Tin>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(decode_smem_floats(kTicketRows) * sizeof(float))) != cudaSuccess)
       return oal_check_launch("decode: shared memory attribute");
     attr_set[dev] = true;
   }
+  if (use_clusters(units)) {
+    const int cs = decode_cluster_size<Tin>(packed);
+    const int rpb = ((F + cs - 1) / cs + 3) & ~3;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cs;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, (unsigned)units);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = decode_smem_floats(rpb) * sizeof(float);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaLaunchKernelEx(&cfg, decode_cluster_kernel<Tin>, q, k, v, y, a, b, C, state, Hq, Hkv, F,
+                       packed, rpb, oal_device_status_word());
+    return oal_after_launch("decode_cluster_kernel", stream);
+  }
+  const int nslices = ticket_slices(packed);
+  const size_t part_bytes = ((units * nslices * kMaxRho * kU * sizeof(float) + 255) / 256) * 256;
+  float *partial = (float *)ws;
+  unsigned *tickets = (unsigned *)((char *)ws + part_bytes);
+  if (cudaMemsetAsync(tickets, 0, units * sizeof(unsigned), stream) != cudaSuccess)
+    return oal_check_launch("decode ticket reset");
+  launch_pdl(decode_ticket_kernel<Tin>, dim3(nslices, (unsigned)units), dim3(kThreads),
+             decode_smem_floats(kTicketRows) * sizeof(float), stream, q, k, v, y, a, b, C, state,
+             Hq, Hkv, F, packed, (int)kTicketRows, nslices, partial, tickets,
+             oal_device_status_word());
+  return oal_after_launch("decode_ticket_kernel", stream);
+}
+
+oal_status launch_decode(const void *q, const void *k, const void *v, int is_bf16,
+                         int B, int Hq, int Hkv, const float *a, const float *b,
+                         const float *C, int packed, float *state, void *y,
+                         void *ws, cudaStream_t stream) {
   if (is_bf16)
-    launch_pdl(decode_kernel<__nv_bfloat16>, grid, dim3(kThreads), smem, stream,
-               (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
-               (__nv_bfloat16 *)y, a, b, C, state, Hq, Hkv, F, packed, rpb, nslices, partial,
-               tickets, oal_device_status_word());
-  else
-    launch_pdl(decode_kernel<float>, grid, dim3(kThreads), smem, stream, (const float *)q,
-               (const float *)k, (const float *)v, (float *)y, a, b, C, state, Hq, Hkv, F, packed,
-               rpb, nslices, partial, tickets, oal_device_status_word());
-  return oal_after_launch("decode_kernel", stream);
+    return launch_decode_t((const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
+                           (const __nv_bfloat16 *)v, B, Hq, Hkv, a, b, C, packed, state,
+                           (__nv_bfloat16 *)y, ws, stream);
+  return launch_decode_t((const float *)q, (const float *)k, (const float *)v, B, Hq, Hkv, a, b, C,
+                         packed, state, (float *)y, ws, stream);
 }
 
 }  // namespace oal
