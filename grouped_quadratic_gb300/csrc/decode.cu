@@ -120,7 +120,15 @@ __device__ __forceinline__ void decode_slice(const Tin *__restrict__ q, const Ti
   // per-row weights: phi_f(k) and Phi~^h_f(q^h); the table loads of all
   // heads are issued before any is used
   const size_t ctab_len = packed ? kH2Packed : kH2Full;
-  for (int n = tid; n < nrows; n += kThreads) {
+  // (rows nrows .. nrows rounded up to 4 get zero weights: the readout reads
+  // weights four rows at a time)
+  for (int n = tid; n < ((nrows + 3) & ~3); n += kThreads) {
+    if (n >= nrows) {
+      s_wk[n] = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < kMaxRho; ++hh) s_wq[hh][n] = 0.f;
+      continue;
+    }
     const int f = f0 + n;
     int r = 0, t = 0, kind;
     if (f == 0) kind = 0;
