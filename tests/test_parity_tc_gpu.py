@@ -1,0 +1,146 @@
+"""GPU parity of the tensor-core prefill and the decode paths across shapes.
+
+Each case runs through the C ABI and is compared with the fp64 oracle:
+outputs at rel-L2 <= 2e-2 (bf16 inputs, fp32 states), states at <= 1e-5 (the
+state contraction is exact up to fp32 accumulation).  The cases cover what the
+Qwen/Llama-shaped workloads do not: every group count the library accepts, a
+tail group wider than two dims (the generic kappa path), GQA ratios 1 to 8, a
+sequence split into many parts, continuation through the tensor-core path,
+chunk-boundary lengths, and both decode reductions (thread-block clusters
+for few sequences, a last-block ticket for many).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from grouped_quadratic_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+FULL, PACKED = 0, 1
+TOL_Y, TOL_S = 2e-2, 1e-5
+
+
+@pytest.fixture(scope="module")
+def oal():
+    from grouped_quadratic_gb300 import build, oal as binding
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    binding.load_library()
+    return binding
+
+
+def rel_l2(got, want):
+    return float(np.linalg.norm((got - want).ravel()) / np.linalg.norm(want.ravel()))
+
+
+def params(oal, w, layout):
+    L = torch.from_numpy(w.L).cuda()
+    group = torch.from_numpy(w.group).cuda()
+    a, b, C = oal.oal_expand_coeffs(L, group, w.eps, layout)
+    return L, group, a, b, C
+
+
+def check_prefill(oal, w, layout=PACKED):
+    Q, K, V = w.torch_inputs("cuda")
+    L, group, a, b, C = params(oal, w, layout)
+    Y, S = oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, layout, chunk=128)
+    oal.oal_sync_status()
+    Yh = Y.float().cpu().numpy()
+    assert np.isfinite(Yh).all()
+    want = oracle.direct(w.Q, w.K, w.V, w.L, w.group, w.eps)
+    assert rel_l2(Yh, want) <= TOL_Y
+    _, S_ref = oracle.recurrent(w.Q, w.K, w.V, w.L, w.group, w.eps)
+    if layout == PACKED:
+        S_ref = oracle.full_to_packed_state(S_ref, 64)
+    assert rel_l2(S.cpu().numpy(), S_ref) <= TOL_S
+
+
+@pytest.mark.parametrize("G", [1, 2, 5, 6, 7])
+def test_tc_prefill_every_group_count(oal, G):
+    w = inputs.make_workload("tc-G%d" % G, B=1, Hq=4, Hkv=2, T=300, G=G, seed=300 + G)
+    check_prefill(oal, w)
+
+
+def test_tc_prefill_wide_tail_group(oal):
+    # tail group {3, 17, 40} has three dims: the intra-chunk kappa takes the
+    # generic path (sums straight from the tiles)
+    w = inputs.make_workload("tc-wide", B=1, Hq=4, Hkv=2, T=260, G=3, seed=311,
+                             fixed_outliers=([3, 17, 40, 58], 12.0),
+                             fixed_groups=[[3, 17, 40], [58]])
+    check_prefill(oal, w)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (6, 3), (8, 2), (16, 2)])
+def test_tc_prefill_gqa_ratios(oal, Hq, Hkv):
+    w = inputs.make_workload("tc-rho", B=2, Hq=Hq, Hkv=Hkv, T=200, G=4, seed=320 + Hq)
+    check_prefill(oal, w, FULL if Hq == 6 else PACKED)
+
+
+@pytest.mark.parametrize("T", [1, 127, 128, 129, 256])
+def test_tc_prefill_chunk_boundaries(oal, T):
+    w = inputs.make_workload("tc-T", B=1, Hq=2, Hkv=1, T=T, G=4, seed=330 + T)
+    check_prefill(oal, w)
+
+
+def test_tc_prefill_many_parts(oal):
+    # one (batch, KV head): the state walk splits 20 chunks into 7 parts of 3
+    w = inputs.make_workload("tc-parts", B=1, Hq=2, Hkv=1, T=20 * 128 - 37, G=4, seed=340)
+    Q, K, V = w.torch_inputs("cuda")
+    L, group, a, b, C = params(oal, w, PACKED)
+    Y, S = oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, PACKED, chunk=128)
+    oal.oal_sync_status()
+    _, S_ref = oracle.recurrent(w.Q, w.K, w.V, w.L, w.group, w.eps)
+    assert rel_l2(S.cpu().numpy(), oracle.full_to_packed_state(S_ref, 64)) <= TOL_S
+    rows = np.concatenate([h * w.T + np.arange(0, w.T, 7) for h in range(w.Hq)])
+    want = oracle.direct(w.Q, w.K, w.V, w.L, w.group, w.eps, rows=rows)
+    got = Y.float().cpu().numpy().reshape(-1, 64)[rows]
+    assert rel_l2(got, want) <= TOL_Y
+
+
+@pytest.mark.parametrize("layout", [FULL, PACKED])
+def test_tc_prefill_continuation(oal, layout):
+    w = inputs.make_workload("tc-cont", B=2, Hq=4, Hkv=2, T=500, G=4, seed=350)
+    Q, K, V = w.torch_inputs("cuda")
+    L, group, a, b, C = params(oal, w, layout)
+    T1 = 200
+    Y1, S = oal.oal_prefill(Q[:, :, :T1].contiguous(), K[:, :, :T1].contiguous(),
+                            V[:, :, :T1].contiguous(), L, group, w.eps, a, b, C, layout,
+                            chunk=128)
+    Y2, S = oal.oal_prefill(Q[:, :, T1:].contiguous(), K[:, :, T1:].contiguous(),
+                            V[:, :, T1:].contiguous(), L, group, w.eps, a, b, C, layout,
+                            state=S, continue_from_state=True, chunk=128)
+    oal.oal_sync_status()
+    got = torch.cat([Y1, Y2], 2).float().cpu().numpy()
+    want = oracle.direct(w.Q, w.K, w.V, w.L, w.group, w.eps)
+    assert rel_l2(got, want) <= TOL_Y
+    _, S_ref = oracle.recurrent(w.Q, w.K, w.V, w.L, w.group, w.eps)
+    if layout == PACKED:
+        S_ref = oracle.full_to_packed_state(S_ref, 64)
+    assert rel_l2(S.cpu().numpy(), S_ref) <= TOL_S
+
+
+@pytest.mark.parametrize("B,Hq,Hkv", [(1, 16, 2), (2, 6, 3), (20, 4, 2)])
+def test_decode_reductions(oal, B, Hq, Hkv):
+    # B * Hkv <= 19: slices meet in a thread-block cluster; 40: ticket path
+    w = inputs.make_workload("dec-red", B=B, Hq=Hq, Hkv=Hkv, T=40 + 3, G=4, seed=360 + B,
+                             decode_steps=3)
+    Q, K, V = w.torch_inputs("cuda")
+    for layout in (FULL, PACKED):
+        L, group, a, b, C = params(oal, w, layout)
+        Tp = w.T_prefill
+        _, S = oal.oal_prefill(Q[:, :, :Tp].contiguous(), K[:, :, :Tp].contiguous(),
+                               V[:, :, :Tp].contiguous(), L, group, w.eps, a, b, C, layout)
+        ys = [oal.oal_decode_step(Q[:, :, t].contiguous(), K[:, :, t].contiguous(),
+                                  V[:, :, t].contiguous(), a, b, C, S, layout)
+              for t in range(Tp, w.T)]
+        oal.oal_sync_status()
+        got = torch.stack(ys, 2).float().cpu().numpy()
+        want = oracle.direct(w.Q, w.K, w.V, w.L, w.group, w.eps)[:, :, Tp:]
+        assert rel_l2(got, want) <= TOL_Y
+        _, S_ref = oracle.recurrent(w.Q, w.K, w.V, w.L, w.group, w.eps)
+        if layout == PACKED:
+            S_ref = oracle.full_to_packed_state(S_ref, 64)
+        assert rel_l2(S.cpu().numpy(), S_ref) <= TOL_S
