@@ -61,6 +61,32 @@ constexpr int kMaxNH = 4;        // query heads per readout block
 constexpr int kIntraNH = 1;      // query heads per intra-chunk block
 constexpr int kMaxTailG = 6;     // tail groups (G - 1 <= 6)
 constexpr size_t kSnapBytes = (size_t)kN * kKP * 2;   // 350,720 B per (unit, chunk)
+// Rank-one form of the H2 readout weights of one query head.  With
+// C_rt = M_{g(r) g(t)}, w(r, t) = alpha_r pw_t for every pair that is not
+// inside the tail groups on both sides (alpha_r = M_{g(r) b} / M_bb, pw_t =
+// 2 M_{b g(t)} / d, b the bulk group; the diagonal carries half of it).  The
+// readout builds such a word as bf16(alpha_r q_r) * bf16(pw_t q_t), one
+// multiply, and overwrites the few other words ("exceptions") with
+// q_r q_t w(r, t).  Heads whose table does not have this form (or has too many
+// exceptions) take the general path with the weights of the table.
+constexpr int kExcMax = 32;
+constexpr int kH2Words = kH2P / 2;        // 1056 bf16 pairs
+constexpr int kH2Halves = kH2Words / 16;  // 66 half blocks of 16 words
+struct RFactor {
+  float pw[64];
+  float alpha[64];
+  float exc_wlo[kExcMax];      // weights of the low / high feature of each exception word
+  float exc_whi[kExcMax];
+  uint16_t exc_word[kExcMax];  // word index in the paired H2 order, ascending
+  uint8_t exc_start[72];       // exceptions of half block hb: [exc_start[hb], exc_start[hb + 1])
+  int factored;
+  int nexc;
+  int pad[4];
+};
+static_assert(sizeof(RFactor) % 16 == 0, "factor record alignment");
+// Per query head: kKP bf16 readout weights, then the RFactor record.
+constexpr int kCoefRow = kKP + (int)sizeof(RFactor) / 2;
+static_assert((kCoefRow * 2) % 16 == 0 && (kKP * 2) % 16 == 0, "coef row alignment");
 
 __host__ __device__ constexpr int row_len(int r) { return 64 - (r & ~1); }
 __host__ __device__ constexpr int row_off(int r) {
@@ -159,11 +185,11 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
   pdl_trigger();
   pdl_wait();
   const int ncoef = (kKP + 255) / 256;
-  if ((int)blockIdx.y > ncoef) {
+  if ((int)blockIdx.y > ncoef + 1) {
     // ---- K^T for the state kernel: [unit][64 dims][nC * 128 tokens], zero past T
     __shared__ __nv_bfloat16 ks[kC][64 + 2];      // padded: column reads hit distinct banks
-    const int ntr = (gridDim.y - ncoef - 1) * gridDim.x;
-    for (int tile = blockIdx.x + gridDim.x * (blockIdx.y - ncoef - 1); tile < kt.U * kt.nC;
+    const int ntr = (gridDim.y - ncoef - 2) * gridDim.x;
+    for (int tile = blockIdx.x + gridDim.x * (blockIdx.y - ncoef - 2); tile < kt.U * kt.nC;
          tile += ntr) {
       const int u = tile / kt.nC, c = tile % kt.nC;
       __syncthreads();
@@ -209,8 +235,14 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
     atomicAdd(&scnt[g], 1);
   }
   // readout weights in the internal feature order (blockIdx.y < ncoef split
-  // the rows); block row ncoef forms the kappa plan meanwhile
+  // the rows); meanwhile block row ncoef forms the kappa plan and block row
+  // ncoef + 1 the rank-one record of the weights
   const float *Ch = Ctab + (size_t)h * (packed ? kH2Packed : kH2Full);
+  // weight of H2 entry (r, t), t >= r: C_rt / d with multiplicity two off the diagonal
+  auto h2w = [&](int r, int t) -> float {
+    if (packed) return Ch[r * kD - r * (r - 1) / 2 + (t - r)] * 0.015625f;
+    return Ch[r * kD + t] * (t == r ? 0.015625f : 0.03125f);
+  };
   for (int f = blockIdx.y * blockDim.x + tid; blockIdx.y < ncoef && f < kKP;
        f += blockDim.x * ncoef) {
     const uint16_t code = g_feat.code[f];
@@ -223,18 +255,108 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
       w = b[(size_t)h * kD + (code & 0xff)] * 0.125f;
     } else {
       const int r = code >> 8, t = code & 0xff;
-      if (t < r) w = 0.f;
-      else if (packed) w = Ch[r * kD - r * (r - 1) / 2 + (t - r)] * 0.015625f;
-      else w = Ch[r * kD + t] * (t == r ? 0.015625f : 0.03125f);
+      w = t < r ? 0.f : h2w(r, t);
     }
-    coef[(size_t)h * kKP + f] = __float2bfloat16_rn(w);
+    coef[(size_t)h * kCoefRow + f] = __float2bfloat16_rn(w);
   }
   __syncthreads();
-  if (blockIdx.y != ncoef) return;
+  if (blockIdx.y != ncoef && blockIdx.y != ncoef + 1) return;
   // kappa constants: the bulk group g* is the largest; the others are tail groups
   int gstar = 1;
   for (int g = 2; g <= G; ++g)
     if (scnt[g] > scnt[gstar]) gstar = g;
+  if (blockIdx.y == ncoef + 1) {
+    // Rank-one form of the H2 weights (RFactor): b = g*, its first dim r*.
+    __shared__ float spw[kD], salpha[kD];
+    __shared__ uint8_t sexc[kH2Words];
+    __shared__ uint16_t slist[kExcMax];
+    __shared__ int sbad, snexc;
+    RFactor *F = reinterpret_cast<RFactor *>(coef + (size_t)h * kCoefRow + kKP);
+    int rstar = 0;
+    while (rstar < kD - 1 && sgrp[rstar] != gstar) ++rstar;
+    if (tid == 0) sbad = 0;
+    if (tid < kD) {
+      const int t = tid;
+      spw[t] = t == rstar ? 2.f * h2w(rstar, rstar) : h2w(min(t, rstar), max(t, rstar));
+    }
+    __syncthreads();
+    if (tid < kD) {
+      const int r = tid;
+      float al = 1.f;
+      if (sgrp[r] != gstar) {
+        if (spw[rstar] != 0.f) al = h2w(min(r, rstar), max(r, rstar)) / spw[rstar];
+        else sbad = 1;
+      }
+      salpha[r] = al;
+    }
+    __syncthreads();
+    // exception words: a feature inside the tail groups on both sides, or one
+    // whose table weight the rank-one form does not reproduce to fp32 rounding
+    auto tail = [&](int d) { return sgrp[d] != gstar; };
+    auto feat_exc = [&](int f) -> bool {
+      const uint16_t code = g_feat.code[f];
+      const int r = code >> 8, t = code & 0xff;
+      if (t < r) return false;   // duplicate entry: weight 0 on both forms
+      if (tail(r) && tail(t)) return true;
+      const float want = h2w(r, t);
+      const float got = t == r ? 0.5f * salpha[r] * spw[r] : salpha[r] * spw[t];
+      return !(fabsf(want - got) <= 4e-6f * fmaxf(fabsf(want), fabsf(got)));
+    };
+    for (int w = tid; w < kH2Words; w += blockDim.x)
+      sexc[w] = (feat_exc(2 * w) || feat_exc(2 * w + 1)) ? 1 : 0;
+    __syncthreads();
+    if (tid < 32) {
+      // ascending list: lane l scans words [33 l, 33 l + 33)
+      constexpr int kPer = kH2Words / 32;
+      int cnt = 0;
+      for (int i = 0; i < kPer; ++i) cnt += sexc[kPer * tid + i];
+      int pre = cnt;
+  #pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, pre, o);
+        if (tid >= o) pre += v;
+      }
+      int pos = pre - cnt;
+      for (int i = 0; i < kPer; ++i)
+        if (sexc[kPer * tid + i]) {
+          if (pos < kExcMax) slist[pos] = (uint16_t)(kPer * tid + i);
+          ++pos;
+        }
+      if (tid == 31) snexc = pre;
+    }
+    __syncthreads();
+    const int nexc = snexc;
+    const int nlist = nexc < kExcMax ? nexc : kExcMax;
+    if (tid < kD) F->pw[tid] = spw[tid];
+    if (tid >= 64 && tid < 128) F->alpha[tid - 64] = salpha[tid - 64];
+    if (tid >= 128 && tid < 128 + kExcMax) {
+      const int i = tid - 128;
+      float wl = 0.f, wh = 0.f;
+      uint16_t wd = 0;
+      if (i < nlist) {
+        wd = slist[i];
+        const uint16_t cl = g_feat.code[2 * wd], ch = g_feat.code[2 * wd + 1];
+        const int r = cl >> 8, tl = cl & 0xff, th = ch & 0xff;
+        wl = tl < r ? 0.f : h2w(r, tl);
+        wh = th < r ? 0.f : h2w(r, th);
+      }
+      F->exc_wlo[i] = wl;
+      F->exc_whi[i] = wh;
+      F->exc_word[i] = wd;
+    }
+    if (tid >= 160 && tid < 160 + 72) {
+      const int hb = tid - 160;
+      int n = 0;
+      for (int i = 0; i < nlist; ++i) n += slist[i] < 16 * hb ? 1 : 0;
+      F->exc_start[hb] = (uint8_t)(hb <= kH2Halves ? n : nlist);
+    }
+    if (tid == 0) {
+      F->factored = (!sbad && nexc <= kExcMax) ? 1 : 0;
+      F->nexc = nexc;
+      for (int i = 0; i < 4; ++i) F->pad[i] = 0;
+    }
+    return;
+  }
   auto Lat = [&](int g, int c) { return c <= g ? sL[g * G1 + c] : 0.f; };
   KPlan *P = plans + h;
   if (tid >= 1 && tid <= G && tid != gstar) {
@@ -723,13 +845,14 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
 
 // ================================================================= readout kernel
 constexpr int kNB = 6;           // snapshot K-block stages
-constexpr int kNA = 6;           // A slots in tensor memory
+constexpr int kNA = 12;          // A half slots (128 x 32 bf16, 16 columns) in tensor memory
 constexpr int kTailSlots = 2 * kMaxTailG;
 
 struct __align__(1024) ReadSmem {
-  __nv_bfloat16 q[kMaxNH][kC * 64];    // 128B-swizzled [token][dim]
+  __nv_bfloat16 q[kMaxNH][kC * 64];    // 128B-swizzled [token][dim], then q^T [dim][token]
+  __nv_bfloat16 qs[kMaxNH][kC * 64];   // bf16(alpha_dim q) [dim][token]
   __nv_bfloat16 b[kNB][kN * 64];       // snapshot K blocks [n][64 features]
-  __nv_bfloat16 coef[kMaxNH][kKP];
+  __nv_bfloat16 coef[kMaxNH][kCoefRow];
   uint64_t qkv_full, b_full[kNB], b_empty[kNB], a_full[kNA], a_empty[kNA], d_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -753,14 +876,14 @@ struct ReadArgs {
   __nv_bfloat16 *Y;
   float *intra_num;            // [B*Hq][T][64] intra-chunk numerators
   float *intra_den;            // [B*Hq][T]     intra-chunk denominators
-  const __nv_bfloat16 *coef;   // [Hq][kKP]
+  const __nv_bfloat16 *coef;   // [Hq][kCoefRow]
   const KPlan *plans;          // [Hq]
   int *status;
 };
 
 constexpr int kReadThreads = 640;   // 20 warps
 constexpr int kTmemD = 0;         // D^h at [80h, 80h + 80)
-constexpr int kTmemA = 320;       // six A slots of 32 columns at [320, 512)
+constexpr int kTmemA = 320;       // twelve A half slots of 16 columns at [320, 512)
 constexpr uint32_t kReadTmemCols = 512;
 constexpr int kIntraThreads = 192;  // 6 warps
 constexpr int kTmemS = 0;         // intra kernel: two 32-key s / P sub-tiles at 0 and 32
@@ -768,55 +891,109 @@ constexpr int kTmemI = 64;        // intra kernel: numerators at [64, 128)
 constexpr uint32_t kIntraTmemCols = 128;  // up to four intra blocks per SM
 
 // ---- readout A block builders (compile-time feature layout)
-template <int KB, int P>
-__device__ __forceinline__ uint32_t h2_pair(const uint32_t (&q)[32], uint32_t cw) {
-  constexpr int f = 64 * KB + 2 * P;
-  constexpr int r = feat_r(f);
-  constexpr int t = feat_t(f);
-  const uint32_t qr = (r & 1) ? bcast_hi(q[r >> 1]) : bcast_lo(q[r >> 1]);
-  return hmul2(hmul2(qr, q[t >> 1]), cw);
+// The builder of token row m keeps p = bf16(pw * q) in registers and reads
+// q from transposed copies in shared memory, one conflict-free 16-bit load
+// per value: qs[dim][token] = bf16(alpha_dim q) for the rank-one words,
+// qT[dim][token] = q for the rest.  Rows r of the paired H2 order split into
+// runs of words that share r; a word of a run is qs_r * p_t, the row's first
+// word rescaled (the diagonal entry by 1/2, the duplicate (r, r - 1) by 0).
+__device__ __forceinline__ uint32_t qt_ld(const __nv_bfloat16 *qcol, int r) {
+  return *reinterpret_cast<const uint16_t *>(qcol + r * kC);
 }
 
-template <int KB, int H, int... P>
-__device__ __forceinline__ void h2_half(const uint32_t (&q)[32], const uint32_t (&cw)[16],
-                                        uint32_t (&out)[16], std::integer_sequence<int, P...>) {
-  ((out[P] = h2_pair<KB, 16 * H + P>(q, cw[P])), ...);
+template <int KB, int H, int P0, int... I>
+__device__ __forceinline__ void h2_run(uint32_t qr, const uint32_t (&p)[32], uint32_t (&out)[16],
+                                       std::integer_sequence<int, I...>) {
+  constexpr int r = feat_r(64 * KB + 2 * (16 * H + P0));
+  constexpr uint32_t fix = (r & 1) ? 0x3F000000u : 0x3F803F00u;   // bf16x2 (0, 1/2) : (1/2, 1)
+  ((out[P0 + I] = (64 * KB + 2 * (16 * H + P0 + I) == row_off(r))
+                      ? hmul2(hmul2(qr, p[feat_t(64 * KB + 2 * (16 * H + P0 + I)) >> 1]), fix)
+                      : hmul2(qr, p[feat_t(64 * KB + 2 * (16 * H + P0 + I)) >> 1])),
+   ...);
 }
 
-// Words 16 H .. 16 H + 15 of K block KB of one A row (token row of Phi~(Q)):
-// the weights come from this head's table in shared memory (cp = block KB).
+template <int KB, int H, int P0>
+__device__ __forceinline__ void h2_runs(const __nv_bfloat16 *qscol, const uint32_t (&p)[32],
+                                        uint32_t (&out)[16]) {
+  constexpr int r = feat_r(64 * KB + 2 * (16 * H + P0));
+  constexpr int end_w = row_off(r + 1) / 2 - 32 * KB - 16 * H;   // run end (word in half)
+  constexpr int P1 = end_w < 16 ? end_w : 16;
+  const uint32_t qr = qt_ld(qscol, r) * 0x10001u;   // (qs_r, qs_r)
+  h2_run<KB, H, P0>(qr, p, out, std::make_integer_sequence<int, P1 - P0>{});
+  if constexpr (P1 < 16) h2_runs<KB, H, P1>(qscol, p, out);
+}
+
+// Words 16 H .. 16 H + 15 of K block KB of one A row (token row of Phi~(Q)),
+// rank-one form; cw = this head's weights of block KB (H1 and H0 blocks).
 template <int KB, int H>
-__device__ __forceinline__ void build_half(const uint32_t (&q)[32], const uint4 *cp,
+__device__ __forceinline__ void build_half(const __nv_bfloat16 *qcol, const __nv_bfloat16 *qscol,
+                                           const uint32_t (&p)[32], const uint32_t *cw,
                                            uint32_t (&out)[16]) {
-  if constexpr (KB < kNKB - 1) {
-    uint32_t cw[16];
+  if constexpr (KB < 33) {
+    h2_runs<KB, H, 0>(qscol, p, out);
+  } else if constexpr (KB < kNKB - 1) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint4 v = cp[4 * H + e];
-      cw[4 * e] = v.x; cw[4 * e + 1] = v.y; cw[4 * e + 2] = v.z; cw[4 * e + 3] = v.w;
-    }
-    if constexpr (KB < 33) {
-      h2_half<KB, H>(q, cw, out, std::make_integer_sequence<int, 16>{});
-    } else {
-#pragma unroll
-      for (int p = 0; p < 16; ++p) out[p] = hmul2(q[16 * H + p], cw[p]);
+    for (int w = 0; w < 16; ++w) {
+      const int t = 2 * (16 * H + w);
+      out[w] = hmul2(qt_ld(qcol, t) | (qt_ld(qcol, t + 1) << 16), cw[16 * H + w]);
     }
   } else {
     // H0 block: feature 2176 carries a, the 15 after it are zero
 #pragma unroll
-    for (int p = 0; p < 16; ++p) out[p] = 0u;
-    if constexpr (H == 0) out[0] = cp[0].x & 0xffffu;
+    for (int w = 0; w < 16; ++w) out[w] = 0u;
+    if constexpr (H == 0) out[0] = cw[0] & 0xffffu;
+  }
+}
+
+// General form of one half block (heads whose table is not rank-one plus
+// exceptions): q_r q_t times the table weight, feature codes from the table.
+__device__ __forceinline__ void build_half_general(int kb, int H, const __nv_bfloat16 *qcol,
+                                                const uint32_t *cw, uint32_t (&out)[16]) {
+#pragma unroll
+  for (int w = 0; w < 16; ++w) {
+    const int f = 64 * kb + 2 * (16 * H + w);
+    const uint16_t code = g_feat.code[f];
+    uint32_t qa, qb;
+    if (code == 0xFFFF) {
+      qa = 0u; qb = 0u;
+    } else if (code == 0xC000) {
+      qa = 0x3F80u; qb = 0x3F80u;   // (1, 0) * (1, 0): the H0 feature
+    } else if (code & 0x8000) {
+      const int r = code & 0xff;
+      qa = 0x3F803F80u; qb = qt_ld(qcol, r) | (qt_ld(qcol, r + 1) << 16);   // H1 pair (r, r + 1)
+    } else {
+      const int r = code >> 8, t = code & 0xff;
+      qa = qt_ld(qcol, r) * 0x10001u;
+      qb = qt_ld(qcol, t) | (qt_ld(qcol, t + 1) << 16);
+    }
+    out[w] = hmul2(hmul2(qa, qb), cw[16 * H + w]);
+  }
+}
+
+// Exception words of half block hb: their exact value q_r q_t w(r, t), stored
+// over the rank-one words already in tensor memory.
+__device__ __noinline__ void patch_exceptions(const RFactor &F, int hb, const __nv_bfloat16 *qcol,
+                                              uint32_t taddr) {
+  for (int e = F.exc_start[hb]; e < F.exc_start[hb + 1]; ++e) {
+    const int wd = F.exc_word[e];
+    const uint16_t code = g_feat.code[2 * wd];
+    const int r = code >> 8, t = code & 0xff;
+    const float qr = __uint_as_float(qt_ld(qcol, r) << 16);
+    const float lo = qr * __uint_as_float(qt_ld(qcol, t) << 16) * F.exc_wlo[e];
+    const float hi = qr * __uint_as_float(qt_ld(qcol, t + 1) << 16) * F.exc_whi[e];
+    tmem_st1(taddr + (uint32_t)(wd - 16 * hb), pack_bf16x2(lo, hi));
   }
 }
 
 #define OAL_BUILD_CASE(n) \
   case n:                 \
-    build_half<n, H>(q, cp, out); \
+    build_half<n, H>(qcol, qscol, p, cw, out); \
     break;
 
 template <int H>
-__device__ __forceinline__ void build_dispatch(int kb, const uint32_t (&q)[32], const uint4 *cp,
-                                               uint32_t (&out)[16]) {
+__device__ __forceinline__ void build_dispatch(int kb, const __nv_bfloat16 *qcol,
+                                               const __nv_bfloat16 *qscol, const uint32_t (&p)[32],
+                                               const uint32_t *cw, uint32_t (&out)[16]) {
   switch (kb) {
     OAL_BUILD_CASE(0) OAL_BUILD_CASE(1) OAL_BUILD_CASE(2) OAL_BUILD_CASE(3)
     OAL_BUILD_CASE(4) OAL_BUILD_CASE(5) OAL_BUILD_CASE(6) OAL_BUILD_CASE(7)
@@ -1194,8 +1371,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   const int bidx = unit / args.Hkv, kv = unit % args.Hkv;
   const int h0 = kv * args.rho + hg * args.nh_per_block;
   const int nh = min(args.nh_per_block, args.rho - hg * args.nh_per_block);
-  const int njobs = kNKB * nh;
-  constexpr int kIss0 = 16, kMem = 18, kTma = 19;
+  constexpr int kIss0 = 16;   // issuer of head h: warp 16 + h (head 0's also runs the TMA)
   pdl_trigger();
 
   if (tid == 0) {
@@ -1203,132 +1379,221 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     mbar_init(&s.qkv_full, 1);
     for (int i = 0; i < kNB; ++i) {
       mbar_init(&s.b_full[i], 1);
-      mbar_init(&s.b_empty[i], nh >= 2 ? 2 : 1);   // one commit per readout issuer
+      mbar_init(&s.b_empty[i], nh);     // one commit per head's issuer
     }
     for (int i = 0; i < kNA; ++i) { mbar_init(&s.a_full[i], 4); mbar_init(&s.a_empty[i], 1); }
-    mbar_init(&s.d_full, 2);                       // both issuers done
+
+    mbar_init(&s.d_full, nh);           // every head's issuer done
     fence_mbar_init();
+    // Q is an input of the call that no kernel of it writes: its load starts
+    // before the wait on the previous kernels
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmS);
+    mbar_arrive_expect_tx(&s.qkv_full, (uint32_t)nh * kC * 64 * 2);
+    for (int h = 0; h < nh; ++h)
+      tma_load_3d(s.q[h], &tmQ, &s.qkv_full, 0, c * kC, bidx * args.Hq + h0 + h);
   }
-  if (warp == kMem) {
+  if (warp == kIss0) {
     tmem_alloc(&s.tmem_base, kReadTmemCols);
     tmem_relinquish();
   }
   pdl_wait();   // weights, snapshots and intra rows of the previous kernels
-  for (int n = tid; n < nh * (kKP / 8); n += kReadThreads) {
-    const int hh = n / (kKP / 8), e = n % (kKP / 8);
+  if (tid == 32) {
+    // the intra-chunk rows the epilogue reads, into L2 while the contraction runs
+    const int rows = min(kC, args.T - c * kC);
+    for (int h = 0; h < nh; ++h) {
+      const size_t row0 = ((size_t)bidx * args.Hq + h0 + h) * args.T + (size_t)c * kC;
+      prefetch_l2(args.intra_num + row0 * 64, (uint32_t)rows * 256u);
+      const uintptr_t d0 = (reinterpret_cast<uintptr_t>(args.intra_den + row0) + 15) & ~uintptr_t(15);
+      const uintptr_t d1 = reinterpret_cast<uintptr_t>(args.intra_den + row0 + rows) & ~uintptr_t(15);
+      if (d1 > d0) prefetch_l2(reinterpret_cast<const void *>(d0), (uint32_t)(d1 - d0));
+    }
+  }
+  for (int n = tid; n < nh * (kCoefRow / 8); n += kReadThreads) {
+    const int hh = n / (kCoefRow / 8), e = n % (kCoefRow / 8);
     reinterpret_cast<uint4 *>(s.coef[hh])[e] =
-        reinterpret_cast<const uint4 *>(args.coef + (size_t)(h0 + hh) * kKP)[e];
+        reinterpret_cast<const uint4 *>(args.coef + (size_t)(h0 + hh) * kCoefRow)[e];
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = s.tmem_base;
-  if (warp < 4) {
-    // zero the accumulators D^h of this thread's lane
-    uint32_t z[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) z[e] = 0u;
-    for (int col = 0; col < 80 * nh; col += 16) tmem_st16(tmem_lane_addr(tb, warp, kTmemD + col), z);
-    tmem_wait_st();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
   volatile int *abort_flag = &s.abort_flag;
 
-  if (warp == kIss0 || warp == kIss0 + 1) {
-    if (lane == 0) {
-      // ---------------- readout UMMA issuer t: jobs t, t + 2, t + 4, ...
-      const int t = warp - kIss0;
+  if (warp >= kIss0) {
+    const int hh = warp - kIss0;
+    if (hh < nh) {
+      // ---------------- UMMA issuer of head hh: D^h = sum over K blocks of A_kb B_kb.
+      // One warp per head runs the loop (warp-uniform; an elected lane issues),
+      // so four heads' MMAs are issued in parallel.  Head 0's warp also loads
+      // the snapshot K blocks (6 stages) by TMA.
       const uint32_t id80 = idesc_bf16_f32(128, kN, 0);
       const uint64_t bdesc0 = sdesc_sw128(smem_u32(s.b[0]), 16, 1024);
       constexpr uint64_t kStageStep = (kN * 64 * 2) >> 4;   // one snapshot stage
-      int jr = t, kb = t / nh, hh = t % nh;
-      int st = kb % kNB, sph = (kb / kNB) & 1;               // stage and its phase
-      int slot = t, aph = 0;                                 // A slot and its phase
-      int kb_seen = -1;
-      while (jr < njobs) {
-        if (kb != kb_seen) {
-          if (!mbar_wait(&s.b_full[st], sph, abort_flag, args.status)) break;
-          kb_seen = kb;
+      const uint32_t dt = tb + kTmemD + 80 * hh;
+      const bool tma = hh == 0;
+      int loaded = 0;                            // K blocks whose load was issued
+      auto load_block = [&](int kb2) {
+        if (lane == 0) {
+          const int st2 = kb2 % kNB;
+          mbar_arrive_expect_tx(&s.b_full[st2], kN * 64 * 2);
+          tma_load_3d(s.b[st2], &tmS, &s.b_full[st2], 64 * kb2, 0, unit * args.nC + c);
         }
-        if (!mbar_wait(&s.a_full[slot], aph, abort_flag, args.status)) break;
-        tc_fence_after();
+      };
+      if (tma)
+        for (; loaded < kNB && loaded < kNKB; ++loaded) load_block(loaded);
+      // this head owns half slots [hh * nhs, (hh + 1) * nhs), used in turn
+      const int nhs = kNA / nh > 6 ? 6 : kNA / nh;
+      const int a0 = hh * nhs;
+      const int fper = (nhs & 1) ? nhs : nhs / 2;   // K blocks between two uses as a first half
+      int st = 0, sph = 0;                       // snapshot stage and its phase
+      int hs = 0;                                // first half slot of K block kb: (2 kb) % nhs
+      int fk = 0, fph = 0;                       // kb % fper and the phase of (kb / fper)
+      bool ok = true;
+      for (int kb = 0; kb < kNKB && ok; ++kb) {
+        if (tma) {
+          // refill stages freed by every head (K block `loaded` reuses the
+          // stage of loaded - kNB); blocking only for the block needed now
+          while (loaded < kNKB) {
+            const int st2 = loaded % kNB, ph2 = ((loaded / kNB) & 1) ^ 1;
+            if (loaded > kb) {
+              if (!mbar_test(&s.b_empty[st2], ph2)) break;
+            } else if (!mbar_wait(&s.b_empty[st2], ph2, abort_flag, args.status)) {
+              ok = false;
+              break;
+            }
+            load_block(loaded++);
+          }
+          if (!ok) break;
+        }
+        if (!mbar_wait(&s.b_full[st], sph, abort_flag, args.status)) break;
         const uint64_t bd = bdesc0 + kStageStep * st;
-        const uint32_t at = tb + kTmemA + 32 * slot;
-        const uint32_t dt = tb + kTmemD + 80 * hh;
-        umma_ts(dt, at, bd, id80, 1u);
+        // K block kb: halves of K = 32 in half slots (2 kb) % nhs and
+        // (2 kb + 1) % nhs of this head (the last block: one half of K = 16);
+        // its builders arrive once, on the first half slot's barrier
+        const int hs1 = hs + 1 == nhs ? 0 : hs + 1;
+        if (!mbar_wait(&s.a_full[a0 + hs], fph, abort_flag, args.status)) break;
+        tc_fence_after();
+        const uint32_t at0 = tb + kTmemA + 16 * (a0 + hs), at1 = tb + kTmemA + 16 * (a0 + hs1);
         if (kb != kNKB - 1) {
-          umma_ts(dt, at + 8, bd + 2, id80, 1u);
-          umma_ts(dt, at + 16, bd + 4, id80, 1u);
-          umma_ts(dt, at + 24, bd + 6, id80, 1u);
+          umma_ts_warp(dt, at0, bd, id80, kb > 0 ? 1u : 0u);
+          umma_ts_warp(dt, at0 + 8, bd + 2, id80, 1u);
+          umma_ts_warp(dt, at1, bd + 4, id80, 1u);
+          umma_ts_warp(dt, at1 + 8, bd + 6, id80, 1u);
+          umma_commit_warp(&s.a_empty[a0 + hs]);
+          umma_commit_warp(&s.a_empty[a0 + hs1]);
+        } else {
+          umma_ts_warp(dt, at0, bd, id80, 1u);
+          umma_commit_warp(&s.a_empty[a0 + hs]);
         }
-        umma_commit(&s.a_empty[slot]);
-        // advance to this issuer's next job
-        jr += 2;
-        slot += 2;
-        if (slot >= kNA) { slot -= kNA; aph ^= 1; }
-        hh += 2;
-        int nkb = kb;
-        while (hh >= nh) { hh -= nh; ++nkb; }
-        if (nkb != kb || jr >= njobs) {
-          umma_commit(&s.b_empty[st]);        // this issuer is done with the stage
-          for (; kb < nkb; ++kb)
-            if (++st == kNB) { st = 0; sph ^= 1; }
-        }
-      }
-      umma_commit(&s.d_full);
-      mbar_wait_teardown(&s.d_full, 0, args.status);   // no MMA in flight at exit
-    }
-    __syncwarp();
-  } else if (warp == kTma) {
-    if (lane == 0) {
-      // ---------------- TMA producer
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmS);
-      mbar_arrive_expect_tx(&s.qkv_full, (uint32_t)nh * kC * 64 * 2);
-      for (int hh = 0; hh < nh; ++hh)
-        tma_load_3d(s.q[hh], &tmQ, &s.qkv_full, 0, c * kC, bidx * args.Hq + h0 + hh);
-      int issued = 0, st = 0, sph = 0;
-      for (int kb = 0; kb < kNKB; ++kb) {
-        if (!mbar_wait(&s.b_empty[st], sph ^ 1, abort_flag, args.status)) break;
-        mbar_arrive_expect_tx(&s.b_full[st], kN * 64 * 2);
-        tma_load_3d(s.b[st], &tmS, &s.b_full[st], 64 * kb, 0, unit * args.nC + c);
-        issued = kb + 1;
+        umma_commit_warp(&s.b_empty[st]);
+        hs = hs1 + 1 == nhs ? 0 : hs1 + 1;
+        if (++fk == fper) { fk = 0; fph ^= 1; }
         if (++st == kNB) { st = 0; sph ^= 1; }
       }
-      // copies still in flight must land before the block exits
-      mbar_wait_teardown(&s.qkv_full, 0, args.status);
-      for (int kb = max(0, issued - kNB); kb < issued; ++kb)
-        mbar_wait_teardown(&s.b_full[kb % kNB], (kb / kNB) & 1, args.status);
+      umma_commit_warp(&s.d_full);
+      mbar_wait_teardown(&s.d_full, 0, args.status);   // no MMA in flight at exit
+      if (tma) {
+        // copies still in flight must land before the block exits
+        mbar_wait_teardown(&s.qkv_full, 0, args.status);
+        for (int kb = max(0, loaded - kNB); kb < loaded; ++kb)
+          mbar_wait_teardown(&s.b_full[kb % kNB], (kb / kNB) & 1, args.status);
+      }
     }
     __syncwarp();
   } else if (warp < 16) {
     // ---------------- readout A builders: group hh builds head hh; thread = token row
     const int m = 32 * (warp & 3) + lane;
     const int hh = warp >> 2;
-    if (hh < nh && mbar_wait(&s.qkv_full, 0, abort_flag, args.status)) {
-      uint32_t q[32];
-      const uint8_t *qrow = reinterpret_cast<const uint8_t *>(s.q[hh]) + m * 128;
+    // q^T [64 dims][128 tokens] replaces the swizzled Q tile of head hh
+    __nv_bfloat16 *qT = s.q[hh];
+    const __nv_bfloat16 *qcol = qT + m, *qscol = s.qs[hh] + m;
+    const RFactor &F = *reinterpret_cast<const RFactor *>(s.coef[hh] + kKP);
+    const bool ok = hh < nh && mbar_wait(&s.qkv_full, 0, abort_flag, args.status);
+    uint32_t p[32], q[32];
+    if (ok) {
+      // p_t = bf16(pw_t q_t): the rank-one weights applied once per token row
+      const uint8_t *qrow = reinterpret_cast<const uint8_t *>(qT) + m * 128;
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
         const uint4 v = *reinterpret_cast<const uint4 *>(qrow + ((cc ^ (m & 7)) << 4));
         q[4 * cc] = v.x; q[4 * cc + 1] = v.y; q[4 * cc + 2] = v.z; q[4 * cc + 3] = v.w;
       }
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        p[i] = pack_bf16x2(F.pw[2 * i] * __uint_as_float(q[i] << 16),
+                           F.pw[2 * i + 1] * __uint_as_float(q[i] & 0xffff0000u));
+    }
+    if (hh < nh) {   // all four warps of the group pass both barriers, ok or not
+      named_bar(1 + hh, 128);   // every row of the tile read
+      if (ok) {
+        uint16_t *qs = reinterpret_cast<uint16_t *>(s.qs[hh]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float q0 = __uint_as_float(q[i] << 16), q1 = __uint_as_float(q[i] & 0xffff0000u);
+          reinterpret_cast<uint16_t *>(qT)[(2 * i) * kC + m] = (uint16_t)(q[i] & 0xffffu);
+          reinterpret_cast<uint16_t *>(qT)[(2 * i + 1) * kC + m] = (uint16_t)(q[i] >> 16);
+          const uint32_t sc = pack_bf16x2(F.alpha[2 * i] * q0, F.alpha[2 * i + 1] * q1);
+          qs[(2 * i) * kC + m] = (uint16_t)(sc & 0xffffu);
+          qs[(2 * i + 1) * kC + m] = (uint16_t)(sc >> 16);
+        }
+      }
+      named_bar(1 + hh, 128);   // q^T and qs complete
+    }
+    if (ok) {
+      const bool factored = F.factored != 0;
+      const int nhs = kNA / nh > 6 ? 6 : kNA / nh;   // as the issuer
+      const int a0 = hh * nhs;
+      int hs = 0;                // first half slot of K block kb, (2 kb) % nhs, as the issuer
+      uint32_t uph = 0;          // bit j: number of completed uses of half slot j, mod 2
+      uint64_t em = 0;                               // H2 half blocks 0..63 with exception words
+      uint32_t em2 = 0;                              // half blocks 64, 65
+      if (factored)
+        for (int hb = 0; hb < kH2Halves; ++hb)
+          if (F.exc_start[hb] != F.exc_start[hb + 1]) {
+            if (hb < 64) em |= 1ull << hb;
+            else em2 |= 1u << (hb - 64);
+          }
       for (int kb = 0; kb < kNKB; ++kb) {
-        const int jr = kb * nh + hh;
-        const int slot = jr % kNA, aph = (jr / kNA) & 1;
-        const uint4 *cp = reinterpret_cast<const uint4 *>(s.coef[hh] + 64 * kb);
-        uint32_t out[16];
-        build_dispatch<0>(kb, q, cp, out);
-        if (!mbar_wait(&s.a_empty[slot], aph ^ 1, abort_flag, args.status)) break;
-        tmem_st16(tmem_lane_addr(tb, warp, kTmemA + 32 * slot), out);
-        build_dispatch<1>(kb, q, cp, out);
-        tmem_st16(tmem_lane_addr(tb, warp, kTmemA + 32 * slot + 16), out);
+        const uint32_t *cw = reinterpret_cast<const uint32_t *>(s.coef[hh] + 64 * kb);
+        // p is loop-invariant: keep the compiler from hoisting the per-row
+        // products of every K block out of the loop (they would spill)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(p[i]));
+        uint32_t out0[16], out1[16];
+        if (factored) {
+          build_dispatch<0>(kb, qcol, qscol, p, cw, out0);
+          build_dispatch<1>(kb, qcol, qscol, p, cw, out1);
+        } else {
+          build_half_general(kb, 0, qcol, cw, out0);
+          build_half_general(kb, 1, qcol, cw, out1);
+        }
+        // half index hx = 2 kb + H goes to half slot hx % nhs, its (hx / nhs)-th
+        // use: wait for the MMAs of its previous use, store, arrive once
+        const uint32_t xb = 2 * kb < 64 ? (uint32_t)(em >> (2 * kb)) & 3u : (em2 >> (2 * kb - 64)) & 3u;
+        const bool two = kb != kNKB - 1;   // the last block has one half
+        const int hs1 = hs + 1 == nhs ? 0 : hs + 1;
+        const uint32_t par0 = ((uph >> hs) & 1u) ^ 1u, par1 = ((uph >> hs1) & 1u) ^ 1u;
+        uint64_t *e0 = &s.a_empty[a0 + hs], *e1 = &s.a_empty[a0 + hs1];
+        if (!mbar_test(e0, par0) && !mbar_wait(e0, par0, abort_flag, args.status)) break;
+        const uint32_t ta0 = tmem_lane_addr(tb, warp, kTmemA + 16 * (a0 + hs));
+        const uint32_t ta1 = tmem_lane_addr(tb, warp, kTmemA + 16 * (a0 + hs1));
+        tmem_st16(ta0, out0);
+        if (two) {
+          if (!mbar_test(e1, par1) && !mbar_wait(e1, par1, abort_flag, args.status)) break;
+          tmem_st16(ta1, out1);
+        }
+        if (xb) {
+          tmem_wait_st();
+          if (xb & 1u) patch_exceptions(F, 2 * kb, qcol, ta0);
+          if (xb & 2u) patch_exceptions(F, 2 * kb + 1, qcol, ta1);
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.a_full[slot]);
+        if (lane == 0) mbar_arrive(&s.a_full[a0 + hs]);
+        uph ^= (1u << hs) | (two ? 1u << hs1 : 0u);
+        hs = hs1 + 1 == nhs ? 0 : hs1 + 1;
       }
     }
     if (hh < nh) {
@@ -1382,7 +1647,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMem) {
+  if (warp == kIss0) {
     tc_fence_after();
     tmem_dealloc(tb, kReadTmemCols);
   }
@@ -1434,7 +1699,7 @@ static Layout plan_layout(int B, int Hq, int Hkv, int T) {
   size_t o = 0;
   L.snap_off = o; o = al(o + (size_t)L.U * L.nC * kSnapBytes);
   L.ptot_off = o; o = al(o + (size_t)L.U * L.nparts * kTiles * 128 * kN * sizeof(float));
-  L.coef_off = o; o = al(o + (size_t)Hq * kKP * 2);
+  L.coef_off = o; o = al(o + (size_t)Hq * kCoefRow * 2);
   L.plan_off = o; o = al(o + (size_t)Hq * sizeof(KPlan));
   L.inum_off = o; o = al(o + (size_t)B * Hq * T * 64 * sizeof(float));
   L.iden_off = o; o = al(o + (size_t)B * Hq * T * sizeof(float));
@@ -1494,7 +1759,7 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   kta.T = T; kta.Tpad = Tpad; kta.U = lay.U; kta.nC = lay.nC;
   const int ntiles = lay.U * lay.nC;
   const int ntr = (std::min(ntiles, 2 * 152) + Hq - 1) / Hq;   // block rows of transposes
-  launch_pdl(tc_prep_kernel, dim3(Hq, (kKP + 255) / 256 + 1 + ntr), dim3(256), 0, stream, a, b, C,
+  launch_pdl(tc_prep_kernel, dim3(Hq, (kKP + 255) / 256 + 2 + ntr), dim3(256), 0, stream, a, b, C,
              L, group, G, eps, packed, coef, plans, status, kta);
   oal_status st = oal_after_launch("tc_prep_kernel", stream);
   if (st != OAL_OK) return st;

@@ -92,6 +92,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
   }
 }
 
+// Bounded wait that polls with test_wait instead of sleeping in try_wait:
+// for waits on the critical path of a short producer / consumer ring, where
+// the wake-up of a suspended thread would add to every round trip.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity,
+                                               volatile int *abort, int *status) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = cycles_now();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test(bar, parity)) return true;
+    if (*abort) return false;
+    if (cycles_now() - t0 > kWaitLimitCycles) {
+      *abort = 1;
+      if (status) atomicCAS(status, 0, 4 /* OAL_ERR_TIMEOUT */);
+      return false;
+    }
+  }
+}
+
 // Teardown wait: ignores the abort flag (used to drain copies and MMAs that
 // are already in flight before a block releases its memory); bounded.
 constexpr uint64_t kTeardownLimitCycles = 1ull << 29;  // about 0.25 s
@@ -118,6 +137,14 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Bulk prefetch of [src, src + bytes) into L2 (src 16-byte aligned, bytes a
+// multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
 }
 
 // Plain (untiled) bulk copy global -> shared; both addresses 16-byte aligned,
@@ -201,6 +228,26 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
+// Warp-wide forms: every lane of the warp executes them (operands warp-
+// uniform) and one elected lane issues.  Keeping the issuing loop warp-uniform
+// lets the operands stay in uniform registers; an issuing loop under a
+// single-lane branch pays a long per-MMA issue latency.
+__device__ __forceinline__ void umma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_warp(uint64_t *bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
 // Arrive (once) on `bar` when all previously issued tcgen05 ops of this thread finish.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile(
@@ -231,6 +278,9 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
       "r"(r[15])
       : "memory");
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
