@@ -92,25 +92,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
   }
 }
 
-// Bounded wait that polls with test_wait instead of sleeping in try_wait:
-// for waits on the critical path of a short producer / consumer ring, where
-// the wake-up of a suspended thread would add to every round trip.
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity,
-                                               volatile int *abort, int *status) {
-  if (mbar_test(bar, parity)) return true;
-  const uint64_t t0 = cycles_now();
-  while (true) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_test(bar, parity)) return true;
-    if (*abort) return false;
-    if (cycles_now() - t0 > kWaitLimitCycles) {
-      *abort = 1;
-      if (status) atomicCAS(status, 0, 4 /* OAL_ERR_TIMEOUT */);
-      return false;
-    }
-  }
-}
-
 // Teardown wait: ignores the abort flag (used to drain copies and MMAs that
 // are already in flight before a block releases its memory); bounded.
 constexpr uint64_t kTeardownLimitCycles = 1ull << 29;  // about 0.25 s

@@ -4,7 +4,9 @@ Each case runs through the C ABI and is compared with the fp64 oracle:
 outputs at rel-L2 <= 2e-2 (bf16 inputs, fp32 states), states at <= 1e-5 (the
 state contraction is exact up to fp32 accumulation).  The cases cover what the
 Qwen/Llama-shaped workloads do not: every group count the library accepts, a
-tail group wider than two dims (the generic kappa path), GQA ratios 1 to 8, a
+tail group wider than two dims (the generic kappa path), readout weights
+without the rank-one form or with exception words at the first and last
+rows (the general and the patched builder paths), GQA ratios 1 to 8, a
 sequence split into many parts, continuation through the tensor-core path,
 chunk-boundary lengths, and both decode reductions (thread-block clusters
 for few sequences, a last-block ticket for many).
@@ -70,6 +72,35 @@ def test_tc_prefill_wide_tail_group(oal):
     w = inputs.make_workload("tc-wide", B=1, Hq=4, Hkv=2, T=260, G=3, seed=311,
                              fixed_outliers=([3, 17, 40, 58], 12.0),
                              fixed_groups=[[3, 17, 40], [58]])
+    check_prefill(oal, w)
+
+
+def test_tc_prefill_readout_general_weights(oal):
+    # heads 0 and 2: the bulk row of L is zero, so M_bb = 0 and the readout
+    # weights have no rank-one form; those heads take the general builder
+    # path while heads 1 and 3 (same kv heads) keep the rank-one path
+    w = inputs.make_workload("tc-gen", B=1, Hq=4, Hkv=2, T=290, G=4, seed=315)
+    w.L[0, 1, :] = 0.0
+    w.L[2, 1, :] = 0.0
+    check_prefill(oal, w)
+    check_prefill(oal, w, FULL)
+
+
+def test_tc_prefill_readout_many_exception_words(oal):
+    # a tail group of nine dims: 45 pairs inside it on both sides, more
+    # exception words than the rank-one record holds (general path)
+    dims = [2, 9, 17, 23, 30, 38, 44, 51, 60]
+    w = inputs.make_workload("tc-exc", B=1, Hq=2, Hkv=1, T=200, G=3, seed=316,
+                             fixed_outliers=(dims[:4], 10.0), fixed_groups=[dims, [63]])
+    check_prefill(oal, w)
+
+
+def test_tc_prefill_readout_exception_words(oal):
+    # six tail dims in three groups, one of them at dim 0 and one at dim 63:
+    # exception words at the first and the last paired rows
+    w = inputs.make_workload("tc-exc2", B=1, Hq=4, Hkv=1, T=257, G=4, seed=317,
+                             fixed_outliers=([0, 31, 32, 63], 14.0),
+                             fixed_groups=[[0, 31], [32, 62], [63, 1]])
     check_prefill(oal, w)
 
 
