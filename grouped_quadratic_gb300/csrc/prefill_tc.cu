@@ -56,11 +56,14 @@ constexpr int kKP = 2192;        // internal features
 constexpr int kH2P = 2112;       // paired H2 features
 constexpr int kNKB = 35;         // readout K blocks of 64 (the last one has K = 16)
 constexpr int kTiles = 18;       // 128-feature tiles of the state kernel
-constexpr int kN = 80;           // snapshot rows: 64 value columns, the "1" column, 15 zeros
+constexpr int kN = 80;           // UMMA N of [v | 1]: 64 value columns, the "1" column, 15 zeros
 constexpr int kMaxNH = 4;        // query heads per readout block
 constexpr int kIntraNH = 1;      // query heads per intra-chunk block
 constexpr int kMaxTailG = 6;     // tail groups (G - 1 <= 6)
-constexpr size_t kSnapBytes = (size_t)kN * kKP * 2;   // 350,720 B per (unit, chunk)
+// Snapshot rows: the 64 value columns and the "1" column; the readout's TMA box
+// is kN = 80 rows high and reads rows 65..79 as zero (out of range).
+constexpr int kSnapRows = kU;
+constexpr size_t kSnapBytes = (size_t)kSnapRows * kKP * 2;   // 284,960 B per (unit, chunk)
 // Rank-one form of the H2 readout weights of one query head.  With
 // C_rt = M_{g(r) g(t)}, w(r, t) = alpha_r pw_t for every pair that is not
 // inside the tail groups on both sides (alpha_r = M_{g(r) b} / M_bb, pw_t =
@@ -271,20 +274,33 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
     __shared__ uint8_t sexc[kH2Words];
     __shared__ uint16_t slist[kExcMax];
     __shared__ int sbad, snexc;
+    // this head's C table and the feature codes in shared memory: every
+    // check below reads them many times
+    __shared__ __align__(16) float sC[kH2Full];
+    __shared__ uint16_t scode[kH2P];
+    const int nCt = packed ? kH2Packed : kH2Full;
+    for (int i = tid; i < nCt / 4; i += blockDim.x)
+      reinterpret_cast<float4 *>(sC)[i] = reinterpret_cast<const float4 *>(Ch)[i];
+    for (int i = tid; i < kH2P; i += blockDim.x) scode[i] = g_feat.code[i];
     RFactor *F = reinterpret_cast<RFactor *>(coef + (size_t)h * kCoefRow + kKP);
     int rstar = 0;
     while (rstar < kD - 1 && sgrp[rstar] != gstar) ++rstar;
     if (tid == 0) sbad = 0;
+    __syncthreads();
+    auto h2ws = [&](int r, int t) -> float {   // h2w from the staged table
+      if (packed) return sC[r * kD - r * (r - 1) / 2 + (t - r)] * 0.015625f;
+      return sC[r * kD + t] * (t == r ? 0.015625f : 0.03125f);
+    };
     if (tid < kD) {
       const int t = tid;
-      spw[t] = t == rstar ? 2.f * h2w(rstar, rstar) : h2w(min(t, rstar), max(t, rstar));
+      spw[t] = t == rstar ? 2.f * h2ws(rstar, rstar) : h2ws(min(t, rstar), max(t, rstar));
     }
     __syncthreads();
     if (tid < kD) {
       const int r = tid;
       float al = 1.f;
       if (sgrp[r] != gstar) {
-        if (spw[rstar] != 0.f) al = h2w(min(r, rstar), max(r, rstar)) / spw[rstar];
+        if (spw[rstar] != 0.f) al = h2ws(min(r, rstar), max(r, rstar)) / spw[rstar];
         else sbad = 1;
       }
       salpha[r] = al;
@@ -294,11 +310,11 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
     // whose table weight the rank-one form does not reproduce to fp32 rounding
     auto tail = [&](int d) { return sgrp[d] != gstar; };
     auto feat_exc = [&](int f) -> bool {
-      const uint16_t code = g_feat.code[f];
+      const uint16_t code = scode[f];
       const int r = code >> 8, t = code & 0xff;
       if (t < r) return false;   // duplicate entry: weight 0 on both forms
       if (tail(r) && tail(t)) return true;
-      const float want = h2w(r, t);
+      const float want = h2ws(r, t);
       const float got = t == r ? 0.5f * salpha[r] * spw[r] : salpha[r] * spw[t];
       return !(fabsf(want - got) <= 4e-6f * fmaxf(fabsf(want), fabsf(got)));
     };
@@ -335,10 +351,10 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
       uint16_t wd = 0;
       if (i < nlist) {
         wd = slist[i];
-        const uint16_t cl = g_feat.code[2 * wd], ch = g_feat.code[2 * wd + 1];
+        const uint16_t cl = scode[2 * wd], ch = scode[2 * wd + 1];
         const int r = cl >> 8, tl = cl & 0xff, th = ch & 0xff;
-        wl = tl < r ? 0.f : h2w(r, tl);
-        wh = th < r ? 0.f : h2w(r, th);
+        wl = tl < r ? 0.f : h2ws(r, tl);
+        wh = th < r ? 0.f : h2ws(r, th);
       }
       F->exc_wlo[i] = wl;
       F->exc_whi[i] = wh;
@@ -503,7 +519,7 @@ struct StateArgs {
   const float *state_in;     // external state (continue) or null
   float *state_out;          // external state (mode 1, last part)
   float *ptot;               // [U][nparts][kTiles][128][kN] fp32 part totals
-  __nv_bfloat16 *snap;       // [U*nC][kN][kKP]
+  __nv_bfloat16 *snap;       // [U*nC][kSnapRows][kKP]
   int *status;
 };
 
@@ -764,13 +780,12 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       }
     }
     __nv_bfloat16 *snap_row =
-        f < kKP ? args.snap + ((size_t)unit * args.nC + c0) * kN * kKP + f : nullptr;
+        f < kKP ? args.snap + ((size_t)unit * args.nC + c0) * kSnapRows * kKP + f : nullptr;
     auto write_snapshot = [&](int cc) {   // S_{cc-1} for chunk cc of this part
       if (snap_row) {
-        __nv_bfloat16 *dst = snap_row + (size_t)cc * kN * kKP;
+        __nv_bfloat16 *dst = snap_row + (size_t)cc * kSnapRows * kKP;
 #pragma unroll
-        for (int n = 0; n < kN; ++n)
-          dst[(size_t)n * kKP] = n < kU ? __float2bfloat16_rn(S[n]) : __float2bfloat16_rn(0.f);
+        for (int n = 0; n < kSnapRows; ++n) dst[(size_t)n * kKP] = __float2bfloat16_rn(S[n]);
       }
     };
     if (mode == 1 && nchunks > 0) write_snapshot(0);
@@ -1750,7 +1765,7 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
       !make_map3(&tmK, Kt, (uint64_t)Tpad, 64, (uint64_t)lay.U, (uint64_t)Tpad * 2,
                  (uint64_t)Tpad * 2 * 64, 64) ||
       !make_map3(&tmV, V, 64, T, (uint64_t)lay.U, rowb, rowb * T, kC) ||
-      !make_map3(&tmS, snap, kKP, kN, (uint64_t)lay.U * lay.nC, (uint64_t)kKP * 2, kSnapBytes,
+      !make_map3(&tmS, snap, kKP, kSnapRows, (uint64_t)lay.U * lay.nC, (uint64_t)kKP * 2, kSnapBytes,
                  kN))
     return oal_fail(OAL_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 

@@ -144,7 +144,7 @@ oal_status oal_prefill(const void *Q, const void *K, const void *V,
  *  Limit: a problem whose oal_prefill_workspace_bytes(...) exceeds
  *    OAL_PREFILL_NOALLOC_SCRATCH_BYTES is rejected with OAL_ERR_INVALID_ARG
  *    and a message giving both sizes (in this version bf16 with B = 1,
- *    Hq = 14, Hkv = 2 fits up to T = 6508); use oal_prefill with a
+ *    Hq = 14, Hkv = 2 fits up to T = 7296); use oal_prefill with a
  *    workspace beyond that.
  *  First call on a device: looks up the array's device address with
  *    cudaGetSymbolAddress on the current device (this may load the
