@@ -18,8 +18,10 @@
 // ways.  Few sequences: the slices of one (batch, KV head) form a thread-block
 // cluster and meet in distributed shared memory, where the first block sums
 // them in rank order and divides (no scratch, no extra launch).  Many
-// sequences: 128-row slices, partials in the workspace, and the last block of
-// a (batch, KV head) to finish (atomic ticket) sums them in a fixed order.
+// sequences: persistent blocks stream runs of 112-row slices with the next
+// slice's copy in flight, sum their partials per (batch, KV head) in shared
+// memory and write them to the workspace; a second small kernel adds them in
+// a fixed order and divides.
 #include <cooperative_groups.h>
 
 #include "oal_internal.cuh"
@@ -34,7 +36,6 @@ static __device__ const PairTable c_pairs = make_pair_table();
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kTicketRows = 128;        // rows of a slice, many-sequence kernel
 constexpr int kClusterRows = 528;       // rows of a slice, cluster kernel (state rows / 8)
 constexpr int kMaxRho = 8;
 
@@ -50,6 +51,181 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {   // a *
 
 constexpr int kGroups = 4;             // row groups of a slice, each with its own bulk copy
 
+// k, u = [v; 1] and the query rows of every head sharing the KV head of
+// `unit`, as fp32 in shared memory.
+template <typename Tin>
+__device__ __forceinline__ void load_unit_vectors(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                                                  const Tin *__restrict__ v, int unit, int Hq,
+                                                  int Hkv, float *s_k, float *s_u,
+                                                  float (*s_q)[kD]) {
+  const int rho = Hq / Hkv, bidx = unit / Hkv, h0 = (unit % Hkv) * rho;
+  for (int n = threadIdx.x; n < kD; n += kThreads) s_k[n] = to_f32(k[(size_t)unit * kD + n]);
+  for (int n = threadIdx.x; n < kU; n += kThreads)
+    s_u[n] = n < kDv ? to_f32(v[(size_t)unit * kDv + n]) : 1.f;
+  for (int n = threadIdx.x; n < rho * kD; n += kThreads)
+    s_q[n / kD][n % kD] = to_f32(q[((size_t)bidx * Hq + h0) * kD + n]);
+}
+
+// Per-row weights, in two steps so the table loads can be issued early:
+// weight_fetch reads the row's kind, dims and every head's table entry;
+// weight_finish forms phi_f(k) into s_wk[n] and Phi~^h_f(q^h) into
+// s_wq[h * stride + n] from the head's k and q in shared memory.
+struct WeightRow {
+  int kind, r, t;            // kind 0: H0, 1: H1 (dim r), 2: H2 (dims r, t)
+  float coef[kMaxRho];
+};
+
+__device__ __forceinline__ WeightRow weight_fetch(const float *__restrict__ a,
+                                                  const float *__restrict__ b,
+                                                  const float *__restrict__ Ctab, int packed,
+                                                  int h0, int rho, int f) {
+  const size_t ctab_len = packed ? kH2Packed : kH2Full;
+  WeightRow w;
+  w.r = 0;
+  w.t = 0;
+  if (f == 0) w.kind = 0;
+  else if (f <= kD) { w.kind = 1; w.r = f - 1; }
+  else {
+    w.kind = 2;
+    const int nn = f - 1 - kD;
+    if (packed) { w.r = c_pairs.rt[nn] >> 8; w.t = c_pairs.rt[nn] & 0xff; }
+    else { w.r = nn >> 6; w.t = nn & 63; }
+  }
+#pragma unroll
+  for (int hh = 0; hh < kMaxRho; ++hh) {
+    w.coef[hh] = 0.f;
+    if (hh < rho) {
+      const int h = h0 + hh;
+      w.coef[hh] = w.kind == 0 ? __ldg(a + h)
+                 : (w.kind == 1 ? __ldg(b + (size_t)h * kD + w.r)
+                                : __ldg(Ctab + (size_t)h * ctab_len + (f - 1 - kD)));
+    }
+  }
+  return w;
+}
+
+__device__ __forceinline__ void weight_finish(const WeightRow &w, int rho, int n, const float *s_k,
+                                              const float (*s_q)[kD], float *s_wk, float *s_wq,
+                                              int stride) {
+  s_wk[n] = w.kind == 0 ? 1.f : (w.kind == 1 ? s_k[w.r] : s_k[w.r] * s_k[w.t]);
+#pragma unroll
+  for (int hh = 0; hh < kMaxRho; ++hh) {
+    if (hh < rho) {
+      float x;
+      if (w.kind == 0) x = w.coef[hh];
+      else if (w.kind == 1) x = w.coef[hh] * s_q[hh][w.r] * 0.125f;
+      else x = w.coef[hh] * s_q[hh][w.r] * s_q[hh][w.t] * 0.015625f;
+      s_wq[hh * stride + n] = x;
+    }
+  }
+}
+
+// Rows nrows .. nrows rounded up to 4 get zero weights (the readout reads
+// weights four rows at a time).
+__device__ __forceinline__ void weight_pad(int n, float *s_wk, float *s_wq, int stride) {
+  s_wk[n] = 0.f;
+#pragma unroll
+  for (int hh = 0; hh < kMaxRho; ++hh) s_wq[hh * stride + n] = 0.f;
+}
+
+// Per-row weights of rows f0 .. f0 + nrows - 1 (and the padding rows).
+__device__ __forceinline__ void slice_weights(const float *__restrict__ a,
+                                              const float *__restrict__ b,
+                                              const float *__restrict__ Ctab, int packed, int h0,
+                                              int rho, int f0, int nrows, const float *s_k,
+                                              const float (*s_q)[kD], float *s_wk, float *s_wq,
+                                              int stride) {
+  for (int n = threadIdx.x; n < ((nrows + 3) & ~3); n += kThreads) {
+    if (n >= nrows) {
+      weight_pad(n, s_wk, s_wq, stride);
+      continue;
+    }
+    const WeightRow w = weight_fetch(a, b, Ctab, packed, h0, rho, f0 + n);
+    weight_finish(w, rho, n, s_k, s_q, s_wk, s_wq, stride);
+  }
+}
+
+// Value columns of rows r0 .. r1 - 1 (r0 a multiple of 4): each warp takes 4
+// consecutive rows per step (lane l owns columns l and l + 32), writes the
+// updated rows and accumulates the readout of every head with packed fp32
+// FMAs.  s_rows[i] holds float i of the slice, S the slice in the state.
+__device__ __forceinline__ void rows_step(const float *s_rows, float *S, int r0, int r1, int rho,
+                                          const float *s_u, const float *s_wk, const float *s_wq,
+                                          int stride, float2 (&acc)[kMaxRho]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float2 u01 = make_float2(s_u[lane], s_u[lane + 32]);
+  for (int rb = r0 + 4 * warp; rb < r1; rb += 4 * kWarps) {
+    const float4 wk4 = *reinterpret_cast<const float4 *>(&s_wk[rb]);
+    const float wk[4] = {wk4.x, wk4.y, wk4.z, wk4.w};
+    float2 nv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int rr = rb + u;
+      nv[u] = make_float2(0.f, 0.f);
+      if (rr < r1) {
+        const float *src = s_rows + rr * kU;
+        nv[u] = make_float2(fmaf(wk[u], u01.x, src[lane]), fmaf(wk[u], u01.y, src[lane + 32]));
+        float *dst = S + (size_t)rr * kU;
+        __stcs(dst + lane, nv[u].x);
+        __stcs(dst + lane + 32, nv[u].y);
+      }
+    }
+#pragma unroll
+    for (int hh = 0; hh < kMaxRho; ++hh) {
+      if (hh < rho) {
+        const float4 wq = *reinterpret_cast<const float4 *>(&s_wq[hh * stride + rb]);
+        acc[hh] = ffma2(make_float2(wq.x, wq.x), nv[0], acc[hh]);
+        acc[hh] = ffma2(make_float2(wq.y, wq.y), nv[1], acc[hh]);
+        acc[hh] = ffma2(make_float2(wq.z, wq.z), nv[2], acc[hh]);
+        acc[hh] = ffma2(make_float2(wq.w, wq.w), nv[3], acc[hh]);
+      }
+    }
+  }
+}
+
+// Column 64 (the normaliser, one row per thread), then the block's readout
+// partial of every head in a fixed order: into s_out (accumulate: added to
+// it).  s_red is a free buffer of kWarps * kMaxRho * kU floats; the block
+// passes a barrier at the end.
+__device__ __forceinline__ void slice_reduce(const float *s_rows, float *S, int nrows, int rho,
+                                             const float *s_wk, const float *s_wq, int stride,
+                                             const float2 (&acc)[kMaxRho], float *s_red_buf,
+                                             float (*s_out)[kU], bool accumulate) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float den[kMaxRho];
+#pragma unroll
+  for (int hh = 0; hh < kMaxRho; ++hh) den[hh] = 0.f;
+  for (int rr = tid; rr < nrows; rr += kThreads) {
+    const float n2 = s_rows[rr * kU + kDv] + s_wk[rr];   // u_64 = 1
+    __stcs(S + (size_t)rr * kU + kDv, n2);
+#pragma unroll
+    for (int hh = 0; hh < kMaxRho; ++hh)
+      if (hh < rho) den[hh] = fmaf(s_wq[hh * stride + rr], n2, den[hh]);
+  }
+#pragma unroll
+  for (int hh = 0; hh < kMaxRho; ++hh)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den[hh] += __shfl_xor_sync(0xffffffffu, den[hh], o);
+  __syncthreads();   // the slice buffer is reused for the block reduction
+  float(*s_red)[kMaxRho][kU] = reinterpret_cast<float(*)[kMaxRho][kU]>(s_red_buf);
+#pragma unroll
+  for (int hh = 0; hh < kMaxRho; ++hh) {
+    if (hh < rho) {
+      s_red[warp][hh][lane] = acc[hh].x;
+      s_red[warp][hh][lane + 32] = acc[hh].y;
+      if (lane == 0) s_red[warp][hh][64] = den[hh];
+    }
+  }
+  __syncthreads();
+  for (int n = tid; n < rho * kU; n += kThreads) {
+    const int hh = n / kU, c = n % kU;
+    float sum = 0.f;
+    for (int w = 0; w < kWarps; ++w) sum += s_red[w][hh][c];
+    s_out[hh][c] = accumulate ? s_out[hh][c] + sum : sum;
+  }
+  __syncthreads();
+}
+
 // One slice of rows of one (batch, KV head): state update in place and this
 // block's partial readout of every head in s_part (rho x 65, fixed order).
 template <typename Tin, int kRows>
@@ -64,11 +240,10 @@ __device__ __forceinline__ void decode_slice(const Tin *__restrict__ q, const Ti
   pdl_trigger();
   pdl_wait();
   const int rho = Hq / Hkv;
-  const int bidx = unit / Hkv, kv = unit % Hkv;
-  const int h0 = kv * rho;
+  const int h0 = (unit % Hkv) * rho;
   const int f0 = slice * rows_per_block;
   const int nrows = min(rows_per_block, F - f0);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
 
   extern __shared__ __align__(16) float s_buf[];   // decode_smem_floats(rows_per_block)
   __shared__ float s_k[kD];
@@ -110,134 +285,22 @@ __device__ __forceinline__ void decode_slice(const Tin *__restrict__ q, const Ti
   if (tid < head) s_rows[tid] = __ldcs(S + tid);
   if (tid >= 32 && tid < 32 + tail) s_rows[nel - tail + tid - 32] = __ldcs(S + nel - tail + tid - 32);
 
-  for (int n = tid; n < kD; n += kThreads) s_k[n] = to_f32(k[(size_t)unit * kD + n]);
-  for (int n = tid; n < kU; n += kThreads)
-    s_u[n] = n < kDv ? to_f32(v[(size_t)unit * kDv + n]) : 1.f;
-  for (int n = tid; n < rho * kD; n += kThreads)
-    s_q[n / kD][n % kD] = to_f32(q[((size_t)bidx * Hq + h0) * kD + n]);
+  load_unit_vectors(q, k, v, unit, Hq, Hkv, s_k, s_u, s_q);
   __syncthreads();
+  slice_weights(a, b, Ctab, packed, h0, rho, f0, nrows, s_k, s_q, s_wk, &s_wq[0][0], kRows);
+  __syncthreads();   // (also publishes the head and tail floats)
 
-  // per-row weights: phi_f(k) and Phi~^h_f(q^h); the table loads of all
-  // heads are issued before any is used
-  const size_t ctab_len = packed ? kH2Packed : kH2Full;
-  // (rows nrows .. nrows rounded up to 4 get zero weights: the readout reads
-  // weights four rows at a time)
-  for (int n = tid; n < ((nrows + 3) & ~3); n += kThreads) {
-    if (n >= nrows) {
-      s_wk[n] = 0.f;
-#pragma unroll
-      for (int hh = 0; hh < kMaxRho; ++hh) s_wq[hh][n] = 0.f;
-      continue;
-    }
-    const int f = f0 + n;
-    int r = 0, t = 0, kind;
-    if (f == 0) kind = 0;
-    else if (f <= kD) { kind = 1; r = f - 1; }
-    else {
-      kind = 2;
-      const int nn = f - 1 - kD;
-      if (packed) { r = c_pairs.rt[nn] >> 8; t = c_pairs.rt[nn] & 0xff; }
-      else { r = nn >> 6; t = nn & 63; }
-    }
-    s_wk[n] = kind == 0 ? 1.f : (kind == 1 ? s_k[r] : s_k[r] * s_k[t]);
-    float coef[kMaxRho];
-#pragma unroll
-    for (int hh = 0; hh < kMaxRho; ++hh) {
-      coef[hh] = 0.f;
-      if (hh < rho) {
-        const int h = h0 + hh;
-        coef[hh] = kind == 0 ? __ldg(a + h)
-                 : (kind == 1 ? __ldg(b + (size_t)h * kD + r)
-                              : __ldg(Ctab + (size_t)h * ctab_len + (f - 1 - kD)));
-      }
-    }
-#pragma unroll
-    for (int hh = 0; hh < kMaxRho; ++hh) {
-      if (hh < rho) {
-        float w;
-        if (kind == 0) w = coef[hh];
-        else if (kind == 1) w = coef[hh] * s_q[hh][r] * 0.125f;
-        else w = coef[hh] * s_q[hh][r] * s_q[hh][t] * 0.015625f;
-        s_wq[hh][n] = w;
-      }
-    }
-  }
-  __syncthreads();
-
-  // Value columns: each warp takes 4 consecutive rows per step (lane l owns
-  // columns l and l + 32) and accumulates the readout of every head with
-  // packed fp32 FMAs.  Column 64 (the normaliser) follows, one row per thread.
   float2 acc[kMaxRho];
 #pragma unroll
   for (int hh = 0; hh < kMaxRho; ++hh) acc[hh] = make_float2(0.f, 0.f);
-  const float2 u01 = make_float2(s_u[lane], s_u[lane + 32]);
-  // (the __syncthreads above also publishes the head and tail floats)
   for (int g = 0; g < kGroups; ++g) {
     if (!oal::tc::mbar_wait(&s_bar[g], 0, &s_abort, status)) break;
-    const int r1 = min(nrows, (g + 1) * rows_per_group);
-    for (int rb = g * rows_per_group + 4 * warp; rb < r1; rb += 4 * kWarps) {
-      const float4 wk4 = *reinterpret_cast<const float4 *>(&s_wk[rb]);
-      const float wk[4] = {wk4.x, wk4.y, wk4.z, wk4.w};
-      float2 nv[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int rr = rb + u;
-        nv[u] = make_float2(0.f, 0.f);
-        if (rr < r1) {
-          const float *src = s_rows + rr * kU;
-          nv[u] = make_float2(fmaf(wk[u], u01.x, src[lane]), fmaf(wk[u], u01.y, src[lane + 32]));
-          float *dst = S + (size_t)rr * kU;
-          __stcs(dst + lane, nv[u].x);
-          __stcs(dst + lane + 32, nv[u].y);
-        }
-      }
-#pragma unroll
-      for (int hh = 0; hh < kMaxRho; ++hh) {
-        if (hh < rho) {
-          const float4 wq = *reinterpret_cast<const float4 *>(&s_wq[hh][rb]);
-          acc[hh] = ffma2(make_float2(wq.x, wq.x), nv[0], acc[hh]);
-          acc[hh] = ffma2(make_float2(wq.y, wq.y), nv[1], acc[hh]);
-          acc[hh] = ffma2(make_float2(wq.z, wq.z), nv[2], acc[hh]);
-          acc[hh] = ffma2(make_float2(wq.w, wq.w), nv[3], acc[hh]);
-        }
-      }
-    }
+    rows_step(s_rows, S, g * rows_per_group, min(nrows, (g + 1) * rows_per_group), rho, s_u, s_wk,
+              &s_wq[0][0], kRows, acc);
   }
   // every copy has landed (or timed out) before the buffer is read again
   for (int g = 0; g < kGroups; ++g) oal::tc::mbar_wait_teardown(&s_bar[g], 0, status);
-  float den[kMaxRho];
-#pragma unroll
-  for (int hh = 0; hh < kMaxRho; ++hh) den[hh] = 0.f;
-  for (int rr = tid; rr < nrows; rr += kThreads) {
-    const float n2 = s_rows[rr * kU + kDv] + s_wk[rr];   // u_64 = 1
-    __stcs(S + (size_t)rr * kU + kDv, n2);
-#pragma unroll
-    for (int hh = 0; hh < kMaxRho; ++hh)
-      if (hh < rho) den[hh] = fmaf(s_wq[hh][rr], n2, den[hh]);
-  }
-#pragma unroll
-  for (int hh = 0; hh < kMaxRho; ++hh)
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den[hh] += __shfl_xor_sync(0xffffffffu, den[hh], o);
-  __syncthreads();   // the slice buffer is reused for the block reduction
-  float(*s_red)[kMaxRho][kU] = reinterpret_cast<float(*)[kMaxRho][kU]>(s_buf);
-
-  // block reduction (fixed order) -> this block's partial readout
-#pragma unroll
-  for (int hh = 0; hh < kMaxRho; ++hh) {
-    if (hh < rho) {
-      s_red[warp][hh][lane] = acc[hh].x;
-      s_red[warp][hh][lane + 32] = acc[hh].y;
-      if (lane == 0) s_red[warp][hh][64] = den[hh];
-    }
-  }
-  __syncthreads();
-  for (int n = tid; n < rho * kU; n += kThreads) {
-    const int hh = n / kU, c = n % kU;
-    float sum = 0.f;
-    for (int w = 0; w < kWarps; ++w) sum += s_red[w][hh][c];
-    s_part[hh][c] = sum;
-  }
+  slice_reduce(s_rows, S, nrows, rho, s_wk, &s_wq[0][0], kRows, acc, s_buf, s_part, false);
 }
 
 template <typename Tin>
@@ -275,56 +338,154 @@ decode_cluster_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
   cluster.sync();   // no block leaves while the first one reads its partial
 }
 
+// ---------------------------------------------------------------- many sequences
+// Persistent blocks, each walking a contiguous run of (batch x KV head, slice)
+// items with the next slice's bulk copy in flight while the current one is
+// updated (two slice buffers), so the memory system always has loads queued.
+// A block sums the partial readouts of the items of one (batch, KV head) in
+// shared memory and writes one partial per (block, batch x KV head) it
+// touched (at most two: a run is never longer than a head's slices);
+// decode_finish_kernel adds them in block order and divides.
+constexpr int kStreamRows = 192;                  // rows of a slice (one per thread at most)
+constexpr int kStreamBuf = kStreamRows * kU + 8;  // floats of one slice buffer (16-byte multiple)
+constexpr int kStreamBlocksPerSM = 2;
+static_assert(kStreamRows <= kThreads && kStreamRows % 4 == 0, "one weight row per thread");
+
+struct SliceGeom {
+  float *S;          // first float of the slice in the state
+  int nrows, nel;    // rows, floats
+  int head, tail;    // floats before the first / after the last 16-byte boundary
+  int f0;            // first row
+};
+
+__device__ __forceinline__ SliceGeom slice_geom(float *state, int F, int rows_per_slice, int unit,
+                                                int slice) {
+  SliceGeom g;
+  g.f0 = slice * rows_per_slice;
+  g.nrows = min(rows_per_slice, F - g.f0);
+  const size_t sf0 = ((size_t)unit * F + g.f0) * kU;
+  g.S = state + sf0;
+  g.nel = g.nrows * kU;
+  g.head = (int)((4 - (sf0 & 3)) & 3);
+  g.tail = (int)((sf0 + g.nel) & 3);
+  return g;
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads, kStreamBlocksPerSM)
+decode_stream_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                     const Tin *__restrict__ v, const float *__restrict__ a,
+                     const float *__restrict__ b, const float *__restrict__ Ctab,
+                     float *__restrict__ state, int Hq, int Hkv, int F, int packed, int nslices,
+                     int nitems, int per_block, float *__restrict__ partial, int *status) {
+  extern __shared__ __align__(16) float s_dyn[];   // two slice buffers
+  __shared__ float s_k[kD];
+  __shared__ float s_u[kU];
+  __shared__ float s_q[kMaxRho][kD];
+  __shared__ __align__(16) float s_wk[kStreamRows];
+  __shared__ __align__(16) float s_wq[kMaxRho][kStreamRows];
+  __shared__ float s_acc[kMaxRho][kU];
+  __shared__ __align__(8) uint64_t s_bar[2];
+  __shared__ int s_abort;
+  const int tid = threadIdx.x;
+  const int rho = Hq / Hkv;
+  const int i0 = blockIdx.x * per_block, i1 = min(nitems, i0 + per_block);
+  if (tid == 0) {
+    s_abort = 0;
+    oal::tc::mbar_init(&s_bar[0], 1);
+    oal::tc::mbar_init(&s_bar[1], 1);
+    oal::tc::fence_mbar_init();
+  }
+  pdl_trigger();
+  pdl_wait();   // the state rows the previous step wrote
+  // bulk copy of the aligned interior of item x into buffer bb
+  auto issue = [&](int x, int bb) {
+    const SliceGeom g = slice_geom(state, F, kStreamRows, x / nslices, x % nslices);
+    float *rows = s_dyn + bb * kStreamBuf + ((4 - g.head) & 3);
+    const int n = g.nel - g.head - g.tail;
+    oal::tc::mbar_arrive_expect_tx(&s_bar[bb], (uint32_t)n * 4u);
+    oal::tc::bulk_load(rows + g.head, g.S + g.head, (uint32_t)n * 4u, &s_bar[bb]);
+  };
+  if (tid == 0 && i0 < i1) issue(i0, 0);
+  // table entries of this thread's row of item x, loaded one item ahead
+  auto fetch = [&](int x) {
+    WeightRow w{};
+    const int f = (x % nslices) * kStreamRows + tid;
+    if (x < i1 && tid < kStreamRows && f < F)
+      w = weight_fetch(a, b, Ctab, packed, (x / nslices) % Hkv * rho, rho, f);
+    return w;
+  };
+  WeightRow wrow = fetch(i0);
+  int cur_unit = -1, slot = -1, fail_at = -1;
+  float *const pblk = partial + (size_t)blockIdx.x * 2 * kMaxRho * kU;
+  for (int it = i0; it < i1; ++it) {
+    const int j = it - i0, bb = j & 1;
+    const int unit = it / nslices, slice = it % nslices;
+    // buffer bb ^ 1 was released by the end of the previous item
+    if (tid == 0 && it + 1 < i1) issue(it + 1, bb ^ 1);
+    if (unit != cur_unit) {
+      if (cur_unit >= 0)
+        for (int n = tid; n < rho * kU; n += kThreads) pblk[slot * kMaxRho * kU + n] = s_acc[n / kU][n % kU];
+      __syncthreads();
+      ++slot;
+      cur_unit = unit;
+      for (int n = tid; n < rho * kU; n += kThreads) s_acc[n / kU][n % kU] = 0.f;
+      load_unit_vectors(q, k, v, unit, Hq, Hkv, s_k, s_u, s_q);
+      __syncthreads();
+    }
+    const SliceGeom g = slice_geom(state, F, kStreamRows, unit, slice);
+    float *s_rows = s_dyn + bb * kStreamBuf + ((4 - g.head) & 3);
+    if (tid < g.head) s_rows[tid] = __ldcs(g.S + tid);
+    if (tid >= 32 && tid < 32 + g.tail)
+      s_rows[g.nel - g.tail + tid - 32] = __ldcs(g.S + g.nel - g.tail + tid - 32);
+    if (tid < g.nrows) weight_finish(wrow, rho, tid, s_k, s_q, s_wk, &s_wq[0][0], kStreamRows);
+    else if (tid < ((g.nrows + 3) & ~3)) weight_pad(tid, s_wk, &s_wq[0][0], kStreamRows);
+    wrow = fetch(it + 1);   // in flight while this item is processed
+    __syncthreads();
+    const bool landed = oal::tc::mbar_wait(&s_bar[bb], (j >> 1) & 1, &s_abort, status);
+    if (__syncthreads_or(!landed)) { fail_at = it; break; }   // the same decision in every thread
+    float2 acc[kMaxRho];
+#pragma unroll
+    for (int hh = 0; hh < kMaxRho; ++hh) acc[hh] = make_float2(0.f, 0.f);
+    rows_step(s_rows, g.S, 0, g.nrows, rho, s_u, s_wk, &s_wq[0][0], kStreamRows, acc);
+    slice_reduce(s_rows, g.S, g.nrows, rho, s_wk, &s_wq[0][0], kStreamRows, acc,
+                 s_dyn + bb * kStreamBuf, s_acc, true);
+  }
+  if (cur_unit >= 0 && fail_at < 0)
+    for (int n = tid; n < rho * kU; n += kThreads) pblk[slot * kMaxRho * kU + n] = s_acc[n / kU][n % kU];
+  if (fail_at >= 0 && tid == 0) {
+    // the copies of the failed item and of the one after it must land before exit
+    const int j = fail_at - i0;
+    oal::tc::mbar_wait_teardown(&s_bar[j & 1], (j >> 1) & 1, status);
+    if (fail_at + 1 < i1) oal::tc::mbar_wait_teardown(&s_bar[(j + 1) & 1], ((j + 1) >> 1) & 1, status);
+  }
+}
+
+// y of every query head of (batch, KV head) blockIdx.x: the partials of the
+// blocks whose runs touched it, in block order, then u~[0:64] / u~[64].
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
-decode_ticket_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
-                     const Tin *__restrict__ v, Tin *__restrict__ y,
-                     const float *__restrict__ a, const float *__restrict__ b,
-                     const float *__restrict__ Ctab, float *__restrict__ state, int Hq, int Hkv,
-                     int F, int packed, int rows_per_block, int nslices,
-                     float *__restrict__ partial, unsigned *__restrict__ tickets, int *status) {
-  __shared__ float s_part[kMaxRho][kU];
-  __shared__ bool s_last;
-  const int unit = blockIdx.y, slice = blockIdx.x, bidx = unit / Hkv, kv = unit % Hkv;
-  const int rho = Hq / Hkv, h0 = kv * rho, tid = threadIdx.x;
-  decode_slice<Tin, kTicketRows>(q, k, v, a, b, Ctab, state, Hq, Hkv, F, packed, rows_per_block,
-                                 slice, unit, status, s_part);
-  float *part = partial + ((size_t)unit * nslices + slice) * kMaxRho * kU;
-  for (int n = tid; n < rho * kU; n += kThreads) part[(n / kU) * kU + n % kU] = s_part[n / kU][n % kU];
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned ticket = atomicAdd(&tickets[unit], 1u);
-    s_last = (ticket == (unsigned)nslices - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  // last block of this (batch, KV head): sum the slices in a fixed order, divide
+decode_finish_kernel(Tin *__restrict__ y, const float *__restrict__ partial, int Hq, int Hkv,
+                     int nslices, int per_block) {
+  pdl_trigger();
+  pdl_wait();
+  const int unit = blockIdx.x, bidx = unit / Hkv, kv = unit % Hkv, rho = Hq / Hkv;
+  const int first = unit * nslices, last = first + nslices - 1;
+  const int b0 = first / per_block, b1 = last / per_block;
   __shared__ float s_tot[kMaxRho][kU];
-  const float *pu = partial + (size_t)unit * nslices * kMaxRho * kU;
-  for (int n = tid; n < rho * kU; n += kThreads) {
-    const int hh = n / kU, c = n % kU;
-    float p16[16];   // sixteen interleaved sums: the loads are in flight together
-#pragma unroll
-    for (int j = 0; j < 16; ++j) p16[j] = 0.f;
-    for (int sl0 = 0; sl0 < nslices; sl0 += 16) {
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (sl0 + j < nslices) p16[j] += __ldcg(pu + (size_t)(sl0 + j) * kMaxRho * kU + hh * kU + c);
+  for (int n = threadIdx.x; n < rho * kU; n += kThreads) {
+    float sum = 0.f;
+    for (int blk = b0; blk <= b1; ++blk) {
+      const int slot = unit - (blk * per_block) / nslices;
+      sum += __ldcg(partial + ((size_t)blk * 2 + slot) * kMaxRho * kU + n);
     }
-#pragma unroll
-    for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-      for (int j = 0; j < w; ++j) p16[j] += p16[j + w];
-    s_tot[hh][c] = p16[0];
+    s_tot[n / kU][n % kU] = sum;
   }
   __syncthreads();
-  for (int n = tid; n < rho * kDv; n += kThreads) {
+  for (int n = threadIdx.x; n < rho * kDv; n += kThreads) {
     const int hh = n / kDv, c = n % kDv;
-    y[((size_t)bidx * Hq + h0 + hh) * kDv + c] = from_f32<Tin>(s_tot[hh][c] / s_tot[hh][kDv]);
+    y[((size_t)bidx * Hq + kv * rho + hh) * kDv + c] = from_f32<Tin>(s_tot[hh][c] / s_tot[hh][kDv]);
   }
-  if (tid == 0) tickets[unit] = 0u;   // ready for the next call
 }
 
 }  // namespace
@@ -340,14 +501,29 @@ static size_t decode_smem_floats(int rpb) {
 // head) all fit the GPU at once.
 static bool use_clusters(size_t units) { return units * 16 <= 2 * 152; }
 
-static int ticket_slices(int packed) { return (state_rows(packed) + kTicketRows - 1) / kTicketRows; }
+// Work split of the streaming kernel: items (batch x KV head, slice), runs of
+// per_block consecutive items, one run per block (a run never spans more than
+// two heads: per_block <= nslices).
+struct StreamPlan {
+  int nslices, nitems, per_block, nblocks;
+};
+static StreamPlan stream_plan(size_t units, int packed) {
+  StreamPlan p;
+  p.nslices = (state_rows(packed) + kStreamRows - 1) / kStreamRows;
+  p.nitems = (int)units * p.nslices;
+  const int target = 152 * kStreamBlocksPerSM;
+  p.per_block = (p.nitems + target - 1) / target;
+  if (p.per_block > p.nslices) p.per_block = p.nslices;
+  p.nblocks = (p.nitems + p.per_block - 1) / p.per_block;
+  return p;
+}
 
 size_t decode_workspace_bytes(int B, int Hkv, int packed) {
   const size_t units = (size_t)B * Hkv;
   if (use_clusters(units)) return 256;
-  const size_t part = units * ticket_slices(packed) * kMaxRho * kU * sizeof(float);
-  const size_t tick = units * sizeof(unsigned);
-  return ((part + 255) / 256) * 256 + ((tick + 255) / 256) * 256;
+  const StreamPlan p = stream_plan(units, packed);
+  const size_t part = (size_t)p.nblocks * 2 * kMaxRho * kU * sizeof(float);
+  return ((part + 255) / 256) * 256;
 }
 
 int decode_max_rho() { return kMaxRho; }
@@ -398,9 +574,9 @@ static oal_status launch_decode_t(const Tin *q, const Tin *k, const Tin *v, int 
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(decode_smem_floats(kClusterRows) * sizeof(float))) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(decode_ticket_kernel<Tin>,
+        cudaFuncSetAttribute(decode_stream_kernel<Tin>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(decode_smem_floats(kTicketRows) * sizeof(float))) != cudaSuccess)
+                             (int)(2 * kStreamBuf * sizeof(float))) != cudaSuccess)
       return oal_check_launch("decode: shared memory attribute");
     attr_set[dev] = true;
   }
@@ -425,17 +601,16 @@ static oal_status launch_decode_t(const Tin *q, const Tin *k, const Tin *v, int 
                        packed, rpb, oal_device_status_word());
     return oal_after_launch("decode_cluster_kernel", stream);
   }
-  const int nslices = ticket_slices(packed);
-  const size_t part_bytes = ((units * nslices * kMaxRho * kU * sizeof(float) + 255) / 256) * 256;
+  const StreamPlan p = stream_plan(units, packed);
   float *partial = (float *)ws;
-  unsigned *tickets = (unsigned *)((char *)ws + part_bytes);
-  if (cudaMemsetAsync(tickets, 0, units * sizeof(unsigned), stream) != cudaSuccess)
-    return oal_check_launch("decode ticket reset");
-  launch_pdl(decode_ticket_kernel<Tin>, dim3(nslices, (unsigned)units), dim3(kThreads),
-             decode_smem_floats(kTicketRows) * sizeof(float), stream, q, k, v, y, a, b, C, state,
-             Hq, Hkv, F, packed, (int)kTicketRows, nslices, partial, tickets,
-             oal_device_status_word());
-  return oal_after_launch("decode_ticket_kernel", stream);
+  launch_pdl(decode_stream_kernel<Tin>, dim3(p.nblocks), dim3(kThreads),
+             2 * kStreamBuf * sizeof(float), stream, q, k, v, a, b, C, state, Hq, Hkv, F, packed,
+             p.nslices, p.nitems, p.per_block, partial, oal_device_status_word());
+  oal_status st = oal_after_launch("decode_stream_kernel", stream);
+  if (st != OAL_OK) return st;
+  launch_pdl(decode_finish_kernel<Tin>, dim3((unsigned)units), dim3(kThreads), 0, stream, y,
+             (const float *)partial, Hq, Hkv, p.nslices, p.per_block);
+  return oal_after_launch("decode_finish_kernel", stream);
 }
 
 oal_status launch_decode(const void *q, const void *k, const void *v, int is_bf16,

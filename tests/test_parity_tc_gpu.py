@@ -9,7 +9,7 @@ without the rank-one form or with exception words at the first and last
 rows (the general and the patched builder paths), GQA ratios 1 to 8, a
 sequence split into many parts, continuation through the tensor-core path,
 chunk-boundary lengths, and both decode reductions (thread-block clusters
-for few sequences, a last-block ticket for many).
+for few sequences, persistent streaming blocks and a finishing kernel for many).
 """
 import numpy as np
 import pytest
@@ -153,9 +153,11 @@ def test_tc_prefill_continuation(oal, layout):
     assert rel_l2(S.cpu().numpy(), S_ref) <= TOL_S
 
 
-@pytest.mark.parametrize("B,Hq,Hkv", [(1, 16, 2), (2, 6, 3), (20, 4, 2)])
+@pytest.mark.parametrize("B,Hq,Hkv", [(1, 16, 2), (2, 6, 3), (20, 4, 2), (24, 16, 2)])
 def test_decode_reductions(oal, B, Hq, Hkv):
-    # B * Hkv <= 19: slices meet in a thread-block cluster; 40: ticket path
+    # B * Hkv <= 19: slices meet in a thread-block cluster; 40 and 48: the
+    # streaming kernel (runs of slices crossing (batch, KV head) boundaries,
+    # eight query heads per KV head in the last case) and its finishing kernel
     w = inputs.make_workload("dec-red", B=B, Hq=Hq, Hkv=Hkv, T=40 + 3, G=4, seed=360 + B,
                              decode_steps=3)
     Q, K, V = w.torch_inputs("cuda")
