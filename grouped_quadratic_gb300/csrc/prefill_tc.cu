@@ -22,22 +22,25 @@
 //
 // Launches per call:
 //   tc_prep_kernel      per query head: readout weights in the feature order
-//                       above (bf16) and the constants of the intra-chunk
-//                       kernel evaluation.
+//                       above (bf16) and their rank-one record, the
+//                       constants of the intra-chunk kernel evaluation; K^T
+//                       for the state kernel.
 //   tc_state_kernel     mode 0 (only when the sequence is split into parts):
 //                       per (feature tile, part): the part's total
 //                       Delta S = sum phi(k_j) u_j^T.
 //                       mode 1: per (feature tile, part): walk the part's
-//                       chunks with the fp32 state resident in tensor memory;
+//                       chunks with the fp32 running state in registers;
 //                       before each chunk write its bf16 snapshot S_{c-1};
 //                       the last part writes the final fp32 state.
-//   tc_readout_kernel   per (chunk, group of <= 4 query heads, batch x KV
-//                       head): inter-chunk readout Phi~(Q_c) S_{c-1} as a
-//                       128 x 80 x 2192 UMMA per head (A = Phi~ built by
-//                       threads straight into tensor memory, B = snapshot
-//                       streamed by TMA), intra-chunk kappa tile from
+//   tc_intra_kernel     per (query head, chunk): intra-chunk kappa tile from
 //                       s = Q_c K_c^T (UMMA) plus the tail-group sums (fp32
-//                       FMA), P.V by UMMA, then normalisation.
+//                       FMA), P.V by UMMA; numerators and denominators to
+//                       the workspace.
+//   tc_readout_kernel   per (query head, chunk, batch x KV head): inter-chunk
+//                       readout Phi~(Q_c) S_{c-1} as a 128 x 80 x 2192 UMMA
+//                       (A = Phi~ built by threads straight into tensor
+//                       memory, B = snapshot streamed by TMA), plus the
+//                       intra-chunk rows, then normalisation.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -57,7 +60,7 @@ constexpr int kH2P = 2112;       // paired H2 features
 constexpr int kNKB = 35;         // readout K blocks of 64 (the last one has K = 16)
 constexpr int kTiles = 18;       // 128-feature tiles of the state kernel
 constexpr int kN = 80;           // UMMA N of [v | 1]: 64 value columns, the "1" column, 15 zeros
-constexpr int kMaxNH = 4;        // query heads per readout block
+constexpr int kMaxNH = 1;        // query heads per readout block (three blocks per SM)
 constexpr int kIntraNH = 1;      // query heads per intra-chunk block
 constexpr int kMaxTailG = 6;     // tail groups (G - 1 <= 6)
 // Snapshot rows: the 64 value columns and the "1" column; the readout's TMA box
@@ -859,8 +862,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
 }
 
 // ================================================================= readout kernel
-constexpr int kNB = 6;           // snapshot K-block stages
-constexpr int kNA = 12;          // A half slots (128 x 32 bf16, 16 columns) in tensor memory
+constexpr int kNB = 3;           // snapshot K-block stages
+constexpr int kNA = 3;           // A half slots (128 x 32 bf16, 16 columns) in tensor memory
 constexpr int kTailSlots = 2 * kMaxTailG;
 
 struct __align__(1024) ReadSmem {
@@ -872,7 +875,7 @@ struct __align__(1024) ReadSmem {
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(ReadSmem) + 1024 <= 227 * 1024, "readout shared memory");
+static_assert(3 * (sizeof(ReadSmem) + 2048) <= 228 * 1024, "three readout blocks per SM");
 
 struct __align__(1024) IntraSmem {
   __nv_bfloat16 q[kIntraNH][kC * 64];
@@ -896,10 +899,10 @@ struct ReadArgs {
   int *status;
 };
 
-constexpr int kReadThreads = 640;   // 20 warps
+constexpr int kReadThreads = 160;   // 5 warps
 constexpr int kTmemD = 0;         // D^h at [80h, 80h + 80)
-constexpr int kTmemA = 320;       // twelve A half slots of 16 columns at [320, 512)
-constexpr uint32_t kReadTmemCols = 512;
+constexpr int kTmemA = 80;        // three A half slots of 16 columns at [80, 128)
+constexpr uint32_t kReadTmemCols = 128;
 constexpr int kIntraThreads = 192;  // 6 warps
 constexpr int kTmemS = 0;         // intra kernel: two 32-key s / P sub-tiles at 0 and 32
 constexpr int kTmemI = 64;        // intra kernel: numerators at [64, 128)
@@ -1367,16 +1370,16 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 }
 
 // ---------------------------------------------------------------- readout kernel
-// Warp roles (20 warps):
-//   0-15   readout A builders: group h = warp / 4 builds every K block of the
-//          block's query head h (its Q row stays in registers), then runs the
-//          epilogue of head h
-//   16, 17 readout UMMA issuers (jobs of even / odd index)
-//   18     tensor memory owner
-//   19     TMA producer
-// Job j = 35-block index kb * nh + head; the accumulators are zeroed first and
-// every UMMA accumulates, so the two issuers need no ordering between them.
-__global__ void __launch_bounds__(kReadThreads, 1)
+// One block per (query head, chunk, batch x KV head), three blocks per SM
+// (128 tensor-memory columns, ~70 KB of shared memory each): the 448 blocks
+// of a 14-head, 4096-token prefill fill one wave with ~3 heads per SM, and
+// blocks that run independently keep the tensor pipe fed from whichever
+// block has a K block ready.  Warp roles (5 warps):
+//   0-3  A builders (one token row per thread): setup (transposed and scaled
+//        Q tile), every K block of Phi~(Q_c), then the epilogue
+//   4    UMMA issuer (warp-uniform loop, elected lane), tensor memory owner,
+//        TMA producer of the snapshot K blocks (3 stages)
+__global__ void __launch_bounds__(kReadThreads, 3)
 tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS,
                   ReadArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -1386,7 +1389,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   const int bidx = unit / args.Hkv, kv = unit % args.Hkv;
   const int h0 = kv * args.rho + hg * args.nh_per_block;
   const int nh = min(args.nh_per_block, args.rho - hg * args.nh_per_block);
-  constexpr int kIss0 = 16;   // issuer of head h: warp 16 + h (head 0's also runs the TMA)
+  constexpr int kIss0 = 4;
   pdl_trigger();
 
   if (tid == 0) {
@@ -1439,9 +1442,9 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     const int hh = warp - kIss0;
     if (hh < nh) {
       // ---------------- UMMA issuer of head hh: D^h = sum over K blocks of A_kb B_kb.
-      // One warp per head runs the loop (warp-uniform; an elected lane issues),
-      // so four heads' MMAs are issued in parallel.  Head 0's warp also loads
-      // the snapshot K blocks (6 stages) by TMA.
+      // The whole warp runs the loop (warp-uniform; an elected lane issues:
+      // an issuing loop under a one-lane branch is several times slower).
+      // Head 0's warp also loads the snapshot K blocks (kNB stages) by TMA.
       const uint32_t id80 = idesc_bf16_f32(128, kN, 0);
       const uint64_t bdesc0 = sdesc_sw128(smem_u32(s.b[0]), 16, 1024);
       constexpr uint64_t kStageStep = (kN * 64 * 2) >> 4;   // one snapshot stage
@@ -1516,7 +1519,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       }
     }
     __syncwarp();
-  } else if (warp < 16) {
+  } else if (warp < 4) {
     // ---------------- readout A builders: group hh builds head hh; thread = token row
     const int m = 32 * (warp & 3) + lane;
     const int hh = warp >> 2;
@@ -1789,6 +1792,7 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
     cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
     cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)rsmem);
+    cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     for (int g = 1; g <= kMaxG; ++g)
       cudaFuncSetAttribute(intra_kernel_for(g), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)ismem);
