@@ -871,9 +871,10 @@ struct __align__(1024) ReadSmem {
   __nv_bfloat16 qs[kMaxNH][kC * 64];   // bf16(alpha_dim q) [dim][token]
   __nv_bfloat16 b[kNB][kN * 64];       // snapshot K blocks [n][64 features]
   __nv_bfloat16 coef[kMaxNH][kCoefRow];
-  uint64_t qkv_full, b_full[kNB], b_empty[kNB], a_full[kNA], a_empty[kNA], d_full;
+  uint64_t qkv_full, b_full[kNB], a_full[kNA], a_empty[kNA], d_full;
   uint32_t tmem_base;
   int abort_flag;
+  int loaded;                          // snapshot K blocks whose load was issued
 };
 static_assert(3 * (sizeof(ReadSmem) + 2048) <= 228 * 1024, "three readout blocks per SM");
 
@@ -1376,9 +1377,11 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 // blocks that run independently keep the tensor pipe fed from whichever
 // block has a K block ready.  Warp roles (5 warps):
 //   0-3  A builders (one token row per thread): setup (transposed and scaled
-//        Q tile), every K block of Phi~(Q_c), then the epilogue
+//        Q tile), every K block of Phi~(Q_c), then the epilogue; warp 0 also
+//        refills the snapshot stages (3) by TMA as soon as the wait for an A
+//        slot shows that the MMAs reading a stage are complete
 //   4    UMMA issuer (warp-uniform loop, elected lane), tensor memory owner,
-//        TMA producer of the snapshot K blocks (3 stages)
+//        loads the first snapshot K blocks
 __global__ void __launch_bounds__(kReadThreads, 3)
 tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS,
                   ReadArgs args) {
@@ -1395,11 +1398,9 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   if (tid == 0) {
     s.abort_flag = 0;
     mbar_init(&s.qkv_full, 1);
-    for (int i = 0; i < kNB; ++i) {
-      mbar_init(&s.b_full[i], 1);
-      mbar_init(&s.b_empty[i], nh);     // one commit per head's issuer
-    }
+    for (int i = 0; i < kNB; ++i) mbar_init(&s.b_full[i], 1);
     for (int i = 0; i < kNA; ++i) { mbar_init(&s.a_full[i], 4); mbar_init(&s.a_empty[i], 1); }
+    s.loaded = min(kNB, kNKB);          // the issuer loads the first kNB K blocks
 
     mbar_init(&s.d_full, nh);           // every head's issuer done
     fence_mbar_init();
@@ -1437,6 +1438,12 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   tc_fence_after();
   const uint32_t tb = s.tmem_base;
   volatile int *abort_flag = &s.abort_flag;
+  // snapshot K block kb2 into its stage (one thread)
+  auto load_block = [&](int kb2) {
+    const int st2 = kb2 % kNB;
+    mbar_arrive_expect_tx(&s.b_full[st2], kN * 64 * 2);
+    tma_load_3d(s.b[st2], &tmS, &s.b_full[st2], 64 * kb2, 0, unit * args.nC + c);
+  };
 
   if (warp >= kIss0) {
     const int hh = warp - kIss0;
@@ -1444,22 +1451,15 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       // ---------------- UMMA issuer of head hh: D^h = sum over K blocks of A_kb B_kb.
       // The whole warp runs the loop (warp-uniform; an elected lane issues:
       // an issuing loop under a one-lane branch is several times slower).
-      // Head 0's warp also loads the snapshot K blocks (kNB stages) by TMA.
+      // Head 0's warp also loads the first kNB snapshot K blocks by TMA.
       const uint32_t id80 = idesc_bf16_f32(128, kN, 0);
       const uint64_t bdesc0 = sdesc_sw128(smem_u32(s.b[0]), 16, 1024);
       constexpr uint64_t kStageStep = (kN * 64 * 2) >> 4;   // one snapshot stage
       const uint32_t dt = tb + kTmemD + 80 * hh;
       const bool tma = hh == 0;
-      int loaded = 0;                            // K blocks whose load was issued
-      auto load_block = [&](int kb2) {
-        if (lane == 0) {
-          const int st2 = kb2 % kNB;
-          mbar_arrive_expect_tx(&s.b_full[st2], kN * 64 * 2);
-          tma_load_3d(s.b[st2], &tmS, &s.b_full[st2], 64 * kb2, 0, unit * args.nC + c);
-        }
-      };
-      if (tma)
-        for (; loaded < kNB && loaded < kNKB; ++loaded) load_block(loaded);
+      // the first kNB K blocks; the builders load the rest as stages free up
+      if (tma && lane == 0)
+        for (int kb2 = 0; kb2 < kNB && kb2 < kNKB; ++kb2) load_block(kb2);
       // this head owns half slots [hh * nhs, (hh + 1) * nhs), used in turn
       const int nhs = kNA / nh > 6 ? 6 : kNA / nh;
       const int a0 = hh * nhs;
@@ -1467,23 +1467,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       int st = 0, sph = 0;                       // snapshot stage and its phase
       int hs = 0;                                // first half slot of K block kb: (2 kb) % nhs
       int fk = 0, fph = 0;                       // kb % fper and the phase of (kb / fper)
-      bool ok = true;
-      for (int kb = 0; kb < kNKB && ok; ++kb) {
-        if (tma) {
-          // refill stages freed by every head (K block `loaded` reuses the
-          // stage of loaded - kNB); blocking only for the block needed now
-          while (loaded < kNKB) {
-            const int st2 = loaded % kNB, ph2 = ((loaded / kNB) & 1) ^ 1;
-            if (loaded > kb) {
-              if (!mbar_test(&s.b_empty[st2], ph2)) break;
-            } else if (!mbar_wait(&s.b_empty[st2], ph2, abort_flag, args.status)) {
-              ok = false;
-              break;
-            }
-            load_block(loaded++);
-          }
-          if (!ok) break;
-        }
+      for (int kb = 0; kb < kNKB; ++kb) {
         if (!mbar_wait(&s.b_full[st], sph, abort_flag, args.status)) break;
         const uint64_t bd = bdesc0 + kStageStep * st;
         // K block kb: halves of K = 32 in half slots (2 kb) % nhs and
@@ -1504,19 +1488,13 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           umma_ts_warp(dt, at0, bd, id80, 1u);
           umma_commit_warp(&s.a_empty[a0 + hs]);
         }
-        umma_commit_warp(&s.b_empty[st]);
         hs = hs1 + 1 == nhs ? 0 : hs1 + 1;
         if (++fk == fper) { fk = 0; fph ^= 1; }
         if (++st == kNB) { st = 0; sph ^= 1; }
       }
       umma_commit_warp(&s.d_full);
       mbar_wait_teardown(&s.d_full, 0, args.status);   // no MMA in flight at exit
-      if (tma) {
-        // copies still in flight must land before the block exits
-        mbar_wait_teardown(&s.qkv_full, 0, args.status);
-        for (int kb = max(0, loaded - kNB); kb < loaded; ++kb)
-          mbar_wait_teardown(&s.b_full[kb % kNB], (kb / kNB) & 1, args.status);
-      }
+      if (tma) mbar_wait_teardown(&s.qkv_full, 0, args.status);   // no copy in flight at exit
     }
     __syncwarp();
   } else if (warp < 4) {
@@ -1594,6 +1572,15 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const uint32_t par0 = ((uph >> hs) & 1u) ^ 1u, par1 = ((uph >> hs1) & 1u) ^ 1u;
         uint64_t *e0 = &s.a_empty[a0 + hs], *e1 = &s.a_empty[a0 + hs1];
         if (!mbar_test(e0, par0) && !mbar_wait(e0, par0, abort_flag, args.status)) break;
+        // the half slot's previous use was half 2 kb - nhs, of K block j: its
+        // MMAs are complete, so j's snapshot stage takes K block j + kNB
+        if (warp == 0 && 2 * kb >= nhs) {
+          const int nxt = ((2 * kb - nhs) >> 1) + kNB;
+          if (nxt < kNKB && lane == 0) {
+            load_block(nxt);
+            s.loaded = nxt + 1;
+          }
+        }
         const uint32_t ta0 = tmem_lane_addr(tb, warp, kTmemA + 16 * (a0 + hs));
         const uint32_t ta1 = tmem_lane_addr(tb, warp, kTmemA + 16 * (a0 + hs1));
         tmem_st16(ta0, out0);
@@ -1615,20 +1602,19 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       }
     }
     if (hh < nh) {
-      // ---------------- epilogue of head hh: y = (u~ + intra)[0:64] / (u~ + intra)[64],
-      // 16 columns at a time; the intra-chunk rows of the next 16 columns are
-      // loaded while the current ones are finished
+      // ---------------- epilogue of head hh: y = (u~ + intra)[0:64] / (u~ + intra)[64].
+      // The row's intra-chunk numerators and denominator are loaded at once
+      // (one memory latency, overlapping the last MMAs), then the
+      // accumulator is read 16 columns at a time
       const int i_tok = c * kC + m;
       const bool row_ok = i_tok < args.T;
       const size_t row = ((size_t)bidx * args.Hq + h0 + hh) * args.T + i_tok;
       const float4 *src = reinterpret_cast<const float4 *>(args.intra_num + row * 64);
-      float4 cur[4], nxt[4];
+      float4 nv[16];
       float iden = 0.f;
-      if (row_ok) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) cur[e] = __ldg(src + e);
-        iden = __ldg(args.intra_den + row);
-      }
+      for (int e = 0; e < 16; ++e) nv[e] = row_ok ? __ldg(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (row_ok) iden = __ldg(args.intra_den + row);
       if (!*abort_flag && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
         tc_fence_after();
         uint32_t r[16];
@@ -1638,16 +1624,12 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         uint4 *dst = reinterpret_cast<uint4 *>(args.Y + row * kDv);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          if (q4 < 3 && row_ok) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) nxt[e] = __ldg(src + 4 * (q4 + 1) + e);
-          }
           tmem_ld16(tmem_lane_addr(tb, warp, kTmemD + 80 * hh + 16 * q4), r);
           tmem_wait_ld();
           uint32_t pk[8];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float4 n4 = cur[e];
+            const float4 n4 = nv[4 * q4 + e];
             pk[2 * e] = pack_bf16x2((__uint_as_float(r[4 * e]) + n4.x) * inv,
                                     (__uint_as_float(r[4 * e + 1]) + n4.y) * inv);
             pk[2 * e + 1] = pack_bf16x2((__uint_as_float(r[4 * e + 2]) + n4.z) * inv,
@@ -1657,8 +1639,6 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             dst[2 * q4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             dst[2 * q4 + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) cur[e] = nxt[e];
         }
       }
     }
@@ -1666,6 +1646,12 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   tc_fence_before();
   __syncthreads();
   if (warp == kIss0) {
+    // snapshot copies still in flight (a block that gave up early) land
+    // before the block exits
+    if (lane == 0)
+      for (int kb = max(0, s.loaded - kNB); kb < s.loaded; ++kb)
+        mbar_wait_teardown(&s.b_full[kb % kNB], (kb / kNB) & 1, args.status);
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tb, kReadTmemCols);
   }
