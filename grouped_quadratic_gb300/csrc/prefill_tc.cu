@@ -182,7 +182,10 @@ struct KtArgs {
   int T, Tpad, U, nC;
 };
 
-__global__ void __launch_bounds__(256)
+constexpr int kPrepThreads = 256;
+static_assert(kPrepThreads == 256, "the K^T tiles and the coefficient rows assume 256 threads");
+
+__global__ void __launch_bounds__(kPrepThreads)
 tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
                const float *__restrict__ Ctab, const float *__restrict__ L,
                const int32_t *__restrict__ group, int G, float eps, int packed,
@@ -324,24 +327,33 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
     for (int w = tid; w < kH2Words; w += blockDim.x)
       sexc[w] = (feat_exc(2 * w) || feat_exc(2 * w + 1)) ? 1 : 0;
     __syncthreads();
-    if (tid < 32) {
-      // ascending list: lane l scans words [33 l, 33 l + 33)
-      constexpr int kPer = kH2Words / 32;
+    {
+      // ascending list, every thread: thread t scans words [kPer t, kPer t + kPer)
+      constexpr int kPer = (kH2Words + kPrepThreads - 1) / kPrepThreads;
+      __shared__ int swarp[kPrepThreads / 32];
+      const int w0 = kPer * tid, lane = tid & 31;
       int cnt = 0;
-      for (int i = 0; i < kPer; ++i) cnt += sexc[kPer * tid + i];
+      for (int i = 0; i < kPer; ++i) cnt += (w0 + i < kH2Words) ? sexc[w0 + i] : 0;
       int pre = cnt;
   #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, pre, o);
-        if (tid >= o) pre += v;
+        if (lane >= o) pre += v;
       }
-      int pos = pre - cnt;
+      if (lane == 31) swarp[tid >> 5] = pre;
+      __syncthreads();
+      int base = 0, total = 0;
+      for (int i = 0; i < kPrepThreads / 32; ++i) {
+        base += i < (tid >> 5) ? swarp[i] : 0;
+        total += swarp[i];
+      }
+      int pos = base + pre - cnt;
       for (int i = 0; i < kPer; ++i)
-        if (sexc[kPer * tid + i]) {
-          if (pos < kExcMax) slist[pos] = (uint16_t)(kPer * tid + i);
+        if (w0 + i < kH2Words && sexc[w0 + i]) {
+          if (pos < kExcMax) slist[pos] = (uint16_t)(w0 + i);
           ++pos;
         }
-      if (tid == 31) snexc = pre;
+      if (tid == 0) snexc = total;
     }
     __syncthreads();
     const int nexc = snexc;
@@ -378,22 +390,37 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
   }
   auto Lat = [&](int g, int c) { return c <= g ? sL[g * G1 + c] : 0.f; };
   KPlan *P = plans + h;
-  if (tid >= 1 && tid <= G && tid != gstar) {
-    const int g = tid;
-    const int slot = g < gstar ? g - 1 : g - 2;
+  // first dims of each tail group, one thread per dim: its rank in its group
+  // from the groups' ballots over the 64 dims
+  __shared__ uint32_t sball[2][kMaxG + 1];
+  auto tail_off = [&](int g) {   // dims of the tail groups before g
     int off = 0;
     for (int gg = 1; gg < g; ++gg)
       if (gg != gstar) off += scnt[gg];
-    P->goff[slot] = off;
-    int k = 0;
-    P->dims[slot][0] = P->dims[slot][1] = 0;
-    for (int r = 0; r < kD; ++r) {
-      if (sgrp[r] != g) continue;
-      if (k < 2) P->dims[slot][k] = r;
-      P->gdims[off + k] = r;
-      ++k;
+    return off;
+  };
+  if (tid < kD) {
+    for (int gg = 1; gg <= G; ++gg) {
+      const uint32_t m = __ballot_sync(0xffffffffu, sgrp[tid] == gg);
+      if ((tid & 31) == 0) sball[tid >> 5][gg] = m;
     }
-    P->nd[slot] = k;
+  }
+  __syncthreads();
+  if (tid < kD && sgrp[tid] != gstar) {
+    const int r = tid, g = sgrp[r];
+    const int slot = g < gstar ? g - 1 : g - 2;
+    const int k = (r < 32 ? 0 : __popc(sball[0][g])) +
+                  __popc(sball[r >> 5][g] & ((1u << (r & 31)) - 1u));
+    P->gdims[tail_off(g) + k] = r;
+    if (k < 2) P->dims[slot][k] = r;
+  }
+  if (tid >= 1 && tid <= G && tid != gstar) {
+    const int g = tid;
+    const int slot = g < gstar ? g - 1 : g - 2;
+    P->goff[slot] = tail_off(g);
+    P->nd[slot] = scnt[g];
+    if (scnt[g] < 2) P->dims[slot][1] = 0;
+    if (scnt[g] < 1) P->dims[slot][0] = 0;
     for (int c = 0; c < 8; ++c) P->beta[slot][c] = c <= G ? (Lat(g, c) - Lat(gstar, c)) * 0.125f : 0.f;
   }
   if (tid == 0) {
@@ -419,7 +446,7 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
   // sbar_{g_i} = z_i / 8; M = L L^T.  A[g][v] has at most two non-zero
   // rows per column, so every entry is a sum of at most four terms of M.
   __shared__ int slot_group[8];     // tail slot -> group
-  __shared__ double sM[8][8];       // M = L L^T in fp64, one entry per thread
+  __shared__ float sM[8][8];        // M = L L^T, one entry per thread
   if (tid == 0) {
     int slot = 0;
     for (int g = 1; g <= G; ++g)
@@ -427,16 +454,16 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
   }
   if (tid < G1 * G1) {
     const int g = tid / G1, h2 = tid % G1;
-    double m = 0.0;
-    for (int c = 0; c <= (g < h2 ? g : h2); ++c) m += (double)Lat(g, c) * (double)Lat(h2, c);
+    float m = 0.f;
+    for (int c = 0; c <= (g < h2 ? g : h2); ++c) m = fmaf(Lat(g, c), Lat(h2, c), m);
     sM[g][h2] = m;
   }
   __syncthreads();
   // the (at most two) groups g with d sbar_g / d z_v != 0, and those values
-  auto deps = [&](int v, int (&gs)[2], double (&as)[2]) -> int {
-    if (v == 0) { gs[0] = gstar; as[0] = 0.125; return 1; }
-    gs[0] = gstar; as[0] = -0.125;
-    gs[1] = slot_group[v]; as[1] = 0.125;
+  auto deps = [&](int v, int (&gs)[2], float (&as)[2]) -> int {
+    if (v == 0) { gs[0] = gstar; as[0] = 0.125f; return 1; }
+    gs[0] = gstar; as[0] = -0.125f;
+    gs[1] = slot_group[v]; as[1] = 0.125f;
     return 2;
   };
   const int nq = G * (G + 1) / 2;
@@ -445,26 +472,26 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
     while (rem >= G - v) { rem -= G - v; ++v; }
     const int w2 = v + rem;
     int gv[2], gw[2];
-    double av[2], aw[2];
+    float av[2], aw[2];
     const int nv = deps(v, gv, av), nw = deps(w2, gw, aw);
-    double q = 0.0;
+    float q = 0.f;   // the coefficients are +-1/8: the products are exact
     for (int i = 0; i < nv; ++i)
       for (int j = 0; j < nw; ++j) q += av[i] * sM[gv[i]][gw[j]] * aw[j];
-    P->quad[tid] = (float)(w2 == v ? q : 2.0 * q);
+    P->quad[tid] = w2 == v ? q : 2.f * q;
   } else if (tid < 36) {
     P->quad[tid] = 0.f;
   } else if (tid >= 64 && tid < 72) {
     const int v = tid - 64;
-    double l = 0.0;
+    float l = 0.f;
     if (v < G) {
       int gv[2];
-      double av[2];
+      float av[2];
       const int nv = deps(v, gv, av);
-      for (int i = 0; i < nv; ++i) l += 2.0 * sM[0][gv[i]] * av[i];
+      for (int i = 0; i < nv; ++i) l += 2.f * sM[0][gv[i]] * av[i];
     }
-    P->lin[v] = (float)l;
+    P->lin[v] = l;
   } else if (tid == 96) {
-    P->c0 = (float)((double)eps + sM[0][0]);
+    P->c0 = eps + sM[0][0];
   }
 }
 
@@ -1763,7 +1790,7 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   kta.T = T; kta.Tpad = Tpad; kta.U = lay.U; kta.nC = lay.nC;
   const int ntiles = lay.U * lay.nC;
   const int ntr = (std::min(ntiles, 2 * 152) + Hq - 1) / Hq;   // block rows of transposes
-  launch_pdl(tc_prep_kernel, dim3(Hq, (kKP + 255) / 256 + 2 + ntr), dim3(256), 0, stream, a, b, C,
+  launch_pdl(tc_prep_kernel, dim3(Hq, (kKP + 255) / 256 + 2 + ntr), dim3(kPrepThreads), 0, stream, a, b, C,
              L, group, G, eps, packed, coef, plans, status, kta);
   oal_status st = oal_after_launch("tc_prep_kernel", stream);
   if (st != OAL_OK) return st;
