@@ -23,6 +23,9 @@ Quadratic Kernels", arXiv:2610.13674):
   packed == full readout     App. D "Exact state and parameter counts".
   continuation               the state after T1 tokens resumes to the same
                              outputs as one pass over T1 + T2 tokens.
+  empty groups               App. B (groups partition the dims) with L lower-
+                             triangular: empty groups give the kernel of the
+                             truncated L, whatever their rows of L hold.
 """
 import json
 import os
@@ -146,6 +149,24 @@ def test_global_embedding_invariant_to_partition(G):
         group = rng.integers(1, G + 1, size=(2, 12)).astype(np.int32)
         y = oracle.direct(Q, K, V, L, group, eps)
         np.testing.assert_allclose(y, want, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("gh", [1, 2, 3])
+def test_empty_groups_equal_fewer_groups(gh):
+    # App. B: the groups partition the dims.  A group with no dims has group
+    # sum 0, and L is lower-triangular, so the kernel of a head whose groups
+    # above gh are empty is the one of the leading (gh + 1) x (gh + 1) block
+    # of L with gh groups: heads of different group counts share one G.
+    Q, K, V, L, group = small_case(60 + gh, B=2, Hq=2, Hkv=1, T=30, d=10, dv=4, G=4)
+    group[group > gh] = 1
+    eps = 1e-3
+    y = oracle.direct(Q, K, V, L, group, eps)
+    y_trunc = oracle.direct(Q, K, V, np.ascontiguousarray(L[:, :gh + 1, :gh + 1]), group, eps)
+    np.testing.assert_allclose(y, y_trunc, rtol=1e-12, atol=1e-13)
+    # and the L entries of the empty groups do not matter
+    L2 = L.copy()
+    L2[:, gh + 1:, :] = 7.0 * np.tril(np.ones_like(L2[:, gh + 1:, :]), gh + 1)
+    np.testing.assert_allclose(oracle.direct(Q, K, V, L2, group, eps), y, rtol=1e-12, atol=1e-13)
 
 
 def test_kappa_at_least_eps():

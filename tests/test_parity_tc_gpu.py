@@ -8,7 +8,8 @@ tail group wider than two dims (the generic kappa path), readout weights
 without the rank-one form or with exception words at the first and last
 rows (the general and the patched builder paths), GQA ratios 1 to 8, a
 sequence split into many parts, continuation through the tensor-core path,
-chunk-boundary lengths, and both decode reductions (thread-block clusters
+chunk-boundary lengths, heads of different group counts in one launch
+(empty groups), and both decode reductions (thread-block clusters
 for few sequences, persistent streaming blocks and a finishing kernel for many).
 """
 import numpy as np
@@ -102,6 +103,18 @@ def test_tc_prefill_readout_exception_words(oal):
                              fixed_outliers=([0, 31, 32, 63], 14.0),
                              fixed_groups=[[0, 31], [32, 62], [63, 1]])
     check_prefill(oal, w)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_prefill_heterogeneous_group_counts(oal, dtype):
+    # heads of 1 to 5 groups in one launch: G = 5 for all, head h keeps
+    # groups 1 .. 1 + h % 5 and leaves the others empty (their dims join the
+    # bulk group 1); bf16 runs the tensor-core path, f32 the CUDA-core one
+    w = inputs.make_workload("het", B=1, Hq=10, Hkv=2, T=300, G=5, dtype=dtype, seed=330)
+    for h in range(w.Hq):
+        w.group[h][w.group[h] > 1 + h % 5] = 1
+    check_prefill(oal, w)
+    check_prefill(oal, w, FULL)
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (6, 3), (8, 2), (16, 2)])
