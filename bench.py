@@ -446,6 +446,7 @@ def run_ours(args, world, rank, local):
                "ms_per_step": 1e3 * e2e_s / args.steps}
 
     decode = None if args.no_decode else run_decode(args, world, dev, stream, lib, pks)
+    calib = run_contribution(args, world, dev, stream, lib, pks) if args.contribution else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -458,9 +459,54 @@ def run_ours(args, world, rank, local):
             "config": workload_config(w, args), "roofline": roofline, "cpu_baseline": cpu,
             "e2e": e2e, "gpu_launches": int(launches), "clocks": clk.summary(),
             "decode": decode, "peaks_source": pks["source"]}
+    if calib is not None:
+        line["calibration"] = calib
     line["config"]["launch"] = "one step captured as a CUDA graph, replayed per timed step"
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_contribution(args, world, dev, stream, lib, pks):
+    """Contribution scores (the calibration step before the path) on 40
+    prompts of 4096 tokens, Qwen-shaped heads: one pass over Q and K."""
+    import torch
+    from grouped_quadratic_gb300 import oal
+    P, Hq, Hkv, T = 40, 14, 2, 4096
+    g = torch.Generator(device="cpu").manual_seed(20261005)
+    Q = torch.randn(P, Hq, T, D, generator=g).to(torch.bfloat16).to(dev)
+    K = torch.randn(P, Hkv, T, D, generator=g).to(torch.bfloat16).to(dev)
+    chi = torch.empty(P, Hq, D, dtype=torch.float32, device=dev)
+    ws = torch.empty(oal.oal_contribution_workspace_bytes(P, Hq, Hkv, T), dtype=torch.uint8,
+                     device=dev)
+
+    def call():
+        oal.oal_contribution_scores(Q, K, chi=chi, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        call()
+    oal.oal_sync_status()
+    n = 20
+    c0 = lib.oal_launch_counter()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = lib.oal_launch_counter() - c0
+    oal.oal_sync_status()
+    secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world) / n
+    nbytes = (Q.numel() + K.numel()) * 2 + chi.numel() * 4
+    gbs = nbytes / secs / 1e9
+    return {"workload": "contribution scores P%d Hq%d Hkv%d T%d d64 bf16 (inputs %.0f MB > L2)"
+                        % (P, Hq, Hkv, T, nbytes / 1e6),
+            "ms_per_call": 1e3 * secs,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pks["hbm_gbs"], "algorithmic_bytes_per_call": nbytes},
+            "gpu_launches": int(launches)}
 
 
 def run_decode(args, world, dev, stream, lib, pks):
@@ -537,6 +583,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--contribution", action="store_true",
+                    help="also time the contribution scores (calibration step)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     args = ap.parse_args()

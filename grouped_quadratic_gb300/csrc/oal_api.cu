@@ -1,8 +1,11 @@
 // oal_api.cu -- the extern "C" entry points of liboal.so (include/oal.h):
 // argument validation, workspace sizing, dispatch to the kernels, error
 // reporting.  No allocation happens here; all memory is the caller's.
+#include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
+
+#include <algorithm>
 
 #include "oal_internal.cuh"
 
@@ -27,6 +30,14 @@ int decode_max_rho();
 oal_status launch_decode(const void *q, const void *k, const void *v, int is_bf16, int B,
                          int Hq, int Hkv, const float *a, const float *b, const float *C,
                          int packed, float *state, void *y, void *ws, cudaStream_t stream);
+
+size_t contrib_workspace_bytes(int P, int Hq, int Hkv, int T);
+oal_status launch_contrib(const void *Q, const void *K, int is_bf16, int P, int Hq, int Hkv,
+                          int T, const int32_t *lengths, float *chi, void *ws,
+                          cudaStream_t stream);
+oal_status group_dims_host(const float *chi_p, int P, int d, const int32_t *boot_idx,
+                           int nboot, double alpha, double tau, double gamma, int g_min,
+                           double eps, int32_t *group, int *G);
 
 // Device status word (one per device the library runs on).
 __device__ int g_status_word;
@@ -290,6 +301,60 @@ oal_status oal_decode_step(const void *q, const void *k, const void *v, oal_dtyp
                             layout == OAL_STATE_PACKED, state, y, workspace, stream);
 }
 
+size_t oal_contribution_workspace_bytes(int P, int Hq, int Hkv, int T, int d) {
+  if (P < 0 || Hq <= 0 || Hkv <= 0 || T < 0 || d != oal::kD) return 0;
+  return std::max<size_t>(256, oal::contrib_workspace_bytes(P, Hq, Hkv, T));
+}
+
+oal_status oal_contribution_scores(const void *Q, const void *K, oal_dtype dtype, int P,
+                                   int Hq, int Hkv, int T, int d, const int32_t *lengths,
+                                   float *chi, void *workspace, size_t workspace_bytes,
+                                   cudaStream_t stream) {
+  t_msg[0] = 0;
+  OAL_TRY(check_common(P, Hq, Hkv, d, d, dtype, OAL_STATE_FULL));
+  if (T < 0) return oal_fail(OAL_ERR_INVALID_ARG, "bad T=%d", T);
+  if (P == 0) return OAL_OK;
+  OAL_TRY(check_ptr(chi, "chi"));
+  OAL_TRY(check_ptr(workspace, "workspace"));
+  if (T > 0) {
+    OAL_TRY(check_ptr(Q, "Q"));
+    OAL_TRY(check_ptr(K, "K"));
+  }
+  if (lengths) OAL_TRY(check_ptr(lengths, "lengths"));
+  if (((uintptr_t)workspace & 255u) != 0)
+    return oal_fail(OAL_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  const size_t need = oal_contribution_workspace_bytes(P, Hq, Hkv, T, d);
+  if (workspace_bytes < need)
+    return oal_fail(OAL_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes",
+                    workspace_bytes, need);
+  oal_begin_call(stream);
+  return oal::launch_contrib(Q, K, dtype == OAL_BF16, P, Hq, Hkv, T, lengths, chi, workspace,
+                             stream);
+}
+
+oal_status oal_group_dims(const float *chi_p, int P, int d, const int32_t *boot_idx, int nboot,
+                          double alpha, double tau, double gamma, int g_min, double eps,
+                          int32_t *group, int *G) {
+  t_msg[0] = 0;
+  if (!chi_p || !boot_idx || !group || !G)
+    return oal_fail(OAL_ERR_INVALID_ARG, "null pointer");
+  if (P < 1 || d < 2 || nboot < 1)
+    return oal_fail(OAL_ERR_INVALID_ARG, "bad sizes P=%d d=%d nboot=%d", P, d, nboot);
+  if (!(alpha > 0.0 && alpha <= 1.0) || !(eps > 0.0) || !(tau > 0.0) || !(gamma >= 0.0) ||
+      g_min < 1)
+    return oal_fail(OAL_ERR_INVALID_ARG, "bad parameters alpha=%g tau=%g gamma=%g g_min=%d "
+                    "eps=%g", alpha, tau, gamma, g_min, eps);
+  for (size_t i = 0; i < (size_t)nboot * P; ++i)
+    if (boot_idx[i] < 0 || boot_idx[i] >= P)
+      return oal_fail(OAL_ERR_INVALID_ARG, "bootstrap index %d outside 0..%d", boot_idx[i],
+                      P - 1);
+  for (size_t i = 0; i < (size_t)P * d; ++i)
+    if (!isfinite(chi_p[i]) || chi_p[i] < 0.f)
+      return oal_fail(OAL_ERR_INVALID_ARG, "score %zu is negative or not finite", i);
+  return oal::group_dims_host(chi_p, P, d, boot_idx, nboot, alpha, tau, gamma, g_min, eps,
+                              group, G);
+}
+
 oal_status oal_sync_status(cudaStream_t stream) {
   t_msg[0] = 0;
   cudaError_t e = cudaStreamSynchronize(stream);
@@ -303,7 +368,8 @@ oal_status oal_sync_status(cudaStream_t stream) {
   if (v != 0) {
     const int zero = 0;
     cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice);
-    const char *what = v == OAL_ERR_INVALID_ARG ? "a group id was outside 1..G"
+    const char *what = v == OAL_ERR_INVALID_ARG ? "a group id outside 1..G or a prompt "
+                                                  "length outside 0..T"
                        : v == OAL_ERR_TIMEOUT   ? "a device-side wait timed out"
                                                 : "device error";
     return oal_fail((oal_status)v, "device status %d: %s", v, what);

@@ -77,6 +77,12 @@ class Workload:
                      for a in (self.Q, self.K, self.V))
 
 
+def bootstrap_indices(nboot: int, P: int, seed: int) -> np.ndarray:
+    """[nboot, P] int32 prompt indices, each row drawn with replacement from
+    0..P-1 (the prompt-level bootstrap replicates of the grouping step)."""
+    return np.random.default_rng([seed, 7]).integers(0, P, size=(nboot, P)).astype(np.int32)
+
+
 def random_L(rng: np.random.Generator, G: int, offdiag_std=0.3, diag_std=0.3,
              diag_shift=0.5) -> np.ndarray:
     L = np.zeros((G + 1, G + 1), np.float32)

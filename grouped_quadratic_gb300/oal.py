@@ -65,6 +65,13 @@ def load_library(path: str = LIB_PATH):
     lib.oal_decode_step.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, ci,
                                     vp, vp, vp, sz, vp]
     lib.oal_decode_step.restype = ci
+    lib.oal_contribution_workspace_bytes.argtypes = [ci] * 5
+    lib.oal_contribution_workspace_bytes.restype = sz
+    lib.oal_contribution_scores.argtypes = [vp, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, sz, vp]
+    lib.oal_contribution_scores.restype = ci
+    cd = ctypes.c_double
+    lib.oal_group_dims.argtypes = [vp, ci, ci, vp, ci, cd, cd, cd, ci, cd, vp, vp]
+    lib.oal_group_dims.restype = ci
     lib.oal_sync_status.argtypes = [vp]
     lib.oal_sync_status.restype = ci
     lib.oal_last_error.argtypes = []
@@ -227,6 +234,48 @@ def oal_decode_step(q, k, v, a, b, C, state, layout=OAL_STATE_FULL, y=None,
                                _ptr(workspace), workspace.numel() * workspace.element_size(),
                                _stream(stream)))
     return y
+
+
+def oal_contribution_workspace_bytes(P, Hq, Hkv, T, d=64):
+    return int(load_library().oal_contribution_workspace_bytes(P, Hq, Hkv, T, d))
+
+
+def oal_contribution_scores(Q, K, lengths=None, chi=None, workspace=None, stream=None):
+    """Per-prompt contribution scores: Q [P,Hq,T,64], K [P,Hkv,T,64], lengths
+    [P] int32 (CUDA) or None for T tokens each.  Returns chi [P,Hq,64] float32."""
+    lib = load_library()
+    P, Hq, T, d = Q.shape
+    Hkv = K.shape[1]
+    if chi is None:
+        chi = torch.empty(P, Hq, d, dtype=torch.float32, device=Q.device)
+    if workspace is None:
+        need = lib.oal_contribution_workspace_bytes(P, Hq, Hkv, T, d)
+        workspace = torch.empty(max(int(need), 256), dtype=torch.uint8, device=Q.device)
+    _need_cuda(Q, K, lengths, chi, workspace)
+    _check(lib.oal_contribution_scores(_ptr(Q), _ptr(K), _dtype_code(Q), P, Hq, Hkv, T, d,
+                                       _ptr(lengths), _ptr(chi), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream)))
+    return chi
+
+
+def oal_group_dims(chi_p, boot_idx, alpha, tau, gamma, g_min, eps=1e-12):
+    """Dimension groups of one query head (host arrays, no GPU): chi_p [P, d]
+    per-prompt scores, boot_idx [nboot, P] bootstrap prompt indices.
+    Returns (group [d] int32 in 1..G, G)."""
+    import numpy as np
+    lib = load_library()
+    chi_p = np.ascontiguousarray(np.asarray(chi_p, dtype=np.float32))
+    boot_idx = np.ascontiguousarray(np.asarray(boot_idx, dtype=np.int32))
+    if chi_p.ndim != 2 or boot_idx.ndim != 2 or boot_idx.shape[1] != chi_p.shape[0]:
+        raise OALError(OAL_ERR_INVALID_ARG, "chi_p must be [P, d] and boot_idx [nboot, P]")
+    P, d = chi_p.shape
+    group = np.zeros(d, np.int32)
+    G = ctypes.c_int(0)
+    _check(lib.oal_group_dims(chi_p.ctypes.data, P, d, boot_idx.ctypes.data, boot_idx.shape[0],
+                              float(alpha), float(tau), float(gamma), int(g_min), float(eps),
+                              group.ctypes.data, ctypes.byref(G)))
+    return group, G.value
 
 
 def oal_sync_status(stream=None):

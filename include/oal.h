@@ -17,7 +17,8 @@
  *
  * Conventions shared by every entry point
  *  - All tensor pointers are DEVICE pointers owned by the caller, contiguous
- *    in the stated row-major layout, and 16-byte aligned.  The library keeps
+ *    in the stated row-major layout, and 16-byte aligned (oal_group_dims, a
+ *    host function, takes host pointers).  The library keeps
  *    no allocation between calls; scratch memory is passed in `workspace`.
  *  - Calls are asynchronous on `stream` (0 = legacy default stream).
  *    Argument errors are detected on the host and returned synchronously,
@@ -187,6 +188,61 @@ oal_status oal_decode_step(const void *q, const void *k, const void *v,
                            const float *C, oal_state_layout layout,
                            float *state, void *y, void *workspace,
                            size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Calibration, the step before the path ([OAL] Sec. 3.1 and App. B "Dimension
+ * grouping"): the groups of each query head follow from contribution scores.
+ *
+ * oal_contribution_scores -- [OAL] Eq. (2) for every prompt p of a batch:
+ *     chi[p][h][r] = 1/|Omega_p| * sum_{0 <= j <= i < N_p} |q_{p,i,r} k_{p,j,r}| / sqrt(d),
+ *     |Omega_p| = N_p (N_p + 1) / 2   (chi = 0 for N_p = 0),
+ * query head h paired with key/value head h / (Hq / Hkv).  The average over
+ * prompts (chi_r of Eq. (2)) and its bootstrap replicates belong to
+ * oal_group_dims.  Evaluated through prefix sums of |k| (the pair set is
+ * never formed); sums within a 128-token chunk in fp32, across chunks in fp64.
+ *  Q        [P][Hq][T][d], K [P][Hkv][T][d] (device), dtype as oal_prefill.
+ *  lengths  [P] int32 (device): N_p in 0..T; NULL = every prompt has T
+ *           tokens.  A length outside 0..T is clamped and recorded in the
+ *           device status word (OAL_ERR_INVALID_ARG at oal_sync_status).
+ *  chi      [P][Hq][d] fp32 output (device).
+ *  workspace  >= oal_contribution_workspace_bytes(P, Hq, Hkv, T, d) bytes,
+ *           256-byte aligned (device); 0 from the size query means
+ *           unsupported or invalid sizes.
+ * Supported: d == 64.  P == 0 launches nothing; T == 0 writes zeros.
+ */
+size_t oal_contribution_workspace_bytes(int P, int Hq, int Hkv, int T, int d);
+oal_status oal_contribution_scores(const void *Q, const void *K, oal_dtype dtype, int P,
+                                   int Hq, int Hkv, int T, int d, const int32_t *lengths,
+                                   float *chi, void *workspace, size_t workspace_bytes,
+                                   cudaStream_t stream);
+
+/*
+ * oal_group_dims -- the dimension grouping of [OAL] App. B, Eqs. (16)-(19),
+ * for one query head.  HOST function: every pointer is host memory, nothing
+ * runs on the GPU, and the call is synchronous.
+ *  chi_p     [P][d] fp32: this head's per-prompt scores (Eq. (2) before the
+ *            average), finite and >= 0.
+ *  boot_idx  [nboot][P] int32 in 0..P-1: the prompt indices of each
+ *            bootstrap replicate (resampled with replacement by the caller).
+ *  alpha     tail fraction: candidate cuts k in {max(1, d - ceil(alpha d)),
+ *            ..., d - 1}; 0 < alpha <= 1.
+ *  tau, gamma  gap threshold of Eq. (16) and minimum bootstrap support of
+ *            Eq. (18) for a natural cut; g_min >= 1 the minimum group count,
+ *            reached (as far as the candidates allow) by fallback cuts in
+ *            descending (support, gap) order, ties in candidate order.
+ *  eps       the small constant of Eqs. (16)-(17), > 0.
+ *  group     [d] int32 output: 1..G in increasing contribution.
+ *  G         output: the number of groups.  The pages set no upper bound;
+ *            the prefill supports G <= 7.
+ * Arithmetic in fp64; chi_r and every replicate's chi^(b) are sums in index
+ * order followed by one division, so results are reproducible bit for bit.
+ * Returns OAL_ERR_INVALID_ARG for null pointers, P < 1, d < 2, nboot < 1,
+ * an index outside 0..P-1, a negative or non-finite score, or a parameter
+ * outside its range.
+ */
+oal_status oal_group_dims(const float *chi_p, int P, int d, const int32_t *boot_idx, int nboot,
+                          double alpha, double tau, double gamma, int g_min, double eps,
+                          int32_t *group, int *G);
 
 /*
  * oal_sync_status -- synchronises `stream`, then returns and clears the

@@ -17,6 +17,10 @@ Linearization with Grouped Quadratic Kernels" (arXiv:2610.13674).
                      under the rounding rule stated in oal_oracle.c.
   full_to_packed_state() -- re-indexes an ordered-pair state into the packed
                      symmetric layout of App. D (indexing only, no arithmetic).
+  contribution_scores() -- the per-prompt contribution score of Sec. 3.1,
+                     Eq. (2), pair by pair over the causal pair set.
+  bootstrap_groups() -- the dimension grouping of App. B, Eqs. (16)-(19), for
+                     one query head, step by step in the appendix's order.
 
 Parity status of each function (what pins it) is listed in the test module
 ``tests/test_oracle_pins.py``.
@@ -170,3 +174,86 @@ def full_to_packed_state(S_full, d: int):
     head = S_full[..., : 1 + d, :]
     h2 = S_full[..., 1 + d + r * d + t, :]
     return np.concatenate([head, h2], axis=-2)
+
+
+def contribution_scores(Q, K, lengths=None):
+    """Eq. (2) for every prompt: chi[p, h, r] = 1/|Omega_p| * sum over the
+    causal pairs (i, j), j <= i < N_p, of |q_{p,i,r} k_{p,j,r} / sqrt(d)|,
+    with |Omega_p| = N_p (N_p + 1) / 2 (chi = 0 for an empty prompt).
+
+    Q [P,Hq,T,d], K [P,Hkv,T,d]; query head h pairs with KV head h // (Hq/Hkv)
+    (the model's GQA map, App. B).  lengths [P] (default: T for every prompt).
+    Pair by pair, in fp64: O(N^2 d) per head, for small cases.
+    """
+    Q, K = _f64(Q), _f64(K)
+    P, Hq, T, d = Q.shape
+    Hkv = K.shape[1]
+    rho = Hq // Hkv
+    if lengths is None:
+        lengths = [T] * P
+    chi = np.zeros((P, Hq, d), np.float64)
+    for p in range(P):
+        n = int(lengths[p])
+        if n == 0:
+            continue
+        omega = n * (n + 1) / 2.0
+        causal = np.tril(np.ones((n, n), dtype=bool))   # [i, j] with j <= i
+        for h in range(Hq):
+            q, k = Q[p, h, :n], K[p, h // rho, :n]
+            for r in range(d):
+                pair = np.abs(np.outer(q[:, r], k[:, r]) / np.sqrt(d))
+                chi[p, h, r] = pair[causal].sum() / omega
+    return chi
+
+
+def bootstrap_groups(chi_p, boot_idx, alpha, tau, gamma, g_min, eps=1e-12):
+    """App. B grouping of one query head.  Returns (group [d] int32 in 1..G, G).
+
+    chi_p [P, d] per-prompt scores (Eq. (2) before the average over prompts);
+    boot_idx [nboot, P] the prompt indices of each bootstrap replicate.
+    fp64 throughout; every average is a sum in index order, then one division.
+    """
+    chi_p = np.asarray(chi_p, dtype=np.float64)
+    boot_idx = np.asarray(boot_idx)
+    P, d = chi_p.shape
+    nboot = boot_idx.shape[0]
+
+    def average(rows):
+        acc = np.zeros(d, np.float64)
+        for t in rows:
+            acc = acc + chi_p[t]
+        return acc / len(rows)
+
+    chi = average(range(P))
+    # increasing contribution, stable: pi[0] is pi_1 of the appendix
+    pi = sorted(range(d), key=lambda r: chi[r])
+    m = int(np.ceil(alpha * d))
+    cands = list(range(max(1, d - m), d))          # k: L_k = pi[:k], U_k = pi[k:]
+    # Eq. (16): the adjacent gap across cut k
+    rho_gap = {k: chi[pi[k]] / max(chi[pi[k - 1]], eps) for k in cands}
+    # Eqs. (17)-(18): the bootstrap support of each cut, ordering pi kept fixed
+    hits = {k: 0 for k in cands}
+    for b in range(nboot):
+        chi_b = average(boot_idx[b])
+        for k in cands:
+            lo = max(chi_b[r] for r in pi[:k])
+            hi = min(chi_b[r] for r in pi[k:])
+            if hi / max(lo, eps) >= tau:
+                hits[k] += 1
+    support = {k: hits[k] / nboot for k in cands}
+    # natural cuts; then fallback cuts by descending (support, gap) until
+    # g_min groups (ties keep the candidate order)
+    cuts = [k for k in cands if rho_gap[k] >= tau and support[k] >= gamma]
+    if len(cuts) + 1 < g_min:
+        rest = [k for k in cands if k not in cuts]
+        rest = sorted(rest, key=lambda k: (-support[k], -rho_gap[k]))
+        for k in rest:
+            if len(cuts) + 1 >= g_min:
+                break
+            cuts.append(k)
+    bounds = [0] + sorted(cuts) + [d]
+    group = np.zeros(d, np.int32)
+    for g in range(1, len(bounds)):                # Eq. (19)
+        for r in pi[bounds[g - 1]:bounds[g]]:
+            group[r] = g
+    return group, len(bounds) - 1
