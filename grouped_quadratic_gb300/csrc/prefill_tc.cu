@@ -506,8 +506,6 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t x, uint32_t y) {
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
   return r;
 }
-__device__ __forceinline__ uint32_t bcast_lo(uint32_t x) { return __byte_perm(x, 0, 0x1010); }
-__device__ __forceinline__ uint32_t bcast_hi(uint32_t x) { return __byte_perm(x, 0, 0x3232); }
 __device__ __forceinline__ uint32_t tmem_lane_addr(uint32_t base, int warp, int col) {
   return base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)col;
 }
