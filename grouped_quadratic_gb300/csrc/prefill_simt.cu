@@ -329,13 +329,20 @@ static oal_status launch_simt(const Tin *Q, const Tin *K, const Tin *V, int B,
                               int chunk, float *ws, cudaStream_t stream) {
   const int F = state_rows(packed);
   const int nC = (T + chunk - 1) / chunk;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaFuncSetAttribute(chunk_delta_kernel<Tin>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)delta_smem());
-    cudaFuncSetAttribute(readout_kernel<Tin>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)readout_smem());
-    attr_done = true;
+  // shared-memory limits above 48 KB: a function attribute of each device
+  static bool attr_set[256] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256)
+    return oal_fail(OAL_ERR_CUDA, "prefill: no current device");
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(chunk_delta_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)delta_smem()) != cudaSuccess ||
+        cudaFuncSetAttribute(readout_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)readout_smem()) != cudaSuccess) {
+      cudaGetLastError();   // reported here, not by the next launch
+      return oal_fail(OAL_ERR_CUDA, "prefill: setting the shared memory limit failed");
+    }
+    attr_set[dev] = true;
   }
   dim3 g1((F + kTile - 1) / kTile, nC, B * Hkv);
   launch_pdl(chunk_delta_kernel<Tin>, g1, dim3(kThreads), delta_smem(), stream, K, V, T, chunk,

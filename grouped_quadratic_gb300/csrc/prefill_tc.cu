@@ -1796,18 +1796,27 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   const size_t ssmem = sizeof(StateSmem) + 1024;
   const size_t rsmem = sizeof(ReadSmem) + 1024;
   const size_t ismem = sizeof(IntraSmem) + 1024;
-  static int attr_dev = -1;
+  // shared-memory limits above 48 KB: a function attribute of each device
+  static bool attr_set[256] = {};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev != dev) {
-    cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
-    cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)rsmem);
-    cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    for (int g = 1; g <= kMaxG; ++g)
-      cudaFuncSetAttribute(intra_kernel_for(g), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)ismem);
-    attr_dev = dev;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256)
+    return oal_fail(OAL_ERR_CUDA, "prefill: no current device");
+  if (!attr_set[dev]) {
+    bool ok = cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)ssmem) == cudaSuccess &&
+              cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)rsmem) == cudaSuccess &&
+              cudaFuncSetAttribute(tc_readout_kernel,
+                                   cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   100) == cudaSuccess;
+    for (int g = 1; ok && g <= kMaxG; ++g)
+      ok = cudaFuncSetAttribute(intra_kernel_for(g), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)ismem) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();   // reported here, not by the next launch
+      return oal_fail(OAL_ERR_CUDA, "prefill: setting the shared memory limit failed");
+    }
+    attr_set[dev] = true;
   }
   StateArgs sa;
   sa.T = T; sa.nC = lay.nC; sa.U = lay.U; sa.cpp = lay.cpp; sa.nparts = lay.nparts;
