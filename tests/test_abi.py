@@ -71,12 +71,35 @@ def test_prefill_rejects_bad_arguments_on_host(lib, kw, status):
     assert lib.oal_last_error().decode() != ""
 
 
+def _contrib_raw(lib, **kw):
+    from grouped_quadratic_gb300 import oal
+    p = ctypes.c_void_p(4096)  # a fake, aligned address; never dereferenced
+    args = dict(Q=p, K=p, dtype=oal.OAL_BF16, P=2, Hq=4, Hkv=2, T=8, d=64, lengths=None,
+                chi=p, ws=p, ws_bytes=1 << 20, stream=None)
+    args.update(kw)
+    return lib.oal_contribution_scores(*args.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=32), 2), (dict(Hq=3), 1), (dict(Hkv=0), 1), (dict(dtype=5), 1), (dict(P=-1), 1),
+    (dict(T=-2), 1), (dict(chi=ctypes.c_void_p(0)), 1), (dict(Q=ctypes.c_void_p(4100)), 1),
+    (dict(lengths=ctypes.c_void_p(4098)), 1), (dict(ws=ctypes.c_void_p(4096 + 16)), 1),
+    (dict(ws_bytes=8), 1),
+])
+def test_contribution_scores_reject_bad_arguments_on_host(lib, kw, status):
+    assert _contrib_raw(lib, **kw) == status
+    assert lib.oal_last_error().decode() != ""
+
+
 def test_workspace_queries(lib):
     from grouped_quadratic_gb300 import oal
     n = oal.oal_prefill_workspace_bytes(1, 14, 2, 4096, layout=oal.OAL_STATE_PACKED)
     assert n > 0
     assert oal.oal_prefill_workspace_bytes(1, 14, 2, 4096, chunk=96) == 0
     assert oal.oal_decode_workspace_bytes(64, 14, 2) > 0
+    n = oal.oal_contribution_workspace_bytes(40, 14, 2, 4096)
+    assert n == 40 * 32 * 64 * 4 * (2 + 2 * 14)
+    assert oal.oal_contribution_workspace_bytes(40, 14, 2, 4096, d=32) == 0
 
 
 def test_missing_library_fails_loudly(tmp_path):
