@@ -21,6 +21,10 @@ Linearization with Grouped Quadratic Kernels" (arXiv:2610.13674).
                      Eq. (2), pair by pair over the causal pair set.
   bootstrap_groups() -- the dimension grouping of App. B, Eqs. (16)-(19), for
                      one query head, step by step in the appendix's order.
+  backward()      -- gradients of the causal output with respect to Q, K, V
+                     and L (the derivative of the definition above; the
+                     calibration of App. B, Eq. (20), and the LoRA adaptation
+                     of Sec. 5 differentiate through it), pair by pair.
 
 Parity status of each function (what pins it) is listed in the test module
 ``tests/test_oracle_pins.py``.
@@ -257,3 +261,52 @@ def bootstrap_groups(chi_p, boot_idx, alpha, tau, gamma, g_min, eps=1e-12):
         for r in pi[bounds[g - 1]:bounds[g]]:
             group[r] = g
     return group, len(bounds) - 1
+
+
+def backward(Q, K, V, L, group, eps, dY):
+    """Gradients of <dY, Y> for Y = direct(Q, K, V, L, group, eps).
+
+    Returns (dQ, dK, dV, dL) in fp64, shaped like Q, K, V, L; dL is zero
+    above the diagonal (the upper triangle of L is not a parameter).  With
+    y_i = N_i / D_i, N_i = sum_{j<=i} kappa_ij v_j, D_i = sum_{j<=i} kappa_ij:
+        d/d kappa_ij = dY_i . (v_j - y_i) / D_i =: g_ij,
+        dV_j = sum_{i>=j} kappa_ij dY_i / D_i,
+        kappa_ij = eps + s_bar^T M s_bar, M = L L^T:
+            d kappa / d s_g = 2 (M s_bar)_g,  d kappa / d M = s_bar s_bar^T,
+        s_g = sum_{r in G_g} q_ir k_jr / sqrt(d),
+        dL = (dM + dM^T) L restricted to the lower triangle.
+    Key/value gradients are summed over the query heads of a KV head.  Every
+    pair is formed explicitly: O(T^2 d) memory per head, for small cases.
+    """
+    Q, K, V, L, dY = _f64(Q), _f64(K), _f64(V), _f64(L), _f64(dY)
+    group = np.asarray(group)
+    B, Hq, T, d = Q.shape
+    Hkv = K.shape[1]
+    rho = Hq // Hkv
+    G = L.shape[1] - 1
+    sd = np.sqrt(d)
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    dL = np.zeros_like(L)
+    causal = np.tril(np.ones((T, T)))
+    for h in range(Hq):
+        kv = h // rho
+        Lh = np.tril(L[h])
+        M = Lh @ Lh.T
+        member = np.zeros((d, G + 1))                     # dim r -> its group column
+        member[np.arange(d), group[h]] = 1.0
+        for b in range(B):
+            q, k, v, dy = Q[b, h], K[b, kv], V[b, kv], dY[b, h]
+            x = q[:, None, :] * k[None, :, :] / sd        # [i, j, r]
+            sbar = x @ member                             # [i, j, g]
+            sbar[..., 0] = 1.0
+            kap = (eps + np.einsum("ija,ab,ijb->ij", sbar, M, sbar)) * causal
+            D = kap.sum(axis=1)
+            y = (kap @ v) / D[:, None]
+            g = (dy @ v.T - (dy * y).sum(axis=1)[:, None]) / D[:, None] * causal
+            dV[b, kv] += (kap / D[:, None]).T @ dy
+            dx = (2.0 * g[..., None] * (sbar @ M)) @ member.T   # d/dx_ijr = d/ds_{g(r)}
+            dQ[b, h] += (dx * k[None, :, :]).sum(axis=1) / sd
+            dK[b, kv] += (dx * q[:, None, :]).sum(axis=0) / sd
+            dM = np.einsum("ij,ija,ijb->ab", g, sbar, sbar)
+            dL[h] += np.tril((dM + dM.T) @ Lh)
+    return dQ, dK, dV, dL

@@ -26,6 +26,10 @@ Quadratic Kernels", arXiv:2610.13674):
   empty groups               App. B (groups partition the dims) with L lower-
                              triangular: empty groups give the kernel of the
                              truncated L, whatever their rows of L hold.
+  backward                   every gradient entry against central differences
+                             of the forward oracle (the C pair sum); the
+                             constant kernel's closed form (dQ = dK = 0, dV of
+                             a running mean, no gradient on L00).
 """
 import json
 import os
@@ -280,3 +284,51 @@ def test_named_workloads_shapes_and_structure():
     assert np.array_equal(inputs.round_to_bf16(w1.Q), w1.Q)
     for h in range(14):
         assert set(np.unique(w1.group[h])) == {1, 2, 3, 4}
+
+
+# ---------------------------------------------------------------- backward
+def _loss(Q, K, V, L, group, eps, dY):
+    return float((oracle.direct(Q, K, V, L, group, eps) * dY).sum())
+
+
+def test_backward_matches_central_differences():
+    # every gradient entry of a small GQA case against central differences of
+    # the forward oracle (an independent code path: the C pair sum)
+    Q, K, V, L, group = small_case(70, B=1, Hq=2, Hkv=1, T=6, d=5, dv=3, G=2)
+    eps = 1e-2
+    dY = np.random.default_rng(71).standard_normal((1, 2, 6, 3))
+    dQ, dK, dV, dL = oracle.backward(Q, K, V, L, group, eps, dY)
+    h = 1e-6
+    for name, X, dX in (("Q", Q, dQ), ("K", K, dK), ("V", V, dV), ("L", L, dL)):
+        for idx in np.ndindex(X.shape):
+            if name == "L" and idx[2] > idx[1]:
+                assert dX[idx] == 0.0          # the upper triangle is not a parameter
+                continue
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += h
+            Xm[idx] -= h
+            args = {"Q": Q, "K": K, "V": V, "L": L}
+            args[name] = Xp
+            fp = _loss(args["Q"], args["K"], args["V"], args["L"], group, eps, dY)
+            args[name] = Xm
+            fm = _loss(args["Q"], args["K"], args["V"], args["L"], group, eps, dY)
+            fd = (fp - fm) / (2 * h)
+            assert abs(fd - dX[idx]) <= 1e-6 * max(1.0, abs(fd)), (name, idx, fd, dX[idx])
+
+
+def test_backward_constant_kernel():
+    # L = diag(L00, 0, ...): kappa is the constant eps + L00^2, y_i is the
+    # causal running mean of v, so dQ = dK = 0 and dV_j = sum_{i >= j} dY_i / (i + 1)
+    Q, K, V, _, group = small_case(72, B=2, Hq=4, Hkv=2, T=9, d=6, dv=4, G=3)
+    L = np.zeros((4, 4, 4))
+    L[:, 0, 0] = 0.7
+    dY = np.random.default_rng(73).standard_normal((2, 4, 9, 4))
+    dQ, dK, dV, dL = oracle.backward(Q, K, V, L, group, 1e-3, dY)
+    assert not dQ.any() and not dK.any()
+    want = np.zeros_like(V)
+    for i in range(9):
+        for h in range(4):
+            want[:, h // 2, : i + 1] += dY[:, h, i][:, None, :] / (i + 1)
+    np.testing.assert_allclose(dV, want, rtol=1e-12, atol=1e-13)
+    # L00 only moves the constant, which the normalisation cancels
+    np.testing.assert_allclose(dL[:, 0, 0], 0.0, atol=1e-12)
