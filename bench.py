@@ -2,15 +2,15 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Step (default workload, Qwen2.5-0.5B-shaped prefill: B=1, Hq=14, Hkv=2,
-d=64, T=4096, G=4, bf16 inputs, packed fp32 states): coefficient expansion,
-chunked causal prefill of 4096 tokens, then one decode token continuing from
-the prefill state -- every step of the method in one pass.  Inputs are
-resident in HBM; L2 is flushed (256 MiB write) before every timed step and
-each step is timed with CUDA events on the launching stream.  The timed
-steps replay the step captured once as a CUDA graph (the host's per-call
-Python and tensor-map setup is then off the device timeline); the e2e leg
-calls the API directly every step.
+Step (default workload, Llama-3.2-1B-shaped prefill: B=4, Hq=32, Hkv=8, d=64,
+T=8192, G=6, bf16 inputs, packed fp32 states): coefficient expansion, chunked
+causal prefill of 8192 tokens per sequence, then one decode token for every
+sequence continuing from the prefill state -- every step of the method in one
+pass.  Inputs are resident in HBM; L2 is flushed (256 MiB write) before every
+timed step and each step is timed with CUDA events on the launching stream.
+The timed steps replay the step captured once as a CUDA graph (the host's
+per-call Python and tensor-map setup is then off the device timeline); the
+e2e leg calls the API directly every step.
 
 The JSON line also carries:
   roofline      the dominant kernel (the contraction with the largest device
@@ -19,10 +19,15 @@ The JSON line also carries:
                 against the measured peak in MEASURED_PEAKS.json;
   e2e           the same step through the C ABI with host buffers: pinned
                 host->device copies of the inputs and device->host copies of
-                the outputs inside the timed region;
-  decode        the decode workload (B=64, Hq=14, Hkv=2, full fp32 state of
-                4161 x 65 per KV head, 1024 steps after a 2048-token prefill):
-                steps/s and achieved HBM bandwidth;
+                the outputs inside the timed region, pipelined per sequence
+                on two copy streams beside the compute stream;
+  config1       the Qwen2.5-0.5B-shaped prefill (B=1, Hq=14, Hkv=2, T=4096,
+                G=4) measured the same way;
+  config4       the long-context prefill (B=1, Hq=14, Hkv=2, T=65536, G=4) at
+                chunk sizes 64, 128 and 256;
+  decode        the decode workload (B=64, Hq=14, Hkv=2, 1024 steps after a
+                2048-token prefill): steps/s and achieved HBM bandwidth for the
+                full fp32 state (4161 x 65 per KV head) and the packed one;
   cpu_baseline  the fp64 CPU oracle timed on a bounded sample of the same
                 workload on this host's cores (rank 0, N = 1 only);
   clocks        SM clocks and throttle reasons sampled during the timed region.
@@ -35,6 +40,7 @@ tokens of all ranks / max over ranks of the timed region.
 the pages publish no code) on bounded samples of the same workload.
 """
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -54,16 +60,27 @@ F_PACKED = 1 + D + D * (D + 1) // 2      # 2145
 F_FULL = 1 + D + D * D                   # 4161
 U = D + 1
 FP32_SIMT_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # CUDA-core fp32 FMA at 2070 MHz
+CSRC = os.path.join(ROOT, "grouped_quadratic_gb300", "csrc")
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
-# the dominant kernel, from one ncu capture of the kernel as it is now; valid
-# only for the workload captured, and to be reset to None when the kernel
-# changes.  Summaries: profiles/tc_readout_kernel_qwen05b_T4096.md and
-# profiles/decode_stream_kernel_qwen05b_B64.md.
-READOUT_TRAFFIC = {"kernel": "tc_readout_kernel", "workload": (1, 14, 2, 4096, "packed"),
-                   "bytes": 40_656_128 + 17_920}
-DECODE_TRAFFIC = {"kernel": "decode_stream_kernel", "workload": (64, 14, 2, "full"),
-                  "bytes": 138_900_000 + 82_100_000}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a
+# kernel from one ncu capture, with the SHA-256 of the kernel's source file at
+# the time of the capture.  A record is reported only while that source file
+# is unchanged (otherwise the traffic is null: the counters are stale).
+TRAFFIC = [
+    # (kernel, source file, workload key, bytes per launch, source sha256)
+]
+
+
+def _sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def traffic_for(kernel, key):
+    for k, src, wkey, nbytes, sha in TRAFFIC:
+        if k == kernel and wkey == key and _sha(os.path.join(CSRC, src)) == sha:
+            return nbytes
+    return None
 
 
 def peaks():
@@ -122,7 +139,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.gpu_id)],
+                 "-lms", "100", "-i", str(self.gpu_id)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -165,7 +182,7 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- CPU oracle leg
-def oracle_sample(w, target_s, seed=0, max_rows=None):
+def oracle_sample(w, target_s, max_rows=None):
     """Time the fp64 oracle on a stride sample of query rows; returns dict."""
     import oracle
     total_rows = w.B * w.Hq * w.T_prefill
@@ -185,8 +202,9 @@ def oracle_sample(w, target_s, seed=0, max_rows=None):
     tokens_per_s = rows.size / w.Hq / dt
     return {"value": tokens_per_s, "unit": "tokens/s", "cores": oracle.max_threads(),
             "kind": "oracle", "seconds": dt,
-            "sample": "%d of %d query rows (uniform stride over batch x heads x tokens); "
-                      "tokens/s = rows / Hq / time" % (rows.size, total_rows)}
+            "sample": "%d of %d query rows (uniform stride over batch x heads x tokens) of "
+                      "the %s prefill; tokens/s = rows / Hq / time"
+                      % (rows.size, total_rows, workload_label(w))}
 
 
 def run_reference(args, world, rank):
@@ -209,7 +227,7 @@ def run_reference(args, world, rank):
             "ms_per_step": 1000.0 * secs / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w, args),
+            "config": workload_config(w, args.layout, args.chunk),
             "cpu_baseline": {"kind": "oracle", "cores": last["cores"], "value": value,
                              "unit": "tokens/s", "sample": last["sample"]},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -217,11 +235,16 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(w, args):
-    return {"workload": "qwen2.5-0.5b-prefill+1-decode B%d Hq%d Hkv%d T%d+1 d64 G%d"
-                        % (w.B, w.Hq, w.Hkv, w.T_prefill, w.G),
+def workload_label(w):
+    """e.g. "llama-3.2-1b-prefill+1-decode B4 Hq32 Hkv8 T8192+1 d64 G6"."""
+    return ("%s+1-decode B%d Hq%d Hkv%d T%d+1 d64 G%d"
+            % (w.name.split()[0], w.B, w.Hq, w.Hkv, w.T_prefill, w.G))
+
+
+def workload_config(w, layout, chunk):
+    return {"workload": workload_label(w),
             "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T_prefill, "decode_tokens": 1,
-            "d": 64, "dv": 64, "G": w.G, "state_layout": args.layout, "chunk": args.chunk,
+            "d": 64, "dv": 64, "G": w.G, "state_layout": layout, "chunk": chunk,
             "l2": "flushed (256 MiB write) before every timed step",
             "seed": w.seed}
 
@@ -248,10 +271,289 @@ def kernel_work(name, fl):
     return 0.0, False
 
 
+class PrefillBench:
+    """One prefill workload on the device: inputs resident in HBM, the step
+    (expand + prefill + one decode token) callable directly or from a graph."""
+
+    def __init__(self, cfg_idx, chunk, layout_name, dev, stream):
+        import torch
+        from grouped_quadratic_gb300 import inputs, oal
+        self.oal = oal
+        self.dev, self.stream = dev, stream
+        self.layout_name = layout_name
+        self.layout = oal.OAL_STATE_PACKED if layout_name == "packed" else oal.OAL_STATE_FULL
+        cfg = inputs.CONFIGS[cfg_idx]
+        w = inputs.config(cfg_idx, T=cfg["T"] + 1, decode_steps=1)
+        self.w = w
+        Tp = w.T_prefill
+        self.Tp = Tp
+        self.chunk = chunk
+        Qh, Kh, Vh = w.torch_inputs("cpu")
+        self.host = (Qh, Kh, Vh)
+        self.Q = Qh[:, :, :Tp].contiguous().to(dev)
+        self.K = Kh[:, :, :Tp].contiguous().to(dev)
+        self.V = Vh[:, :, :Tp].contiguous().to(dev)
+        self.q1 = Qh[:, :, Tp].contiguous().to(dev)
+        self.k1 = Kh[:, :, Tp].contiguous().to(dev)
+        self.v1 = Vh[:, :, Tp].contiguous().to(dev)
+        self.L = torch.from_numpy(w.L).to(dev)
+        self.group = torch.from_numpy(w.group).to(dev)
+        self.dt = oal.OAL_BF16 if w.dtype == "bf16" else oal.OAL_F32
+        B, Hq, Hkv = w.B, w.Hq, w.Hkv
+        self.a = torch.empty(Hq, device=dev)
+        self.b = torch.empty(Hq, D, device=dev)
+        self.C = torch.empty(Hq, oal.oal_coeff_table_elems(D, self.layout), device=dev)
+        self.state = torch.empty(B, Hkv, oal.oal_state_rows(D, self.layout), U, device=dev)
+        self.Y = torch.empty(B, Hq, Tp, D, dtype=self.Q.dtype, device=dev)
+        self.y1 = torch.empty(B, Hq, D, dtype=self.Q.dtype, device=dev)
+        self.ws_p = torch.empty(max(256, oal.oal_prefill_workspace_bytes(
+            B, Hq, Hkv, Tp, D, D, self.dt, self.layout, chunk)), dtype=torch.uint8, device=dev)
+        self.ws_p1 = torch.empty(max(256, oal.oal_prefill_workspace_bytes(
+            1, Hq, Hkv, Tp, D, D, self.dt, self.layout, chunk)), dtype=torch.uint8, device=dev)
+        self.ws_d = torch.empty(max(256, oal.oal_decode_workspace_bytes(B, Hq, Hkv, D, D,
+                                                                        self.layout)),
+                                dtype=torch.uint8, device=dev)
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    @property
+    def tokens_per_step(self):
+        return self.w.B * (self.Tp + 1)
+
+    def step(self, st=None):
+        oal, w = self.oal, self.w
+        st = self.stream if st is None else st
+        oal.oal_expand_coeffs(self.L, self.group, w.eps, self.layout, self.a, self.b, self.C,
+                              stream=st)
+        oal.oal_prefill(self.Q, self.K, self.V, self.L, self.group, w.eps, self.a, self.b,
+                        self.C, self.layout, state=self.state, Y=self.Y, chunk=self.chunk,
+                        workspace=self.ws_p, stream=st)
+        oal.oal_decode_step(self.q1, self.k1, self.v1, self.a, self.b, self.C, self.state,
+                            self.layout, y=self.y1, workspace=self.ws_d, stream=st)
+
+    def timed(self, steps, warmup, lib, world=1, clocks=None):
+        """Graph-replayed timed steps; returns (ms per step list, launches per step)."""
+        import torch
+        stream = self.stream
+        for _ in range(warmup):
+            self.flush.zero_()
+            self.step()
+        self.oal.oal_sync_status()
+        graph = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        c0 = lib.oal_launch_counter()
+        with torch.cuda.graph(graph):
+            self.step(torch.cuda.current_stream())
+        launches_per_step = lib.oal_launch_counter() - c0
+        for _ in range(warmup):
+            self.flush.zero_()
+            graph.replay()
+        torch.cuda.synchronize()
+        self.oal.oal_sync_status()
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for s in range(steps):
+            self.flush.zero_()
+            ev0[s].record(stream)
+            graph.replay()
+            ev1[s].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        self.oal.oal_sync_status()
+        del graph
+        return [ev0[s].elapsed_time(ev1[s]) for s in range(steps)], launches_per_step
+
+    def per_kernel(self, steps, lib):
+        """Per-kernel device ms per prefill call: a second pass with CUDA
+        events recorded between the prefill's launches (the C ABI's timing
+        hook, on the launching stream).  The events serialise the launches,
+        so these are upper bounds of the times inside the graph-replayed steps."""
+        import ctypes
+
+        import torch
+        oal, w, stream = self.oal, self.w, self.stream
+        n_ev = 12
+        kev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
+        for evs in kev:
+            for e in evs:
+                e.record(stream)
+        torch.cuda.synchronize()
+        ev_arrays = [(ctypes.c_void_p * n_ev)(*[e.cuda_event for e in evs]) for evs in kev]
+        names = None
+        for s in range(steps):
+            self.flush.zero_()
+            oal.oal_expand_coeffs(self.L, self.group, w.eps, self.layout, self.a, self.b,
+                                  self.C, stream=stream)
+            lib.oal_set_launch_events(ev_arrays[s], n_ev)
+            oal.oal_prefill(self.Q, self.K, self.V, self.L, self.group, w.eps, self.a, self.b,
+                            self.C, self.layout, state=self.state, Y=self.Y, chunk=self.chunk,
+                            workspace=self.ws_p, stream=stream)
+            nk = lib.oal_last_call_launches()
+            names = [lib.oal_last_call_launch_name(i).decode() for i in range(nk)]
+            lib.oal_set_launch_events(None, 0)
+        torch.cuda.synchronize()
+        oal.oal_sync_status()
+        nk = min(len(names), n_ev - 1)
+        per_call, launches = {}, {}
+        for k in range(nk):
+            launches[names[k]] = launches.get(names[k], 0) + 1
+        for s in range(steps):
+            acc = {}
+            for k in range(nk):
+                acc[names[k]] = acc.get(names[k], 0.0) + kev[s][k].elapsed_time(kev[s][k + 1])
+            for k, v in acc.items():
+                per_call.setdefault(k, []).append(v)
+        return {k: statistics.mean(v) for k, v in per_call.items()}, launches
+
+    def roofline(self, pk, launches, step_ms, pks):
+        w = self.w
+        chunk = self.chunk if self.chunk else (128 if self.dt == self.oal.OAL_BF16 else 64)
+        fl = algorithmic_flops(w.B, w.Hq, w.Hkv, self.Tp, chunk)
+        cands = [k for k in pk if kernel_work(k, fl)[0] > 0]
+        dom = max(cands, key=pk.get)
+        work, tensor = kernel_work(dom, fl)
+        achieved = work / (pk[dom] / 1000.0) / 1e12
+        peak = pks["bf16_tflops"] if tensor else FP32_SIMT_PEAK_TFLOPS
+        key = (w.B, w.Hq, w.Hkv, self.Tp, w.G, self.layout_name, chunk)
+        nbytes = traffic_for(dom, key)
+        kernel_ms = pk[dom] / launches[dom]
+        return {"bound": "tensor" if tensor else "alu", "kernel": dom,
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "traffic": nbytes,
+                "traffic_unit": "DRAM bytes per launch (ncu dram__bytes_read.sum + "
+                                "dram__bytes_write.sum, cold cache)",
+                "peak_source": ("measured bf16 burst (MEASURED_PEAKS.json)" if tensor else
+                                "fp32 CUDA-core FMA peak: 152 SMs x 128 lanes x 2 x 2.07 GHz"),
+                "kernel_ms_per_call": pk[dom],
+                "kernel_ms_per_launch": kernel_ms,
+                "kernel_launches_per_call": launches[dom],
+                "kernel_share": pk[dom] / statistics.mean(step_ms),
+                "per_kernel_timing": "second pass, CUDA events between launches",
+                "per_kernel_ms_per_call": pk,
+                "launches_per_call": launches,
+                "algorithmic_flops_per_call": work,
+                "prefill_total": {"algorithmic_flops": fl["total"],
+                                  "device_ms": sum(pk.values()),
+                                  "achieved_tflops": fl["total"] / (sum(pk.values()) / 1e3) / 1e12,
+                                  "frac": fl["total"] / (sum(pk.values()) / 1e3) / 1e12 /
+                                          pks["bf16_tflops"]}}
+
+    def e2e(self, steps, warmup, world):
+        """Step through the C ABI with host buffers: pinned host->device copies
+        of every input and device->host copies of the outputs inside the timed
+        region.  The prefill runs one call per sequence (sequences are
+        independent), so sequence b+1's inputs copy in on one stream and
+        sequence b-1's output copies out on another while sequence b computes."""
+        import torch
+        oal, w = self.oal, self.w
+        stream, Tp, B = self.stream, self.Tp, w.B
+        Qh, Kh, Vh = self.host
+        Qp, Kp, Vp = (t[:, :, :Tp].contiguous().pin_memory() for t in (Qh, Kh, Vh))
+        q1p, k1p, v1p = (t[:, :, Tp].contiguous().pin_memory() for t in (Qh, Kh, Vh))
+        Lp = torch.from_numpy(w.L).pin_memory()
+        gp = torch.from_numpy(w.group).pin_memory()
+        Yp = torch.empty(self.Y.shape, dtype=self.Y.dtype).pin_memory()
+        y1p = torch.empty(self.y1.shape, dtype=self.y1.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (Qp, Kp, Vp, q1p, k1p, v1p, Lp, gp))
+        d2h = Yp.numel() * Yp.element_size() + y1p.numel() * y1p.element_size()
+        cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+
+        def e2e_step(ev_start):
+            cin.wait_event(ev_start)
+            with torch.cuda.stream(cin):
+                self.L.copy_(Lp, non_blocking=True)
+                self.group.copy_(gp, non_blocking=True)
+                e_par = torch.cuda.Event()
+                e_par.record(cin)
+                e_in = []
+                for bb in range(B):
+                    for dst, src in ((self.Q, Qp), (self.K, Kp), (self.V, Vp)):
+                        dst[bb].copy_(src[bb], non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(cin)
+                    e_in.append(e)
+                for dst, src in ((self.q1, q1p), (self.k1, k1p), (self.v1, v1p)):
+                    dst.copy_(src, non_blocking=True)
+                e_tok = torch.cuda.Event()
+                e_tok.record(cin)
+            stream.wait_event(e_par)
+            oal.oal_expand_coeffs(self.L, self.group, w.eps, self.layout, self.a, self.b,
+                                  self.C, stream=stream)
+            for bb in range(B):
+                stream.wait_event(e_in[bb])
+                oal.oal_prefill(self.Q[bb:bb + 1], self.K[bb:bb + 1], self.V[bb:bb + 1],
+                                self.L, self.group, w.eps, self.a, self.b, self.C, self.layout,
+                                state=self.state[bb:bb + 1], Y=self.Y[bb:bb + 1],
+                                chunk=self.chunk, workspace=self.ws_p1, stream=stream)
+                e = torch.cuda.Event()
+                e.record(stream)
+                cout.wait_event(e)
+                with torch.cuda.stream(cout):
+                    Yp[bb].copy_(self.Y[bb], non_blocking=True)
+            stream.wait_event(e_tok)
+            oal.oal_decode_step(self.q1, self.k1, self.v1, self.a, self.b, self.C, self.state,
+                                self.layout, y=self.y1, workspace=self.ws_d, stream=stream)
+            e = torch.cuda.Event()
+            e.record(stream)
+            cout.wait_event(e)
+            with torch.cuda.stream(cout):
+                y1p.copy_(self.y1, non_blocking=True)
+            e_out = torch.cuda.Event()
+            e_out.record(cout)
+            stream.wait_event(e_out)
+
+        for _ in range(warmup):
+            e = torch.cuda.Event()
+            e.record(stream)
+            e2e_step(e)
+        torch.cuda.synchronize()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        barrier(world)
+        for s in range(steps):
+            self.flush.zero_()
+            es[s].record(stream)
+            e2e_step(es[s])
+            ee[s].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_s = max_over_ranks(sum(es[s].elapsed_time(ee[s]) for s in range(steps)) / 1e3,
+                               world)
+        return {"value": self.tokens_per_step * world * steps / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": 1e3 * e2e_s / steps,
+                "pipeline": "one prefill call per sequence; copies in and out on two "
+                            "streams beside the compute stream"}
+
+
+def measure_prefill(cfg_idx, chunk, layout, steps, warmup, dev, stream, lib, pks, world=1,
+                    with_e2e=False):
+    import torch
+    pb = PrefillBench(cfg_idx, chunk, layout, dev, stream)
+    step_ms, launches_per_step = pb.timed(steps, warmup, lib, world)
+    total_s = max_over_ranks(sum(step_ms) / 1000.0, world)
+    pk, launches = pb.per_kernel(steps, lib)
+    out = {"workload": workload_label(pb.w), "config": workload_config(pb.w, layout, chunk),
+           "value": pb.tokens_per_step * world * steps / total_s, "unit": "tokens/s",
+           "ms_per_step": 1e3 * total_s / steps,
+           "step_ms": step_ms,
+           "roofline": pb.roofline(pk, launches, step_ms, pks),
+           "gpu_launches": int(launches_per_step * steps),
+           "launches_per_step": int(launches_per_step)}
+    if with_e2e:
+        out["e2e"] = pb.e2e(steps, warmup, world)
+    out["_w"] = pb.w
+    del pb
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank, local):
     import torch
     from grouped_quadratic_gb300 import build as gq_build
-    from grouped_quadratic_gb300 import inputs, oal
+    from grouped_quadratic_gb300 import oal
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device (no CPU fallback)")
@@ -259,206 +561,50 @@ def run_ours(args, world, rank, local):
     lib = oal.load_library()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    layout = oal.OAL_STATE_PACKED if args.layout == "packed" else oal.OAL_STATE_FULL
-    cfg = inputs.CONFIGS[args.config]
-    w = inputs.config(args.config, T=cfg["T"] + 1, decode_steps=1)
-    Tp = w.T_prefill
-    chunk = args.chunk
-    Qh, Kh, Vh = w.torch_inputs("cpu")
-    Q = Qh[:, :, :Tp].contiguous().to(dev)
-    K = Kh[:, :, :Tp].contiguous().to(dev)
-    V = Vh[:, :, :Tp].contiguous().to(dev)
-    q1 = Qh[:, :, Tp].contiguous().to(dev)
-    k1 = Kh[:, :, Tp].contiguous().to(dev)
-    v1 = Vh[:, :, Tp].contiguous().to(dev)
-    L = torch.from_numpy(w.L).to(dev)
-    group = torch.from_numpy(w.group).to(dev)
-    dt = oal.OAL_BF16 if w.dtype == "bf16" else oal.OAL_F32
-    Hq, Hkv, B = w.Hq, w.Hkv, w.B
-    a = torch.empty(Hq, device=dev)
-    b = torch.empty(Hq, D, device=dev)
-    C = torch.empty(Hq, oal.oal_coeff_table_elems(D, layout), device=dev)
-    state = torch.empty(B, Hkv, oal.oal_state_rows(D, layout), U, device=dev)
-    Y = torch.empty(B, Hq, Tp, D, dtype=Q.dtype, device=dev)
-    y1 = torch.empty(B, Hq, D, dtype=Q.dtype, device=dev)
-    ws_p = torch.empty(max(256, oal.oal_prefill_workspace_bytes(B, Hq, Hkv, Tp, D, D, dt, layout,
-                                                                chunk)), dtype=torch.uint8, device=dev)
-    ws_d = torch.empty(max(256, oal.oal_decode_workspace_bytes(B, Hq, Hkv, D, D, layout)),
-                       dtype=torch.uint8, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-
-    def step(st=stream):
-        oal.oal_expand_coeffs(L, group, w.eps, layout, a, b, C, stream=st)
-        oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, layout, state=state, Y=Y,
-                        chunk=chunk, workspace=ws_p, stream=st)
-        oal.oal_decode_step(q1, k1, v1, a, b, C, state, layout, y=y1, workspace=ws_d,
-                            stream=st)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    oal.oal_sync_status()
-
-    # The timed steps replay one step captured as a CUDA graph, so that the
-    # host's per-call work (Python, argument checks, tensor-map encoding) stays
-    # off the device timeline; the kernels and their programmatic launch
-    # overlap are the same as in a direct call.  Launches are counted while the
-    # step is captured: each replay runs that many of the library's kernels.
-    graph = torch.cuda.CUDAGraph()
-    torch.cuda.synchronize()
-    c0 = lib.oal_launch_counter()
-    with torch.cuda.graph(graph):
-        step(torch.cuda.current_stream())
-    launches_per_step = lib.oal_launch_counter() - c0
-    for _ in range(args.warmup):
-        flush.zero_()
-        graph.replay()
-    torch.cuda.synchronize()
-    oal.oal_sync_status()
-
-    barrier(world)
-    torch.cuda.synchronize()
-    gpu_id = "GPU-%s" % torch.cuda.get_device_properties(dev).uuid
-    ev_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    with ClockSampler(gpu_id) as clk:
-        for s in range(args.steps):
-            flush.zero_()
-            ev_start[s].record(stream)
-            graph.replay()
-            ev_end[s].record(stream)
-        torch.cuda.synchronize()
-    launches = launches_per_step * args.steps
-    barrier(world)
-    oal.oal_sync_status()
-    step_ms = [ev_start[s].elapsed_time(ev_end[s]) for s in range(args.steps)]
-    total_s = max_over_ranks(sum(step_ms) / 1000.0, world)
-    tokens_per_step = B * (Tp + 1)
-    value = tokens_per_step * world * args.steps / total_s
-
-    # Per-kernel durations: a second pass over the same steps with CUDA events
-    # recorded on the stream between the prefill's launches (timing hook of
-    # the C ABI).  The events serialise the launches, so these durations are
-    # upper bounds of what the kernels take inside the timed steps above.
-    n_ev = 8
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
-    for evs in kev:
-        for e in evs:
-            e.record(stream)
-    torch.cuda.synchronize()
-    import ctypes
-    ev_arrays = [(ctypes.c_void_p * n_ev)(*[e.cuda_event for e in evs]) for evs in kev]
-    names = None
-    for s in range(args.steps):
-        flush.zero_()
-        oal.oal_expand_coeffs(L, group, w.eps, layout, a, b, C, stream=stream)
-        lib.oal_set_launch_events(ev_arrays[s], n_ev)
-        oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, layout, state=state, Y=Y,
-                        chunk=chunk, workspace=ws_p, stream=stream)
-        nk = lib.oal_last_call_launches()
-        names = [lib.oal_last_call_launch_name(i).decode() for i in range(nk)]
-        lib.oal_set_launch_events(None, 0)
-        oal.oal_decode_step(q1, k1, v1, a, b, C, state, layout, y=y1, workspace=ws_d,
-                            stream=stream)
-    torch.cuda.synchronize()
-    oal.oal_sync_status()
-
-    # per-kernel durations inside the prefill call (summed per kernel name when a
-    # kernel runs more than once per call)
-    nk = len(names)
-    per_call = {}
-    launches_per_call = {}
-    for k in range(min(nk, n_ev - 1)):
-        launches_per_call[names[k]] = launches_per_call.get(names[k], 0) + 1
-    for s in range(args.steps):
-        acc = {}
-        for k in range(min(nk, n_ev - 1)):
-            acc[names[k]] = acc.get(names[k], 0.0) + kev[s][k].elapsed_time(kev[s][k + 1])
-        for k, v in acc.items():
-            per_call.setdefault(k, []).append(v)
-    pk = {k: statistics.mean(v) for k, v in per_call.items()}
     pks = peaks()
-    fl = algorithmic_flops(B, Hq, Hkv, Tp, chunk if chunk else (128 if dt == oal.OAL_BF16 else 64))
-    # dominant kernel: the largest device time per call among the contractions
-    cands = [k for k in pk if kernel_work(k, fl)[0] > 0]
-    dom = max(cands, key=pk.get)
-    work, tensor = kernel_work(dom, fl)
-    achieved = work / (pk[dom] / 1000.0) / 1e12
-    peak = pks["bf16_tflops"] if tensor else FP32_SIMT_PEAK_TFLOPS
-    captured = (dom == READOUT_TRAFFIC["kernel"] and
-                (B, Hq, Hkv, Tp, args.layout) == READOUT_TRAFFIC["workload"] and
-                args.chunk in (0, 128))
-    roofline = {"bound": "tensor" if tensor else "alu", "kernel": dom,
-                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": READOUT_TRAFFIC["bytes"] if captured else None,
-                "traffic_unit": "bytes per launch (ncu, cold cache)",
-                "peak_source": ("measured bf16 burst (MEASURED_PEAKS.json)" if tensor else
-                                "fp32 CUDA-core FMA peak: 152 SMs x 128 lanes x 2 x 2.07 GHz"),
-                "kernel_ms_per_call": pk[dom],
-                "kernel_launches_per_call": launches_per_call[dom],
-                "kernel_share": pk[dom] / statistics.mean(step_ms),
-                "per_kernel_timing": "second pass, CUDA events between launches",
-                "per_kernel_ms_per_call": pk,
-                "launches_per_call": launches_per_call,
-                "algorithmic_flops_per_call": work,
-                "prefill_total": {"algorithmic_flops": fl["total"],
-                                  "device_ms": sum(pk.values()),
-                                  "achieved_tflops": fl["total"] / (sum(pk.values()) / 1e3) / 1e12}}
+    gpu_id = "GPU-%s" % torch.cuda.get_device_properties(dev).uuid
 
-    # e2e through the C ABI with host buffers
-    e2e = None
-    if not args.no_e2e:
-        Qp, Kp, Vp = (t[:, :, :Tp].contiguous().pin_memory() for t in (Qh, Kh, Vh))
-        q1p, k1p, v1p = (t[:, :, Tp].contiguous().pin_memory() for t in (Qh, Kh, Vh))
-        Lp = torch.from_numpy(w.L).pin_memory()
-        gp = torch.from_numpy(w.group).pin_memory()
-        Yp = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
-        y1p = torch.empty(y1.shape, dtype=y1.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in (Qp, Kp, Vp, q1p, k1p, v1p, Lp, gp))
-        d2h = Yp.numel() * Yp.element_size() + y1p.numel() * y1p.element_size()
+    with ClockSampler(gpu_id) as clk:
+        head = measure_prefill(args.config, args.chunk, args.layout, args.steps, args.warmup,
+                               dev, stream, lib, pks, world, with_e2e=not args.no_e2e)
+    w = head.pop("_w")
 
-        def e2e_step():
-            for dst, src in ((Q, Qp), (K, Kp), (V, Vp), (q1, q1p), (k1, k1p), (v1, v1p),
-                             (L, Lp), (group, gp)):
-                dst.copy_(src, non_blocking=True)
-            step()
-            Yp.copy_(Y, non_blocking=True)
-            y1p.copy_(y1, non_blocking=True)
+    subs = {}
+    if not args.no_sub:
+        with ClockSampler(gpu_id) as clk_sub:
+            if args.config != 1:
+                r = measure_prefill(1, 0, args.layout, args.steps, args.warmup, dev, stream,
+                                    lib, pks, world)
+                r.pop("_w")
+                subs["config1"] = r
+            sweep = {}
+            for ch in (64, 128, 256):
+                r = measure_prefill(4, ch, args.layout, max(3, args.steps // 2), args.warmup,
+                                    dev, stream, lib, pks, world)
+                r.pop("_w")
+                sweep[str(ch)] = r
+            subs["config4"] = {"chunk_sweep": sweep}
+        subs["clocks"] = clk_sub.summary()
 
-        for _ in range(args.warmup):
-            e2e_step()
-        torch.cuda.synchronize()
-        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        barrier(world)
-        for s in range(args.steps):
-            flush.zero_()
-            es[s].record(stream)
-            e2e_step()
-            ee[s].record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        e2e_s = max_over_ranks(sum(es[s].elapsed_time(ee[s]) for s in range(args.steps)) / 1e3,
-                               world)
-        e2e = {"value": tokens_per_step * world * args.steps / e2e_s, "unit": "tokens/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": 1e3 * e2e_s / args.steps}
-
-    decode = None if args.no_decode else run_decode(args, world, dev, stream, lib, pks)
+    decode = None
+    if not args.no_decode:
+        decode = {lay: run_decode(args, world, dev, stream, lib, pks, lay)
+                  for lay in ("full", "packed")}
     calib = run_contribution(args, world, dev, stream, lib, pks) if args.contribution else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_sample(w, args.cpu_seconds)
 
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+    line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "ms_per_step": head["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": workload_config(w, args), "roofline": roofline, "cpu_baseline": cpu,
-            "e2e": e2e, "gpu_launches": int(launches), "clocks": clk.summary(),
-            "decode": decode, "peaks_source": pks["source"]}
+            "config": head["config"], "roofline": head["roofline"], "cpu_baseline": cpu,
+            "e2e": head.get("e2e"), "gpu_launches": head["gpu_launches"],
+            "clocks": clk.summary(), "decode": decode, "peaks_source": pks["source"]}
+    line.update(subs)
     if calib is not None:
         line["calibration"] = calib
     line["config"]["launch"] = "one step captured as a CUDA graph, replayed per timed step"
@@ -509,13 +655,13 @@ def run_contribution(args, world, dev, stream, lib, pks):
             "gpu_launches": int(launches)}
 
 
-def run_decode(args, world, dev, stream, lib, pks):
+def run_decode(args, world, dev, stream, lib, pks, layout_name):
     """Decode workload: B=64, Hq=14, Hkv=2, 2048-token prefill then decode steps."""
     import torch
     from grouped_quadratic_gb300 import inputs, oal
     n_steps = args.decode_steps
     w = inputs.config(3, T=2048 + n_steps, decode_steps=n_steps)
-    layout = oal.OAL_STATE_FULL if args.decode_layout == "full" else oal.OAL_STATE_PACKED
+    layout = oal.OAL_STATE_FULL if layout_name == "full" else oal.OAL_STATE_PACKED
     Tp = w.T_prefill
     Qh, Kh, Vh = w.torch_inputs("cpu")
     Q = Qh[:, :, :Tp].contiguous().to(dev)
@@ -555,18 +701,24 @@ def run_decode(args, world, dev, stream, lib, pks):
     io_bytes = (w.B * w.Hq * D * 2 + 2 * w.B * w.Hkv * D) * qd.element_size()
     bytes_per_step = 2 * state_bytes + io_bytes
     gbs = bytes_per_step * n_steps / secs / 1e9
-    return {"workload": "qwen2.5-0.5b-decode B%d Hq%d Hkv%d prefill %d then %d steps, %s state"
-                        % (w.B, w.Hq, w.Hkv, Tp, n_steps, args.decode_layout),
-            "steps_per_s": world * n_steps / secs, "ms_per_step": 1e3 * secs / n_steps,
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pks["hbm_gbs"],
-                         "unit": "GB/s", "frac": gbs / pks["hbm_gbs"],
-                         "traffic": (DECODE_TRAFFIC["bytes"] if (w.B, w.Hq, w.Hkv, args.decode_layout)
-                                     == DECODE_TRAFFIC["workload"] else None),
-                         "traffic_kernel": DECODE_TRAFFIC["kernel"],
-                         "traffic_unit": "bytes per launch (ncu, cold cache; writes partly still in L2)",
-                         "algorithmic_bytes_per_step": bytes_per_step},
-            "gpu_launches": int(launches), "l2": "state set %.0f MB vs 129 MB L2" % (
-                state_bytes / 1e6)}
+    key = (w.B, w.Hq, w.Hkv, layout_name)
+    dk = "decode_stream_kernel"
+    nbytes = traffic_for(dk, key)
+    out = {"workload": "qwen2.5-0.5b-decode B%d Hq%d Hkv%d prefill %d then %d steps, %s state"
+                       % (w.B, w.Hq, w.Hkv, Tp, n_steps, layout_name),
+           "steps_per_s": world * n_steps / secs, "ms_per_step": 1e3 * secs / n_steps,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": pks["hbm_gbs"],
+                        "unit": "GB/s", "frac": gbs / pks["hbm_gbs"],
+                        "traffic": nbytes, "traffic_kernel": dk,
+                        "traffic_unit": "DRAM bytes per launch (ncu, cold cache)",
+                        "algorithmic_bytes_per_step": bytes_per_step},
+           "gpu_launches": int(launches),
+           "l2": "state set %.0f MB vs 126 MB L2" % (state_bytes / 1e6)}
+    if nbytes:
+        out["roofline"]["dram_frac"] = nbytes / (secs / n_steps) / 1e9 / pks["hbm_gbs"]
+    del state, qd, kd, vd
+    torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -575,13 +727,14 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 4])
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 4])
     ap.add_argument("--layout", choices=["packed", "full"], default="packed")
     ap.add_argument("--chunk", type=int, default=0)
     ap.add_argument("--decode-steps", type=int, default=1024)
-    ap.add_argument("--decode-layout", choices=["packed", "full"], default="full")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="skip the config-1 and config-4 sub-lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--contribution", action="store_true",
                     help="also time the contribution scores (calibration step)")
