@@ -565,9 +565,9 @@ static oal_status launch_decode_t(const Tin *q, const Tin *k, const Tin *v, int 
                                   float *state, Tin *y, void *ws, cudaStream_t stream) {
   const int F = state_rows(packed);
   const size_t units = (size_t)B * Hkv;
-  static bool attr_set[256] = {};   // per device: the slice buffers are above 48 KB
+  static bool attr_set[kMaxDevices] = {};   // per device: the slice buffers are above 48 KB
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256)
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return oal_check_launch("decode: cudaGetDevice");
   if (!attr_set[dev]) {
     if (cudaFuncSetAttribute(decode_cluster_kernel<Tin>,

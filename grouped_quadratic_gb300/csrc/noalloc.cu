@@ -8,7 +8,6 @@
 namespace {
 
 constexpr size_t kScratchBytes = OAL_PREFILL_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 256;
 
 // One copy per device, reserved when the library's device code is loaded on
 // that device and kept until the process exits.  In host code this name is
@@ -17,7 +16,7 @@ constexpr int kMaxDevices = 256;
 static __device__ __align__(256) unsigned char g_prefill_scratch[kScratchBytes];
 
 std::mutex g_scratch_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
+void *g_scratch_ptr[oal::kMaxDevices] = {};
 
 // Device address of g_prefill_scratch on the current device, looked up once
 // per device (with that device current) and cached.
@@ -25,8 +24,8 @@ oal_status scratch_for_current_device(void **out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return oal_fail(OAL_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices)
-    return oal_fail(OAL_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxDevices - 1);
+  if (dev < 0 || dev >= oal::kMaxDevices)
+    return oal_fail(OAL_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, oal::kMaxDevices - 1);
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (g_scratch_ptr[dev] == nullptr) {
     void *p = nullptr;
@@ -41,6 +40,8 @@ oal_status scratch_for_current_device(void **out) {
 }
 
 }  // namespace
+
+size_t oal_prefill_noalloc_scratch_bytes(void) { return kScratchBytes; }
 
 oal_status oal_prefill_noalloc(const void *Q, const void *K, const void *V, oal_dtype dtype,
                                int B, int Hq, int Hkv, int T, int d, int dv, const float *L,

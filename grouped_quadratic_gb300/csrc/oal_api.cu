@@ -19,11 +19,11 @@ oal_status launch_prefill_simt(const void *Q, const void *K, const void *V, int 
                                const int32_t *group, int G, float eps, const float *a,
                                const float *b, const float *C, int packed, float *state,
                                int cont, void *Y, int chunk, void *ws, cudaStream_t stream);
-size_t tc_prefill_workspace_bytes(int B, int Hq, int Hkv, int T);
+size_t tc_prefill_workspace_bytes(int B, int Hq, int Hkv, int T, int chunk);
 oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B, int Hq,
                              int Hkv, int T, const float *L, const int32_t *group, int G,
                              float eps, const float *a, const float *b, const float *C,
-                             int packed, float *state, int cont, void *Y, void *ws,
+                             int packed, float *state, int cont, void *Y, int chunk, void *ws,
                              cudaStream_t stream);
 size_t decode_workspace_bytes(int B, int Hkv, int packed);
 int decode_max_rho();
@@ -39,8 +39,17 @@ oal_status group_dims_host(const float *chi_p, int P, int d, const int32_t *boot
                            int nboot, double alpha, double tau, double gamma, int g_min,
                            double eps, int32_t *group, int *G);
 
-// Device status word (one per device the library runs on).
-__device__ int g_status_word;
+// Device control block (one per device the library runs on): the status
+// word kernels record errors in; then, for tests of the failure path, the
+// kernel whose UMMA issuer is to wait on a barrier nothing arrives on
+// (0 = none), and the limit of the bounded waits in SM cycles (0 = the
+// built-in limit).
+struct DeviceControl {
+  int status;
+  int starve;
+  unsigned long long wait_limit;
+};
+__device__ DeviceControl g_control;
 }  // namespace oal
 
 static thread_local char t_msg[512] = "";
@@ -83,17 +92,24 @@ oal_status oal_after_launch(const char *name, cudaStream_t stream) {
   return OAL_OK;
 }
 
+#include <mutex>
+static std::mutex g_control_mutex;
+static int *g_control_addr[oal::kMaxDevices] = {nullptr};
+
 int *oal_device_status_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  static int *addr[64] = {nullptr};
-  if (dev < 0 || dev >= 64) return nullptr;
-  if (!addr[dev]) {
+  if (dev < 0 || dev >= oal::kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_control_mutex);
+  if (!g_control_addr[dev]) {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, oal::g_status_word) != cudaSuccess) return nullptr;
-    addr[dev] = (int *)p;
+    if (cudaGetSymbolAddress(&p, oal::g_control) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_control_addr[dev] = &static_cast<oal::DeviceControl *>(p)->status;
   }
-  return addr[dev];
+  return g_control_addr[dev];
 }
 
 namespace {
@@ -194,9 +210,9 @@ oal_status oal_expand_coeffs(const float *L, const int32_t *group, int Hq, int G
 
 static int default_chunk(oal_dtype dtype) { return dtype == OAL_BF16 ? 128 : 64; }
 
-// bf16 inputs with 128-token chunks run on the tensor cores (tcgen05); every
-// other combination runs the fp32 CUDA-core kernels.
-static bool use_tc(oal_dtype dtype, int chunk) { return dtype == OAL_BF16 && chunk == 128; }
+// bf16 inputs run on the tensor cores (tcgen05) at every chunk size; fp32
+// inputs run the fp32 CUDA-core kernels.
+static bool use_tc(oal_dtype dtype) { return dtype == OAL_BF16; }
 
 size_t oal_prefill_workspace_bytes(int B, int Hq, int Hkv, int T, int d, int dv,
                                    oal_dtype dtype, oal_state_layout layout, int chunk) {
@@ -204,7 +220,7 @@ size_t oal_prefill_workspace_bytes(int B, int Hq, int Hkv, int T, int d, int dv,
   if (chunk == 0) chunk = default_chunk(dtype);
   if (chunk != 64 && chunk != 128 && chunk != 256) return 0;
   if (T == 0 || B == 0) return 256;
-  if (use_tc(dtype, chunk)) return oal::tc_prefill_workspace_bytes(B, Hq, Hkv, T);
+  if (use_tc(dtype)) return oal::tc_prefill_workspace_bytes(B, Hq, Hkv, T, chunk);
   return oal::simt_prefill_workspace_bytes(B, Hkv, T, layout == OAL_STATE_PACKED, chunk);
 }
 
@@ -255,9 +271,9 @@ oal_status oal_prefill(const void *Q, const void *K, const void *V, oal_dtype dt
   if ((long long)T * Hq * B > (1LL << 40))
     return oal_fail(OAL_ERR_UNSUPPORTED, "problem too large");
   oal_begin_call(stream);
-  if (use_tc(dtype, chunk))
+  if (use_tc(dtype))
     return oal::launch_prefill_tc(Q, K, V, B, Hq, Hkv, T, L, group, G, eps, a, b, C, packed,
-                                  state, continue_from_state != 0, Y, workspace, stream);
+                                  state, continue_from_state != 0, Y, chunk, workspace, stream);
   return oal::launch_prefill_simt(Q, K, V, dtype == OAL_BF16, B, Hq, Hkv, T, L, group, G,
                                   eps, a, b, C, packed, state, continue_from_state != 0,
                                   Y, chunk, workspace, stream);
@@ -353,6 +369,23 @@ oal_status oal_group_dims(const float *chi_p, int P, int d, const int32_t *boot_
       return oal_fail(OAL_ERR_INVALID_ARG, "score %zu is negative or not finite", i);
   return oal::group_dims_host(chi_p, P, d, boot_idx, nboot, alpha, tau, gamma, g_min, eps,
                               group, G);
+}
+
+oal_status oal_debug_wait_test(uint64_t wait_limit_cycles, int starve) {
+  t_msg[0] = 0;
+  if (starve < 0 || starve > 3) return oal_fail(OAL_ERR_INVALID_ARG, "starve=%d", starve);
+  int *w = oal_device_status_word();
+  if (!w) return oal_fail(OAL_ERR_CUDA, "device control block unavailable");
+  oal::DeviceControl c;
+  cudaError_t e = cudaMemcpy(&c, w, sizeof c, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) {
+    c.starve = starve;
+    c.wait_limit = wait_limit_cycles;
+    e = cudaMemcpy(w, &c, sizeof c, cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess)
+    return oal_fail(OAL_ERR_CUDA, "setting the wait test: %s", cudaGetErrorString(e));
+  return OAL_OK;
 }
 
 oal_status oal_sync_status(cudaStream_t stream) {

@@ -25,6 +25,9 @@ constexpr int kH2Packed = kD * (kD + 1) / 2;    // 2080
 constexpr int kFFull = 1 + kD + kH2Full;        // 4161
 constexpr int kFPacked = 1 + kD + kH2Packed;    // 2145
 constexpr int kMaxG = 7;
+// Per-device caches of the library (symbol addresses, function attributes)
+// cover device ordinals 0 .. kMaxDevices - 1.
+constexpr int kMaxDevices = 256;
 
 // Device status word values (written by kernels, read by oal_sync_status).
 constexpr int kStatusOk = 0;
@@ -101,4 +104,13 @@ oal_status oal_check_launch(const char *what);
 oal_status oal_after_launch(const char *name, cudaStream_t stream);
 // At the start of every entry point that may launch kernels.
 void oal_begin_call(cudaStream_t stream);
-int *oal_device_status_word();  // device address of the status word, or null
+// Device address of the status word of the current device, or null.  For
+// tests of the failure path, the int after it names a kernel whose UMMA
+// issuer is to wait on a barrier nothing arrives on (kStarve*; 0 = none) and
+// the 64-bit word 8 bytes after it holds the limit of the bounded waits in SM
+// cycles (0: the built-in limit); kernels read both through the status
+// pointer they are given.
+int *oal_device_status_word();
+namespace oal {
+constexpr int kStarveReadout = 1, kStarveState = 2, kStarveIntra = 3;
+}

@@ -330,9 +330,9 @@ static oal_status launch_simt(const Tin *Q, const Tin *K, const Tin *V, int B,
   const int F = state_rows(packed);
   const int nC = (T + chunk - 1) / chunk;
   // shared-memory limits above 48 KB: a function attribute of each device
-  static bool attr_set[256] = {};
+  static bool attr_set[kMaxDevices] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256)
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return oal_fail(OAL_ERR_CUDA, "prefill: no current device");
   if (!attr_set[dev]) {
     if (cudaFuncSetAttribute(chunk_delta_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -3,11 +3,13 @@
 //
 // [OAL] = "Not All Dimensions Are Equal: Outlier-Aware Attention
 // Linearization with Grouped Quadratic Kernels".  For token i of chunk c
-// (C = 128 tokens)
+// (C = 64, 128 or 256 tokens)
 //     u~_i = Phi~(q_i)^T S_{c-1}  +  sum_{j in c, j <= i} kappa(q_i, k_j) u_j,
 // S_{c-1} = the Eq. (5) prefix states over all tokens before the chunk,
 // Phi~ = the Eq. (6) readout weights, kappa = Eq. (7).  The split is exact
-// (App. D, Eq. (25)).
+// (App. D, Eq. (25)).  The kernels work on 128-token stages and 128-row
+// tiles whatever C is: a tile is one chunk (C = 128), half of one (C = 256)
+// or two (C = 64).
 //
 // Internal feature order (K of every contraction, 2192 = 35 x 64 - 48):
 //   [0, 2112)     H2_rt in "paired" rows: for r = 0..63, t = (r & ~1) .. 63.
@@ -29,21 +31,24 @@
 //                       per (feature tile, part): the part's total
 //                       Delta S = sum phi(k_j) u_j^T.
 //                       mode 1: per (feature tile, part): walk the part's
-//                       chunks with the fp32 running state in registers;
+//                       stages with the fp32 running state in registers;
 //                       before each chunk write its bf16 snapshot S_{c-1};
 //                       the last part writes the final fp32 state.
-//   tc_intra_kernel     per (query head, chunk): intra-chunk kappa tile from
-//                       s = Q_c K_c^T (UMMA) plus the tail-group sums (fp32
-//                       FMA), P.V by UMMA; numerators and denominators to
-//                       the workspace.
-//   tc_readout_kernel   per (query head, chunk, batch x KV head): inter-chunk
-//                       readout Phi~(Q_c) S_{c-1} as a 128 x 80 x 2192 UMMA
-//                       (A = Phi~ built by threads straight into tensor
-//                       memory, B = snapshot streamed by TMA), plus the
+//   tc_intra_kernel     per (query head, 128-row tile): intra-chunk kappa
+//                       from s = Q K^T (UMMA) plus the tail-group sums (fp32
+//                       FMA) over the keys of each row's chunk, P.V by UMMA;
+//                       numerators and denominators to the workspace.
+//   tc_readout_kernel   per (query head, 128-row tile, batch x KV head):
+//                       inter-chunk readout Phi~(Q) S_{c-1} as a
+//                       128 x 80 x 2192 UMMA (128 x 160 for C = 64: the
+//                       snapshots of the tile's two chunks side by side;
+//                       A = Phi~ built by threads straight into tensor
+//                       memory, B = snapshots streamed by TMA), plus the
 //                       intra-chunk rows, then normalisation.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <mutex>
 #include <utility>
 
 #include "oal_internal.cuh"
@@ -61,7 +66,6 @@ constexpr int kNKB = 35;         // readout K blocks of 64 (the last one has K =
 constexpr int kTiles = 18;       // 128-feature tiles of the state kernel
 constexpr int kN = 80;           // UMMA N of [v | 1]: 64 value columns, the "1" column, 15 zeros
 constexpr int kMaxNH = 1;        // query heads per readout block (three blocks per SM)
-constexpr int kIntraNH = 1;      // query heads per intra-chunk block
 constexpr int kMaxTailG = 6;     // tail groups (G - 1 <= 6)
 // Snapshot rows: the 64 value columns and the "1" column; the readout's TMA box
 // is kN = 80 rows high and reads rows 65..79 as zero (out of range).
@@ -537,13 +541,20 @@ struct __align__(1024) StateSmem {
   float rows[128][kU];
   uint64_t kv_full[kStateStages], kv_empty[kStateStages];
   uint64_t a_full[2], a_empty[2], d_full[2], d_empty[2];
+  uint64_t drain;                               // every MMA of the block complete
+  uint64_t never;                               // failure-path tests: nothing arrives
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(StateSmem) + 1024 <= 227 * 1024, "state shared memory");
 
 struct StateArgs {
-  int T, nC, U, cpp, nparts, packed, cont, mode;
+  int T;
+  int nS;                    // 128-token stages: ceil(T / 128)
+  int chunk;                 // snapshot period C: 64, 128 or 256 tokens
+  int nC;                    // chunks: ceil(T / C)
+  int spp;                   // stages per part (a multiple of C / 128 when C = 256)
+  int U, nparts, packed, cont, mode;
   const float *state_in;     // external state (continue) or null
   float *state_out;          // external state (mode 1, last part)
   float *ptot;               // [U][nparts][kTiles][128][kN] fp32 part totals
@@ -580,9 +591,13 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
   StateSmem &s = *reinterpret_cast<StateSmem *>(smem_align1024(smem_raw));
   const int tile = blockIdx.x, part = blockIdx.y, unit = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c0 = part * args.cpp;
-  const int c1 = min(args.nC, c0 + args.cpp);
-  const int nchunks = c1 - c0;
+  // the part's 128-token stages [s0, s1) and chunks [j0, j0 + nchunks)
+  const int C = args.chunk;
+  const int s0 = part * args.spp;
+  const int s1 = min(args.nS, s0 + args.spp);
+  const int nstages = s1 - s0;
+  const int j0 = s0 * kC / C;
+  const int nchunks = min(args.nC, (s1 * kC + C - 1) / C) - j0;
   const int mode = args.mode;
   // Mode 0 signals its dependents only after its own wait, so the walk
   // (mode 1) can never start before the prep kernel's K^T is complete; the
@@ -603,6 +618,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       mbar_init(&s.d_full[i], 1);
       mbar_init(&s.d_empty[i], 4);
     }
+    mbar_init(&s.drain, 1);
+    mbar_init(&s.never, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -676,14 +693,14 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       int issued = 0;
-      for (int i = 0; i < nchunks; ++i) {
+      for (int i = 0; i < nstages; ++i) {
         const int st = i % kStateStages;
         if (!mbar_wait(&s.kv_empty[st], ((i / kStateStages) & 1) ^ 1, abort_flag, args.status))
           break;
         mbar_arrive_expect_tx(&s.kv_full[st], 2 * kC * 64 * 2);
-        tma_load_3d(s.kv[st][0], &tmK, &s.kv_full[st], (c0 + i) * kC, 0, unit);
-        tma_load_3d(s.kv[st][0] + 64 * 64, &tmK, &s.kv_full[st], (c0 + i) * kC + 64, 0, unit);
-        tma_load_3d(s.kv[st][1], &tmV, &s.kv_full[st], 0, (c0 + i) * kC, unit);
+        tma_load_3d(s.kv[st][0], &tmK, &s.kv_full[st], (s0 + i) * kC, 0, unit);
+        tma_load_3d(s.kv[st][0] + 64 * 64, &tmK, &s.kv_full[st], (s0 + i) * kC + 64, 0, unit);
+        tma_load_3d(s.kv[st][1], &tmV, &s.kv_full[st], 0, (s0 + i) * kC, unit);
         issued = i + 1;
       }
       // copies still in flight must land before the block exits
@@ -692,35 +709,65 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer: D[:, 0:80] += A x [V_c | 1] (N = 80), A =
-      // phi(K_c)^T as hi | lo, K = 256; B read MN-major: the V atom straight
-      // from the TMA stage, the constant atom at the stage's atom stride
-      const uint32_t idn = idesc_bf16_f32(128, kN, 1);
-      uint64_t vdesc[kStateStages];
+    // ---------------- MMA issuer (the whole warp runs the loop with warp-uniform
+    // operands; one elected lane issues): D[:, 0:80] += A x [V | 1] (N = 80),
+    // A = phi(K)^T of one stage as hi | lo (K = 256 for its 128 tokens); B read
+    // MN-major: the V atom straight from the TMA stage, the constant atom at
+    // the stage's atom stride.  Accumulator slot j & 1 collects chunk j: a
+    // stage is one chunk (C = 128), half of one (C = 256: the chunk's two
+    // stages accumulate into one slot), or two (C = 64: one MMA group per
+    // 64-token half, each into its own slot).
+    const uint32_t idn = idesc_bf16_f32(128, kN, 1);
+    const bool starve = args.status[1] == kStarveState;   // failure-path test only
+    bool ok = true;
+    for (int i = 0; i < nstages && ok; ++i) {
+      const int sl = i & 1, st = i % kStateStages;
+      if (!mbar_wait(starve && i == 0 ? &s.never : &s.a_full[sl], (i >> 1) & 1, abort_flag,
+                     args.status))
+        break;
+      tc_fence_after();
+      const uint64_t bd = sdesc_sw128(smem_u32(s.kv[st][1]),
+                                      smem_u32(s.ones) - smem_u32(s.kv[st][1]), 1024);
+      const uint32_t a0 = tb + kStateA + 128 * sl;
+      const int ng = C == 64 ? 2 : 1;
+      for (int g = 0; g < ng; ++g) {
+        int j;               // local chunk of this MMA group
+        bool first, last;    // the group opens / closes chunk j
+        if (C == 64) { j = 2 * i + g; first = last = true; }
+        else if (C == 128) { j = i; first = last = true; }
+        else { j = i >> 1; first = (i & 1) == 0; last = (i & 1) == 1 || i == nstages - 1; }
+        if (j >= nchunks) break;   // C = 64: the second half of a last stage lies past T
+        if (first) {
+          if (!mbar_wait(&s.d_empty[j & 1], ((j >> 1) & 1) ^ 1, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        const uint32_t d = tb + kStateD + 128 * (j & 1);
+        // 16-token k-steps k: A columns 8 k (k < 8: hi of tokens 16 k ..; k >= 8:
+        // lo of tokens 16 (k - 8) ..), B token block k & 7
+        const uint32_t acc0 = first ? 0u : 1u;
+        if (C == 64) {
 #pragma unroll
-      for (int st = 0; st < kStateStages; ++st)
-        vdesc[st] = sdesc_sw128(smem_u32(s.kv[st][1]), smem_u32(s.ones) - smem_u32(s.kv[st][1]),
-                                1024);
-      for (int i = 0; i < nchunks; ++i) {
-        const int sl = i & 1, st = i % kStateStages;
-        if (!mbar_wait(&s.a_full[sl], (i >> 1) & 1, abort_flag, args.status)) break;
-        if (!mbar_wait(&s.d_empty[sl], ((i >> 1) & 1) ^ 1, abort_flag, args.status)) break;
-        tc_fence_after();
-        const uint64_t bd = vdesc[st];
-        const uint32_t d = tb + kStateD + 128 * sl;
-        const uint32_t a0 = tb + kStateA + 128 * sl;
+          for (int kk = 0; kk < 8; ++kk) {   // hi then lo of tokens 64 g .. 64 g + 63
+            const int k = 4 * g + kk + (kk >= 4 ? 4 : 0);
+            umma_ts_warp(d, a0 + 8 * k, bd + (uint64_t)(128 * (k & 7)), idn, kk > 0 ? 1u : acc0);
+          }
+        } else {
 #pragma unroll
-        for (int k = 0; k < 16; ++k)       // K = 256: hi half then lo half
-          umma_ts(d, a0 + 8 * k, bd + (uint64_t)(128 * (k & 7)), idn, k > 0 ? 1u : 0u);
-        umma_commit(&s.a_empty[sl]);
-        umma_commit(&s.kv_empty[st]);
-        umma_commit(&s.d_full[sl]);
+          for (int k = 0; k < 16; ++k)
+            umma_ts_warp(d, a0 + 8 * k, bd + (uint64_t)(128 * (k & 7)), idn, k > 0 ? 1u : acc0);
+        }
+        if (last) umma_commit_warp(&s.d_full[j & 1]);
       }
-      // no MMA in flight at dealloc: drain through the accumulator barriers
-      for (int i = max(0, nchunks - 2); i < nchunks; ++i)
-        mbar_wait_teardown(&s.d_full[i & 1], (i >> 1) & 1, args.status);
+      if (!ok) break;
+      umma_commit_warp(&s.a_empty[sl]);
+      umma_commit_warp(&s.kv_empty[st]);
     }
+    // no MMA in flight at dealloc: one commit after every MMA issued
+    umma_commit_warp(&s.drain);
+    if (lane == 0) mbar_wait_teardown(&s.drain, 0, args.status);
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
     // ---------------- builders: group bg builds tokens 64 bg .. 64 bg + 63 of
@@ -729,13 +776,12 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
     const int l = 32 * (warp & 3) + lane;    // TMEM lane = feature row
     const int f = tile * 128 + l;
     const uint16_t code = f < kKP ? g_feat.code[f] : (uint16_t)0xFFFF;
-    for (int i = 0; i < nchunks; ++i) {
+    for (int i = 0; i < nstages; ++i) {
       const int sl = i & 1, st = i % kStateStages;
-      const int c = c0 + i;
       if (!mbar_wait(&s.kv_full[st], (i / kStateStages) & 1, abort_flag, args.status)) break;
-      // slot sl (A in tensor memory) is free once the UMMAs of chunk i - 2 are done
+      // slot sl (A in tensor memory) is free once the UMMAs of stage i - 2 are done
       if (!mbar_wait(&s.a_empty[sl], ((i >> 1) & 1) ^ 1, abort_flag, args.status)) break;
-      const int nvalid = min(kC, args.T - c * kC);
+      const int nvalid = min(kC, args.T - (s0 + i) * kC);
       const uint32_t abase = kStateA + 128 * sl;
       const uint8_t *kth = reinterpret_cast<const uint8_t *>(s.kv[st][0]) + bg * (64 * 128);
 #pragma unroll
@@ -808,7 +854,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       }
     }
     __nv_bfloat16 *snap_row =
-        f < kKP ? args.snap + ((size_t)unit * args.nC + c0) * kSnapRows * kKP + f : nullptr;
+        f < kKP ? args.snap + ((size_t)unit * args.nC + j0) * kSnapRows * kKP + f : nullptr;
     auto write_snapshot = [&](int cc) {   // S_{cc-1} for chunk cc of this part
       if (snap_row) {
         __nv_bfloat16 *dst = snap_row + (size_t)cc * kSnapRows * kKP;
@@ -889,34 +935,27 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
 // ================================================================= readout kernel
 constexpr int kNB = 3;           // snapshot K-block stages
 constexpr int kNA = 3;           // A half slots (128 x 32 bf16, 16 columns) in tensor memory
-constexpr int kTailSlots = 2 * kMaxTailG;
 
+// NS snapshots per 128-row tile: 1 (C = 128: the tile's chunk; C = 256: the
+// chunk the tile is half of) or 2 (C = 64: rows 0..63 read S_{2t-1}, rows
+// 64..127 read S_{2t}, as the two halves of one N = 160 operand).
+template <int NS>
 struct __align__(1024) ReadSmem {
   __nv_bfloat16 q[kMaxNH][kC * 64];    // 128B-swizzled [token][dim], then q^T [dim][token]
   __nv_bfloat16 qs[kMaxNH][kC * 64];   // bf16(alpha_dim q) [dim][token]
-  __nv_bfloat16 b[kNB][kN * 64];       // snapshot K blocks [n][64 features]
+  __nv_bfloat16 b[kNB][NS * kN * 64];  // snapshot K blocks [n][64 features]
   __nv_bfloat16 coef[kMaxNH][kCoefRow];
   uint64_t qkv_full, b_full[kNB], a_full[kNA], a_empty[kNA], d_full;
+  uint64_t never;                      // failure-path tests: nothing arrives
   uint32_t tmem_base;
   int abort_flag;
   int loaded;                          // snapshot K blocks whose load was issued
 };
-static_assert(3 * (sizeof(ReadSmem) + 2048) <= 228 * 1024, "three readout blocks per SM");
-
-struct __align__(1024) IntraSmem {
-  __nv_bfloat16 q[kIntraNH][kC * 64];
-  __nv_bfloat16 k[kC * 64];
-  __nv_bfloat16 v[kC * 64];
-  float kt[kIntraNH][kTailSlots][kC];  // tail-dim key values (fast path), key-major
-  KPlan plan[kIntraNH];
-  uint64_t qkv_full, s_full[2], p_full[2], s_free[2], d_full;
-  uint32_t tmem_base;
-  int abort_flag;
-};
-static_assert(sizeof(IntraSmem) + 1024 <= 56 * 1024, "four intra blocks per SM");
+static_assert(3 * (sizeof(ReadSmem<1>) + 2048) <= 228 * 1024, "three readout blocks per SM");
+static_assert(2 * (sizeof(ReadSmem<2>) + 2048) <= 228 * 1024, "two readout blocks per SM");
 
 struct ReadArgs {
-  int T, nC, Hq, Hkv, rho, nh_per_block;
+  int T, nC, chunk, Hq, Hkv, rho, nh_per_block;
   __nv_bfloat16 *Y;
   float *intra_num;            // [B*Hq][T][64] intra-chunk numerators
   float *intra_den;            // [B*Hq][T]     intra-chunk denominators
@@ -926,13 +965,11 @@ struct ReadArgs {
 };
 
 constexpr int kReadThreads = 160;   // 5 warps
-constexpr int kTmemD = 0;         // D^h at [80h, 80h + 80)
-constexpr int kTmemA = 80;        // three A half slots of 16 columns at [80, 128)
-constexpr uint32_t kReadTmemCols = 128;
-constexpr int kIntraThreads = 192;  // 6 warps
-constexpr int kTmemS = 0;         // intra kernel: two 32-key s / P sub-tiles at 0 and 32
-constexpr int kTmemI = 64;        // intra kernel: numerators at [64, 128)
-constexpr uint32_t kIntraTmemCols = 128;  // up to four intra blocks per SM
+constexpr int kTmemD = 0;         // D at [0, 80 NS)
+template <int NS>
+constexpr int kTmemA = 80 * NS;   // three A half slots of 16 columns
+template <int NS>
+constexpr uint32_t kReadTmemCols = NS == 1 ? 128 : 256;
 
 // ---- readout A block builders (compile-time feature layout)
 // The builder of token row m keeps p = bf16(pw * q) in registers and reads
@@ -1053,6 +1090,53 @@ __device__ __forceinline__ void build_dispatch(int kb, const __nv_bfloat16 *qcol
 }
 #undef OAL_BUILD_CASE
 
+// ---------------------------------------------------------------- intra kernel
+// Intra-chunk part of Eq. (25): sum over the keys j of the query's own chunk
+// with j <= i of kappa(q_i, k_j) u_j, per query row, written to workspace for
+// the readout's epilogue.  One block per (query head, 128-row tile, batch x KV
+// head).  The keys of a tile are those of its chunk up to the tile's last row:
+// 128 (C = 64, 128; for C = 64 the tile's two chunks are told apart by the
+// mask), or 256 for the second half of a 256-token chunk.  Per 32-key block:
+// s = Q K^T by UMMA into tensor memory, the tail-group sums and kappa in fp32
+// on the CUDA cores, P = bf16(kappa) masked to the chunk's causal pairs written
+// back over s, numerators += P V by UMMA.
+constexpr int kIntraNH = 1;              // query heads per intra-chunk block
+constexpr int kTailSlots = 2 * kMaxTailG;
+constexpr int kIntraThreads = 192;       // 6 warps
+constexpr int kTmemS = 0;                // two 32-key s / P sub-tiles at 0 and 32
+constexpr int kTmemI = 64;               // numerators at [64, 128)
+constexpr uint32_t kIntraTmemCols = 128;
+
+template <bool kWide>
+struct __align__(1024) IntraSmem {
+  static constexpr int kKeys = kWide ? 256 : 128;
+  __nv_bfloat16 q[kIntraNH][kC * 64];
+  __nv_bfloat16 k[kKeys * 64];
+  __nv_bfloat16 v[kKeys * 64];
+  float kt[kIntraNH][kTailSlots][kKeys];   // tail-dim key values (fast path), key-major
+  KPlan plan[kIntraNH];
+  uint64_t qkv_full, s_full[2], p_full[2], s_free[2], d_full;
+  uint64_t never;                          // failure-path tests: nothing arrives
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(IntraSmem<false>) + 1024 <= 56 * 1024, "four intra blocks per SM");
+static_assert(sizeof(IntraSmem<true>) + 1024 <= 113 * 1024, "two wide intra blocks per SM");
+
+// Geometry of a tile's keys and of one warp's rows.
+struct IntraGeom {
+  int row0;   // first query row of the tile
+  int ks;     // first key: the start of row0's chunk
+  int nkb;    // 32-key blocks: 4, or 8 for the second half of a 256-token chunk
+};
+__device__ __forceinline__ IntraGeom intra_geom(int t, int C) {
+  IntraGeom g;
+  g.row0 = t * kC;
+  g.ks = (g.row0 / C) * C;
+  g.nkb = (g.row0 + kC - g.ks) / 32;
+  return g;
+}
+
 __device__ __forceinline__ float bf16_at(const __nv_bfloat16 *tile, int row, int col) {
   const uint8_t *base = reinterpret_cast<const uint8_t *>(tile);
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
@@ -1091,16 +1175,18 @@ __device__ __forceinline__ float kappa_g(const KConst<G> &k, float s, const floa
 }
 
 // kappa of two keys (j, j + 1) for one query row, two lanes per packed fp32
-// instruction.  kt: this head's key-major tail values, offset to key j.
+// instruction.  kt: this head's key-major tail values (rows of `stride` keys),
+// offset to key j.
 template <int G>
 __device__ __forceinline__ float2 kappa2_g(const KConst<G> &k, float2 s,
-                                          const float (&qt)[2 * kMaxTailG], const float *kt) {
+                                          const float (&qt)[2 * kMaxTailG], const float *kt,
+                                          int stride) {
   float2 z[G];
   z[0] = s;
 #pragma unroll
   for (int g = 1; g < G; ++g) {
-    const float2 a = *reinterpret_cast<const float2 *>(kt + (2 * g - 2) * kC);
-    const float2 b = *reinterpret_cast<const float2 *>(kt + (2 * g - 1) * kC);
+    const float2 a = *reinterpret_cast<const float2 *>(kt + (2 * g - 2) * stride);
+    const float2 b = *reinterpret_cast<const float2 *>(kt + (2 * g - 1) * stride);
     z[g] = ffma2(make_float2(qt[2 * g - 2], qt[2 * g - 2]), a,
                  make_float2(qt[2 * g - 1] * b.x, qt[2 * g - 1] * b.y));
   }
@@ -1140,32 +1226,43 @@ __device__ float kappa_generic(const KPlan &p, float s, const __nv_bfloat16 *qti
   return kap;
 }
 
-// The intra-chunk role (warps 0-3, thread = query row): for each head and
-// each 32-key block of the chunk, read s = q.k of this row from tensor
-// memory, turn it into kappa (masked to keys j <= i), write P (bf16) back in
-// place for the P.V UMMA, and accumulate the denominator from the same
-// rounded weights.  The two 32-key sub-tiles alternate, so the UMMAs of one
-// block overlap the kappa work of the next.
-template <int G>
-__device__ bool intra_worker(IntraSmem &s, const ReadArgs &args, int nh, int warp, int lane,
-                             uint32_t tb, float (&den_intra)[kIntraNH]) {
+// The intra-chunk role (warps 0-3, thread = query row): for each 32-key block
+// of the tile's keys, read s = q.k of this row from tensor memory, turn it
+// into kappa (masked to the keys j of the row's chunk with j <= i), write P
+// (bf16) back in place for the P.V UMMA, and accumulate the denominator from
+// the same rounded weights.  The two 32-key sub-tiles alternate, so the UMMAs
+// of one block overlap the kappa work of the next.  A warp skips the kappa of
+// a block none of its rows reaches (its P is zero).
+template <int G, bool kWide>
+__device__ bool intra_worker(IntraSmem<kWide> &s, const ReadArgs &args, const IntraGeom &geo,
+                             int nh, int warp, int lane, uint32_t tb,
+                             float (&den_intra)[kIntraNH]) {
+  constexpr int kKeys = IntraSmem<kWide>::kKeys;
   volatile int *abort_flag = &s.abort_flag;
   const int m = threadIdx.x;
+  const int C = args.chunk;
+  const int i_tok = geo.row0 + m;
+  const int cs = (i_tok / C) * C;                  // this row's chunk starts here
+  const int rw0 = geo.row0 + 32 * (warp & 3), rw1 = rw0 + 31;
+  const int csw = (rw0 / C) * C;                   // the warp's rows share one chunk (C >= 64)
   if (!mbar_wait(&s.qkv_full, 0, abort_flag, args.status)) return false;
-  // tail-dim key values of every head (fast path); thread = key row m
+  // tail-dim key values of every head (fast path); thread = key row m (and m + 128)
   for (int hh = 0; hh < nh; ++hh) {
     const KPlan &p = s.plan[hh];
 #pragma unroll
-    for (int g = 0; g < kMaxTailG; ++g) {
-      float k0 = 0.f, k1 = 0.f;
-      if (g < p.ntg && p.nd[g] > 0) k0 = bf16_at(s.k, m, p.dims[g][0]);
-      if (g < p.ntg && p.nd[g] > 1) k1 = bf16_at(s.k, m, p.dims[g][1]);
-      s.kt[hh][2 * g][m] = k0;
-      s.kt[hh][2 * g + 1][m] = k1;
+    for (int x = 0; x < kKeys / kC; ++x) {
+      const int j = m + kC * x;
+#pragma unroll
+      for (int g = 0; g < kMaxTailG; ++g) {
+        float k0 = 0.f, k1 = 0.f;
+        if (g < p.ntg && p.nd[g] > 0) k0 = bf16_at(s.k, j, p.dims[g][0]);
+        if (g < p.ntg && p.nd[g] > 1) k1 = bf16_at(s.k, j, p.dims[g][1]);
+        s.kt[hh][2 * g][j] = k0;
+        s.kt[hh][2 * g + 1][j] = k1;
+      }
     }
   }
   named_bar(2, 128);
-  const int row_max = 32 * (warp & 3) + 31;       // largest query row of this warp
   for (int hh = 0; hh < nh; ++hh) {
     const KPlan &p = s.plan[hh];
     KConst<G> kc;
@@ -1183,14 +1280,15 @@ __device__ bool intra_worker(IntraSmem &s, const ReadArgs &args, int nh, int war
     }
     const bool fast = p.fast != 0;
     float dsum = 0.f;
-    for (int kb = 0; kb < 4; ++kb) {
-      const int it = hh * 4 + kb, buf = it & 1;
+    for (int kb = 0; kb < geo.nkb; ++kb) {
+      const int it = hh * geo.nkb + kb, buf = it & 1;
       const uint32_t col = kTmemS + 32 * buf;
       if (!mbar_wait(&s.s_full[buf], (it >> 1) & 1, abort_flag, args.status)) return false;
       tc_fence_after();
-      const int jbase = 32 * kb;
+      const int jbase = 32 * kb;                   // the block's first key, tile-local
+      const int jg0 = geo.ks + jbase;              // and global
       uint32_t pk[16];
-      if (row_max >= jbase) {
+      if (jg0 + 31 >= csw && jg0 <= rw1) {
         if (fast) {
           // branch-free: every key is evaluated (two per packed instruction),
           // the causal mask is a select; 16 keys per tensor-memory load
@@ -1202,26 +1300,33 @@ __device__ bool intra_worker(IntraSmem &s, const ReadArgs &args, int nh, int war
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 2) {
               const int j0 = jbase + 16 * half + jj;
+              const int jg = geo.ks + j0;
               const float2 kp = kappa2_g<G>(
                   kc, make_float2(__uint_as_float(sv[jj]), __uint_as_float(sv[jj + 1])), qt,
-                  &s.kt[hh][0][j0]);
-              pk[8 * half + (jj >> 1)] = pack_bf16x2(j0 <= m ? kp.x : 0.f, j0 + 1 <= m ? kp.y : 0.f);
+                  &s.kt[hh][0][j0], kKeys);
+              pk[8 * half + (jj >> 1)] =
+                  pack_bf16x2((jg >= cs && jg <= i_tok) ? kp.x : 0.f,
+                              (jg + 1 >= cs && jg + 1 <= i_tok) ? kp.y : 0.f);
             }
           }
         } else {
-          uint32_t sv[32];
           uint32_t r0[16], r1[16];
           tmem_ld16(tmem_lane_addr(tb, warp, col), r0);
           tmem_ld16(tmem_lane_addr(tb, warp, col + 16), r1);
           tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) { sv[e] = r0[e]; sv[16 + e] = r1[e]; }
           float sl[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) sl[e] = __uint_as_float(sv[e]);
+          for (int e = 0; e < 16; ++e) {
+            sl[e] = __uint_as_float(r0[e]);
+            sl[16 + e] = __uint_as_float(r1[e]);
+          }
           float kl[32];
-          for (int jj = 0; jj < 32; ++jj)
-            kl[jj] = jbase + jj <= m ? kappa_generic(p, sl[jj], s.q[hh], s.k, m, jbase + jj) : 0.f;
+          for (int jj = 0; jj < 32; ++jj) {
+            const int jg = jg0 + jj;
+            kl[jj] = (jg >= cs && jg <= i_tok)
+                         ? kappa_generic(p, sl[jj], s.q[hh], s.k, m, jbase + jj)
+                         : 0.f;
+          }
 #pragma unroll
           for (int jj = 0; jj < 32; jj += 2) pk[jj >> 1] = pack_bf16x2(kl[jj], kl[jj + 1]);
         }
@@ -1251,24 +1356,24 @@ __device__ bool intra_worker(IntraSmem &s, const ReadArgs &args, int nh, int war
 }
 
 // ---------------------------------------------------------------- intra kernel
-// Intra-chunk part of Eq. (25): sum_{j in chunk, j <= i} kappa(q_i, k_j) u_j per
-// query row, written to workspace for the readout's epilogue.
 // Warps 0-3: kappa (thread = query row) and the epilogue; warp 4: UMMA issue
 // (s = Q K^T per 32-key block, then P.V) and tensor memory; warp 5: TMA.
 // Blocks per SM by register need: four for small G (the whole grid of a
-// 4096-token, 14-head chunking fits one wave from three up).
-template <int G>
-__global__ void __launch_bounds__(kIntraThreads, G <= 3 ? 4 : (G <= 5 ? 3 : 2))
+// 4096-token, 14-head chunking fits one wave from three up); the 256-key
+// tiles of C = 256 fit two by shared memory.
+template <int G, bool kWide>
+__global__ void __launch_bounds__(kIntraThreads, kWide ? 2 : (G <= 3 ? 4 : (G <= 5 ? 3 : 2)))
 tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, ReadArgs args) {
   extern __shared__ uint8_t smem_raw[];
-  IntraSmem &s = *reinterpret_cast<IntraSmem *>(smem_align1024(smem_raw));
-  const int hg = blockIdx.x, c = blockIdx.y, unit = blockIdx.z;
+  IntraSmem<kWide> &s = *reinterpret_cast<IntraSmem<kWide> *>(smem_align1024(smem_raw));
+  const int hg = blockIdx.x, t = blockIdx.y, unit = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bidx = unit / args.Hkv, kv = unit % args.Hkv;
   const int h0 = kv * args.rho + hg * kIntraNH;
   const int nh = min(kIntraNH, args.rho - hg * kIntraNH);
-  const int nsteps = 4 * nh;            // (head, 32-key block)
+  const IntraGeom geo = intra_geom(t, args.chunk);
+  const int nsteps = geo.nkb * nh;        // (head, 32-key block)
   constexpr int kIss = 4, kTma = 5;
   pdl_trigger();
 
@@ -1281,6 +1386,7 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       mbar_init(&s.s_free[i], 1);
     }
     mbar_init(&s.d_full, 1);
+    mbar_init(&s.never, 1);
     fence_mbar_init();
   }
   if (warp == kIss) {
@@ -1308,7 +1414,7 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       const uint64_t kdesc0 = sdesc_sw128(smem_u32(s.k), 16, 1024);
       const uint64_t vdesc0 = sdesc_sw128(smem_u32(s.v), 16, 1024);
       auto issue_s = [&](int it) {
-        const int hh = it >> 2, kb = it & 3;
+        const int hh = it / geo.nkb, kb = it % geo.nkb;
         const uint64_t qd = qdesc0 + kQStep * hh;
         const uint64_t kd = kdesc0 + (uint64_t)((32 * kb * 128) >> 4);
         const uint32_t dt = tb + kTmemS + 32 * (it & 1);
@@ -1318,7 +1424,8 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         umma_ss(dt, qd + 6, kd + 6, id32k, 1u);
         umma_commit(&s.s_full[it & 1]);
       };
-      bool ok = mbar_wait(&s.qkv_full, 0, abort_flag, args.status);
+      const bool starve = args.status[1] == kStarveIntra;   // failure-path test only
+      bool ok = mbar_wait(starve ? &s.never : &s.qkv_full, 0, abort_flag, args.status);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -1327,7 +1434,7 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       for (int it = 0; it < nsteps && ok; ++it) {
         if (!mbar_wait(&s.p_full[it & 1], (it >> 1) & 1, abort_flag, args.status)) break;
         tc_fence_after();
-        const int hh = it >> 2, kb = it & 3;
+        const int hh = it / geo.nkb, kb = it % geo.nkb;
         const uint32_t at = tb + kTmemS + 32 * (it & 1);
         const uint64_t vd = vdesc0 + (uint64_t)((32 * kb * 128) >> 4);
         const uint32_t dt = tb + kTmemI + 64 * hh;
@@ -1347,20 +1454,23 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   } else if (warp == kTma) {
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
-      mbar_arrive_expect_tx(&s.qkv_full, (uint32_t)(nh + 2) * kC * 64 * 2);
+      const int nkh = geo.nkb / 4;   // 128-key boxes
+      mbar_arrive_expect_tx(&s.qkv_full, (uint32_t)(nh + 2 * nkh) * kC * 64 * 2);
       for (int hh = 0; hh < nh; ++hh)
-        tma_load_3d(s.q[hh], &tmQ, &s.qkv_full, 0, c * kC, bidx * args.Hq + h0 + hh);
-      tma_load_3d(s.k, &tmK, &s.qkv_full, 0, c * kC, unit);
-      tma_load_3d(s.v, &tmV, &s.qkv_full, 0, c * kC, unit);
+        tma_load_3d(s.q[hh], &tmQ, &s.qkv_full, 0, geo.row0, bidx * args.Hq + h0 + hh);
+      for (int x = 0; x < nkh; ++x) {
+        tma_load_3d(s.k + x * kC * 64, &tmK, &s.qkv_full, 0, geo.ks + kC * x, unit);
+        tma_load_3d(s.v + x * kC * 64, &tmV, &s.qkv_full, 0, geo.ks + kC * x, unit);
+      }
       mbar_wait_teardown(&s.qkv_full, 0, args.status);
     }
     __syncwarp();
   } else {
     // warps 0-3: kappa, then the numerators and denominators to workspace
     float den_intra[kIntraNH] = {0.f};
-    const bool ok = intra_worker<G>(s, args, nh, warp, lane, tb, den_intra);
+    const bool ok = intra_worker<G, kWide>(s, args, geo, nh, warp, lane, tb, den_intra);
     const int m = tid;
-    const int i_tok = c * kC + m;
+    const int i_tok = geo.row0 + m;
     if (ok && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
       tc_fence_after();
       for (int hh = 0; hh < nh; ++hh) {
@@ -1407,12 +1517,16 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 //        slot shows that the MMAs reading a stage are complete
 //   4    UMMA issuer (warp-uniform loop, elected lane), tensor memory owner,
 //        loads the first snapshot K blocks
-__global__ void __launch_bounds__(kReadThreads, 3)
+template <int NS>
+__global__ void __launch_bounds__(kReadThreads, NS == 1 ? 3 : 2)
 tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS,
                   ReadArgs args) {
   extern __shared__ uint8_t smem_raw[];
-  ReadSmem &s = *reinterpret_cast<ReadSmem *>(smem_align1024(smem_raw));
-  const int hg = blockIdx.x, c = blockIdx.y, unit = blockIdx.z;
+  ReadSmem<NS> &s = *reinterpret_cast<ReadSmem<NS> *>(smem_align1024(smem_raw));
+  const int hg = blockIdx.x, c = blockIdx.y, unit = blockIdx.z;   // c: 128-row tile
+  // snapshot read by the tile: the state before its chunk (C = 64: the
+  // states before each of its two chunks)
+  const int snap0 = NS == 2 ? 2 * c : (args.chunk == 256 ? c >> 1 : c);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bidx = unit / args.Hkv, kv = unit % args.Hkv;
   const int h0 = kv * args.rho + hg * args.nh_per_block;
@@ -1428,6 +1542,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     s.loaded = min(kNB, kNKB);          // the issuer loads the first kNB K blocks
 
     mbar_init(&s.d_full, nh);           // every head's issuer done
+    mbar_init(&s.never, 1);
     fence_mbar_init();
     // Q is an input of the call that no kernel of it writes: its load starts
     // before the wait on the previous kernels
@@ -1438,7 +1553,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       tma_load_3d(s.q[h], &tmQ, &s.qkv_full, 0, c * kC, bidx * args.Hq + h0 + h);
   }
   if (warp == kIss0) {
-    tmem_alloc(&s.tmem_base, kReadTmemCols);
+    tmem_alloc(&s.tmem_base, kReadTmemCols<NS>);
     tmem_relinquish();
   }
   pdl_wait();   // weights, snapshots and intra rows of the previous kernels
@@ -1466,8 +1581,12 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   // snapshot K block kb2 into its stage (one thread)
   auto load_block = [&](int kb2) {
     const int st2 = kb2 % kNB;
-    mbar_arrive_expect_tx(&s.b_full[st2], kN * 64 * 2);
-    tma_load_3d(s.b[st2], &tmS, &s.b_full[st2], 64 * kb2, 0, unit * args.nC + c);
+    mbar_arrive_expect_tx(&s.b_full[st2], NS * kN * 64 * 2);
+#pragma unroll
+    for (int x = 0; x < NS; ++x)   // (past the last chunk: another unit's rows or zero fill,
+                                   //  read only for rows past T)
+      tma_load_3d(s.b[st2] + x * kN * 64, &tmS, &s.b_full[st2], 64 * kb2, 0,
+                  unit * args.nC + snap0 + x);
   };
 
   if (warp >= kIss0) {
@@ -1477,9 +1596,9 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       // The whole warp runs the loop (warp-uniform; an elected lane issues:
       // an issuing loop under a one-lane branch is several times slower).
       // Head 0's warp also loads the first kNB snapshot K blocks by TMA.
-      const uint32_t id80 = idesc_bf16_f32(128, kN, 0);
+      const uint32_t id80 = idesc_bf16_f32(128, NS * kN, 0);
       const uint64_t bdesc0 = sdesc_sw128(smem_u32(s.b[0]), 16, 1024);
-      constexpr uint64_t kStageStep = (kN * 64 * 2) >> 4;   // one snapshot stage
+      constexpr uint64_t kStageStep = (NS * kN * 64 * 2) >> 4;   // one snapshot stage
       const uint32_t dt = tb + kTmemD + 80 * hh;
       const bool tma = hh == 0;
       // the first kNB K blocks; the builders load the rest as stages free up
@@ -1492,8 +1611,10 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       int st = 0, sph = 0;                       // snapshot stage and its phase
       int hs = 0;                                // first half slot of K block kb: (2 kb) % nhs
       int fk = 0, fph = 0;                       // kb % fper and the phase of (kb / fper)
+      const bool starve = args.status[1] == kStarveReadout;   // failure-path test only
       for (int kb = 0; kb < kNKB; ++kb) {
-        if (!mbar_wait(&s.b_full[st], sph, abort_flag, args.status)) break;
+        if (!mbar_wait(starve && kb == 0 ? &s.never : &s.b_full[st], sph, abort_flag, args.status))
+          break;
         const uint64_t bd = bdesc0 + kStageStep * st;
         // K block kb: halves of K = 32 in half slots (2 kb) % nhs and
         // (2 kb + 1) % nhs of this head (the last block: one half of K = 16);
@@ -1501,7 +1622,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const int hs1 = hs + 1 == nhs ? 0 : hs + 1;
         if (!mbar_wait(&s.a_full[a0 + hs], fph, abort_flag, args.status)) break;
         tc_fence_after();
-        const uint32_t at0 = tb + kTmemA + 16 * (a0 + hs), at1 = tb + kTmemA + 16 * (a0 + hs1);
+        const uint32_t at0 = tb + kTmemA<NS> + 16 * (a0 + hs), at1 = tb + kTmemA<NS> + 16 * (a0 + hs1);
         if (kb != kNKB - 1) {
           umma_ts_warp(dt, at0, bd, id80, kb > 0 ? 1u : 0u);
           umma_ts_warp(dt, at0 + 8, bd + 2, id80, 1u);
@@ -1606,8 +1727,8 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             s.loaded = nxt + 1;
           }
         }
-        const uint32_t ta0 = tmem_lane_addr(tb, warp, kTmemA + 16 * (a0 + hs));
-        const uint32_t ta1 = tmem_lane_addr(tb, warp, kTmemA + 16 * (a0 + hs1));
+        const uint32_t ta0 = tmem_lane_addr(tb, warp, kTmemA<NS> + 16 * (a0 + hs));
+        const uint32_t ta1 = tmem_lane_addr(tb, warp, kTmemA<NS> + 16 * (a0 + hs1));
         tmem_st16(ta0, out0);
         if (two) {
           if (!mbar_test(e1, par1) && !mbar_wait(e1, par1, abort_flag, args.status)) break;
@@ -1625,6 +1746,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         uph ^= (1u << hs) | (two ? 1u << hs1 : 0u);
         hs = hs1 + 1 == nhs ? 0 : hs1 + 1;
       }
+      tmem_wait_st();   // (a loop left early may have a store in flight)
     }
     if (hh < nh) {
       // ---------------- epilogue of head hh: y = (u~ + intra)[0:64] / (u~ + intra)[64].
@@ -1640,16 +1762,18 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 #pragma unroll
       for (int e = 0; e < 16; ++e) nv[e] = row_ok ? __ldg(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
       if (row_ok) iden = __ldg(args.intra_den + row);
+      // this row's columns of D: the second snapshot's (80 ..) for rows 64..127 when NS = 2
+      const int dcol = kTmemD + 80 * hh + ((NS == 2 && m >= 64) ? kN : 0);
       if (!*abort_flag && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
         tc_fence_after();
         uint32_t r[16];
-        tmem_ld16(tmem_lane_addr(tb, warp, kTmemD + 80 * hh + 64), r);
+        tmem_ld16(tmem_lane_addr(tb, warp, dcol + 64), r);
         tmem_wait_ld();
         const float inv = 1.0f / (__uint_as_float(r[0]) + iden);
         uint4 *dst = reinterpret_cast<uint4 *>(args.Y + row * kDv);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          tmem_ld16(tmem_lane_addr(tb, warp, kTmemD + 80 * hh + 16 * q4), r);
+          tmem_ld16(tmem_lane_addr(tb, warp, dcol + 16 * q4), r);
           tmem_wait_ld();
           uint32_t pk[8];
 #pragma unroll
@@ -1678,7 +1802,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         mbar_wait_teardown(&s.b_full[kb % kNB], (kb / kNB) & 1, args.status);
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tb, kReadTmemCols);
+    tmem_dealloc(tb, kReadTmemCols<NS>);
   }
 }
 
@@ -1712,18 +1836,23 @@ static bool make_map3(CUtensorMap *m, const void *ptr, uint64_t nx, uint64_t ny,
 }
 
 struct Layout {
-  int nC, nparts, cpp, U;
+  int nS, nC, nparts, spp, U;
   size_t snap_off, ptot_off, coef_off, plan_off, inum_off, iden_off, kt_off, total;
 };
 
-static Layout plan_layout(int B, int Hq, int Hkv, int T) {
+// Workspace of one call: the sequence splits into parts of spp 128-token
+// stages (whole chunks), as many as give one state block per SM.
+static Layout plan_layout(int B, int Hq, int Hkv, int T, int chunk) {
   Layout L{};
   L.U = B * Hkv;
-  L.nC = (T + kC - 1) / kC;
-  int P = 152 / (kTiles * L.U);   // one wave: every CTA walks its part once
-  P = P < 1 ? 1 : (P > L.nC ? L.nC : P);
-  L.cpp = (L.nC + P - 1) / P;
-  L.nparts = (L.nC + L.cpp - 1) / L.cpp;
+  L.nS = (T + kC - 1) / kC;
+  L.nC = (T + chunk - 1) / chunk;
+  const int spc = chunk == 256 ? 2 : 1;    // stages per chunk (at least one)
+  int P = 152 / (kTiles * L.U);            // one wave: every CTA walks its part once
+  P = P < 1 ? 1 : (P > L.nS ? L.nS : P);
+  L.spp = (L.nS + P - 1) / P;
+  L.spp = (L.spp + spc - 1) / spc * spc;
+  L.nparts = (L.nS + L.spp - 1) / L.spp;
   auto al = [](size_t x) { return (x + 1023) & ~size_t(1023); };
   size_t o = 0;
   L.snap_off = o; o = al(o + (size_t)L.U * L.nC * kSnapBytes);
@@ -1732,46 +1861,48 @@ static Layout plan_layout(int B, int Hq, int Hkv, int T) {
   L.plan_off = o; o = al(o + (size_t)Hq * sizeof(KPlan));
   L.inum_off = o; o = al(o + (size_t)B * Hq * T * 64 * sizeof(float));
   L.iden_off = o; o = al(o + (size_t)B * Hq * T * sizeof(float));
-  L.kt_off = o; o = al(o + (size_t)L.U * 64 * L.nC * kC * 2);
+  L.kt_off = o; o = al(o + (size_t)L.U * 64 * L.nS * kC * 2);
   L.total = o;
   return L;
 }
 
 using IntraKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, ReadArgs);
+template <bool kWide>
 static IntraKernel intra_kernel_for(int G) {
   switch (G) {
-    case 1: return tc_intra_kernel<1>;
-    case 2: return tc_intra_kernel<2>;
-    case 3: return tc_intra_kernel<3>;
-    case 4: return tc_intra_kernel<4>;
-    case 5: return tc_intra_kernel<5>;
-    case 6: return tc_intra_kernel<6>;
-    default: return tc_intra_kernel<7>;
+    case 1: return tc_intra_kernel<1, kWide>;
+    case 2: return tc_intra_kernel<2, kWide>;
+    case 3: return tc_intra_kernel<3, kWide>;
+    case 4: return tc_intra_kernel<4, kWide>;
+    case 5: return tc_intra_kernel<5, kWide>;
+    case 6: return tc_intra_kernel<6, kWide>;
+    default: return tc_intra_kernel<7, kWide>;
   }
 }
 
 }  // namespace tcp
 
-size_t tc_prefill_workspace_bytes(int B, int Hq, int Hkv, int T) {
-  return tcp::plan_layout(B, Hq, Hkv, T).total;
+size_t tc_prefill_workspace_bytes(int B, int Hq, int Hkv, int T, int chunk) {
+  return tcp::plan_layout(B, Hq, Hkv, T, chunk).total;
 }
 
 oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B, int Hq,
                              int Hkv, int T, const float *L, const int32_t *group, int G,
                              float eps, const float *a, const float *b, const float *C,
-                             int packed, float *state, int cont, void *Y, void *ws,
+                             int packed, float *state, int cont, void *Y, int chunk, void *ws,
                              cudaStream_t stream) {
   using namespace tcp;
-  const Layout lay = plan_layout(B, Hq, Hkv, T);
+  const Layout lay = plan_layout(B, Hq, Hkv, T, chunk);
   uint8_t *w = static_cast<uint8_t *>(ws);
   __nv_bfloat16 *snap = reinterpret_cast<__nv_bfloat16 *>(w + lay.snap_off);
   float *ptot = reinterpret_cast<float *>(w + lay.ptot_off);
   __nv_bfloat16 *coef = reinterpret_cast<__nv_bfloat16 *>(w + lay.coef_off);
   KPlan *plans = reinterpret_cast<KPlan *>(w + lay.plan_off);
   int *status = oal_device_status_word();
+  if (!status) return oal_fail(OAL_ERR_CUDA, "prefill: device status word unavailable");
 
   CUtensorMap tmQ, tmK, tmKn, tmV, tmS;
-  const int Tpad = lay.nC * kC;
+  const int Tpad = lay.nS * kC;
   __nv_bfloat16 *Kt = reinterpret_cast<__nv_bfloat16 *>(w + lay.kt_off);
   const uint64_t rowb = 64 * 2;
   if (!make_map3(&tmQ, Q, 64, T, (uint64_t)B * Hq, rowb, rowb * T, kC) ||
@@ -1785,8 +1916,8 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
 
   KtArgs kta;
   kta.K = static_cast<const __nv_bfloat16 *>(K); kta.Kt = Kt;
-  kta.T = T; kta.Tpad = Tpad; kta.U = lay.U; kta.nC = lay.nC;
-  const int ntiles = lay.U * lay.nC;
+  kta.T = T; kta.Tpad = Tpad; kta.U = lay.U; kta.nC = lay.nS;
+  const int ntiles = lay.U * lay.nS;
   const int ntr = (std::min(ntiles, 2 * 152) + Hq - 1) / Hq;   // block rows of transposes
   launch_pdl(tc_prep_kernel, dim3(Hq, (kKP + 255) / 256 + 2 + ntr), dim3(kPrepThreads), 0, stream, a, b, C,
              L, group, G, eps, packed, coef, plans, status, kta);
@@ -1794,32 +1925,50 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   if (st != OAL_OK) return st;
 
   const size_t ssmem = sizeof(StateSmem) + 1024;
-  const size_t rsmem = sizeof(ReadSmem) + 1024;
-  const size_t ismem = sizeof(IntraSmem) + 1024;
+  const size_t rsmem1 = sizeof(ReadSmem<1>) + 1024;
+  const size_t rsmem2 = sizeof(ReadSmem<2>) + 1024;
+  const size_t ismem = sizeof(IntraSmem<false>) + 1024;
+  const size_t ismem_w = sizeof(IntraSmem<true>) + 1024;
   // shared-memory limits above 48 KB: a function attribute of each device
-  static bool attr_set[256] = {};
+  static std::mutex attr_mutex;
+  static bool attr_set[kMaxDevices] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256)
-    return oal_fail(OAL_ERR_CUDA, "prefill: no current device");
-  if (!attr_set[dev]) {
-    bool ok = cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)ssmem) == cudaSuccess &&
-              cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)rsmem) == cudaSuccess &&
-              cudaFuncSetAttribute(tc_readout_kernel,
-                                   cudaFuncAttributePreferredSharedMemoryCarveout,
-                                   100) == cudaSuccess;
-    for (int g = 1; ok && g <= kMaxG; ++g)
-      ok = cudaFuncSetAttribute(intra_kernel_for(g), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)ismem) == cudaSuccess;
-    if (!ok) {
-      cudaGetLastError();   // reported here, not by the next launch
-      return oal_fail(OAL_ERR_CUDA, "prefill: setting the shared memory limit failed");
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return oal_fail(OAL_ERR_CUDA, "prefill: no current device below ordinal %d", kMaxDevices);
+  {
+    std::lock_guard<std::mutex> lock(attr_mutex);
+    if (!attr_set[dev]) {
+      bool ok =
+          cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)ssmem) == cudaSuccess &&
+          cudaFuncSetAttribute(tc_readout_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)rsmem1) == cudaSuccess &&
+          cudaFuncSetAttribute(tc_readout_kernel<1>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout, 100) ==
+              cudaSuccess &&
+          cudaFuncSetAttribute(tc_readout_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)rsmem2) == cudaSuccess &&
+          cudaFuncSetAttribute(tc_readout_kernel<2>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout, 100) ==
+              cudaSuccess &&
+          true;
+      for (int g = 1; ok && g <= kMaxG; ++g)
+        ok = cudaFuncSetAttribute(intra_kernel_for<false>(g),
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)ismem) == cudaSuccess &&
+             cudaFuncSetAttribute(intra_kernel_for<true>(g),
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)ismem_w) == cudaSuccess;
+      if (!ok) {
+        cudaGetLastError();   // reported here, not by the next launch
+        return oal_fail(OAL_ERR_CUDA, "prefill: setting the shared memory limit failed");
+      }
+      attr_set[dev] = true;
     }
-    attr_set[dev] = true;
   }
   StateArgs sa;
-  sa.T = T; sa.nC = lay.nC; sa.U = lay.U; sa.cpp = lay.cpp; sa.nparts = lay.nparts;
+  sa.T = T; sa.nS = lay.nS; sa.chunk = chunk; sa.nC = lay.nC; sa.spp = lay.spp;
+  sa.U = lay.U; sa.nparts = lay.nparts;
   sa.packed = packed; sa.cont = cont; sa.state_in = state; sa.state_out = state;
   sa.ptot = ptot; sa.snap = snap; sa.status = status;
   if (lay.nparts > 1) {
@@ -1836,18 +1985,27 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   if (st != OAL_OK) return st;
 
   ReadArgs ra;
-  ra.T = T; ra.nC = lay.nC; ra.Hq = Hq; ra.Hkv = Hkv; ra.rho = Hq / Hkv;
-  ra.nh_per_block = kMaxNH;
+  ra.T = T; ra.nC = lay.nC; ra.chunk = chunk; ra.Hq = Hq; ra.Hkv = Hkv; ra.rho = Hq / Hkv;
   ra.Y = static_cast<__nv_bfloat16 *>(Y);
   ra.coef = coef; ra.plans = plans; ra.status = status;
   ra.intra_num = reinterpret_cast<float *>(w + lay.inum_off);
   ra.intra_den = reinterpret_cast<float *>(w + lay.iden_off);
-  dim3 gi((ra.rho + kIntraNH - 1) / kIntraNH, lay.nC, lay.U);
-  launch_pdl(intra_kernel_for(G), gi, dim3(kIntraThreads), ismem, stream, tmQ, tmKn, tmV, ra);
+  ra.nh_per_block = kIntraNH;
+  dim3 gi((ra.rho + kIntraNH - 1) / kIntraNH, lay.nS, lay.U);
+  if (chunk == 256)
+    launch_pdl(intra_kernel_for<true>(G), gi, dim3(kIntraThreads), ismem_w, stream, tmQ, tmKn, tmV,
+               ra);
+  else
+    launch_pdl(intra_kernel_for<false>(G), gi, dim3(kIntraThreads), ismem, stream, tmQ, tmKn, tmV,
+               ra);
   st = oal_after_launch("tc_intra_kernel", stream);
   if (st != OAL_OK) return st;
-  dim3 g2((ra.rho + kMaxNH - 1) / kMaxNH, lay.nC, lay.U);
-  launch_pdl(tc_readout_kernel, g2, dim3(kReadThreads), rsmem, stream, tmQ, tmS, ra);
+  ra.nh_per_block = kMaxNH;
+  dim3 g2((ra.rho + kMaxNH - 1) / kMaxNH, lay.nS, lay.U);
+  if (chunk == 64)
+    launch_pdl(tc_readout_kernel<2>, g2, dim3(kReadThreads), rsmem2, stream, tmQ, tmS, ra);
+  else
+    launch_pdl(tc_readout_kernel<1>, g2, dim3(kReadThreads), rsmem1, stream, tmQ, tmS, ra);
   return oal_after_launch("tc_readout_kernel", stream);
 }
 

@@ -75,8 +75,20 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity.  `abort` is a block-wide
-// flag in shared memory; `status` the device status word (may be null).
+// flag in shared memory; `status` the device status word (may be null).  The
+// limit is kWaitLimitCycles, or the 64-bit word 8 bytes after the status word
+// when that is non-zero (set by oal_debug_wait_test for tests of this path).
+// That word is read only once a wait has lasted kWaitFloorCycles, so ordinary
+// waits never touch global memory; test limits below the floor act as the floor.
 constexpr uint64_t kWaitLimitCycles = 1ull << 32;  // about 2 s
+constexpr uint64_t kWaitFloorCycles = 1ull << 20;  // about 0.5 ms
+__device__ __forceinline__ uint64_t wait_limit(const int *status) {
+  if (status) {
+    const uint64_t v = *reinterpret_cast<const volatile uint64_t *>(status + 2);
+    if (v) return v;
+  }
+  return kWaitLimitCycles;
+}
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           volatile int *abort, int *status) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -84,7 +96,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (cycles_now() - t0 > kWaitLimitCycles) {
+    const uint64_t el = cycles_now() - t0;
+    if (el > kWaitFloorCycles && el > wait_limit(status)) {
       *abort = 1;
       if (status) atomicCAS(status, 0, 4 /* OAL_ERR_TIMEOUT */);
       return false;

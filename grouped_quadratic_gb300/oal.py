@@ -74,6 +74,10 @@ def load_library(path: str = LIB_PATH):
     lib.oal_group_dims.restype = ci
     lib.oal_sync_status.argtypes = [vp]
     lib.oal_sync_status.restype = ci
+    lib.oal_debug_wait_test.argtypes = [ctypes.c_uint64, ci]
+    lib.oal_debug_wait_test.restype = ci
+    lib.oal_prefill_noalloc_scratch_bytes.argtypes = []
+    lib.oal_prefill_noalloc_scratch_bytes.restype = sz
     lib.oal_last_error.argtypes = []
     lib.oal_last_error.restype = ctypes.c_char_p
     lib.oal_version.argtypes = []
@@ -187,8 +191,9 @@ def oal_prefill(Q, K, V, L, group, eps, a, b, C, layout=OAL_STATE_FULL, state=No
     return Y, state
 
 
-# Size of the library's fixed prefill scratch (OAL_PREFILL_NOALLOC_SCRATCH_BYTES).
-OAL_PREFILL_NOALLOC_SCRATCH_BYTES = 64 << 20
+def oal_prefill_noalloc_scratch_bytes():
+    """Size of the library's fixed prefill scratch array, read from the library."""
+    return int(load_library().oal_prefill_noalloc_scratch_bytes())
 
 
 def oal_prefill_noalloc(Q, K, V, L, group, eps, a, b, C, state, Y, layout=OAL_STATE_FULL,
@@ -197,7 +202,7 @@ def oal_prefill_noalloc(Q, K, V, L, group, eps, a, b, C, state, Y, layout=OAL_ST
 
     For callers that cannot allocate device memory: `state` and `Y` must be
     passed in, and this wrapper allocates nothing either.  Problems whose
-    workspace would exceed OAL_PREFILL_NOALLOC_SCRATCH_BYTES are rejected.
+    workspace would exceed oal_prefill_noalloc_scratch_bytes() are rejected.
     """
     lib = load_library()
     B, Hq, T, d = Q.shape
@@ -281,6 +286,14 @@ def oal_group_dims(chi_p, boot_idx, alpha, tau, gamma, g_min, eps=1e-12):
 def oal_sync_status(stream=None):
     lib = load_library()
     _check(lib.oal_sync_status(_stream(stream)))
+
+
+def oal_debug_wait_test(wait_limit_cycles=0, starve=0):
+    """Test-only: the limit of the kernels' bounded waits in SM cycles (0: the
+    built-in limit) and the prefill kernel whose UMMA issuer waits on a barrier
+    nothing arrives on (0 none, 1 readout, 2 state, 3 intra-chunk), for kernels
+    launched afterwards on the current device.  (0, 0) restores normal operation."""
+    _check(load_library().oal_debug_wait_test(int(wait_limit_cycles), int(starve)))
 
 
 def oal_last_error():

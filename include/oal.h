@@ -31,6 +31,9 @@
  *  - Supported sizes: d == dv == 64, 1 <= G <= 7.  Other values return
  *    OAL_ERR_UNSUPPORTED.
  *  - On error, oal_last_error() returns a message for the calling thread.
+ *  - Per device (ordinals 0..255) the library caches the addresses of its
+ *    device globals and the function attributes it set; do not keep using
+ *    the library on a device after cudaDeviceReset() on it.
  */
 #ifndef OAL_H
 #define OAL_H
@@ -108,12 +111,16 @@ oal_status oal_expand_coeffs(const float *L, const int32_t *group, int Hq,
  *    token T-1.  continue_from_state != 0 starts from the values in `state`
  *    (resume after an earlier prefill or decode); 0 starts from zero.
  *  Y [B][Hq][T][dv] in `dtype` (bf16 outputs are rounded once from fp32).
- *  chunk: 0 (default) or one of 64, 128, 256.
+ *  chunk: 0 (default: 128 for bf16, 64 for fp32) or one of 64, 128, 256
+ *    tokens: the period of the inter-chunk states.
  *  workspace: device scratch of at least oal_prefill_workspace_bytes(...)
  *    bytes, 256-byte aligned; contents need not be initialised.
  * Arithmetic: OAL_F32 inputs use fp32 CUDA-core FMA throughout.  OAL_BF16
- * inputs use bf16 tensor-core products with fp32 accumulation and fp32
- * states (the state snapshots read by the readout are rounded to bf16).
+ * inputs, at every chunk size, use bf16 tensor-core products with fp32
+ * accumulation and fp32 states (exact products phi(k) split into two bf16
+ * terms; the state snapshots read by the readout and the intra-chunk
+ * kernel values are rounded to bf16, the scaled queries of the intra-chunk
+ * factors w_c too).
  * T == 0 leaves Y untouched and sets `state` to zero unless
  * continue_from_state != 0.
  */
@@ -160,6 +167,8 @@ oal_status oal_prefill(const void *Q, const void *K, const void *V,
  *    oal_prefill.
  */
 #define OAL_PREFILL_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+/* The size of that array in this build of the library, in bytes. */
+size_t oal_prefill_noalloc_scratch_bytes(void);
 oal_status oal_prefill_noalloc(const void *Q, const void *K, const void *V,
                                oal_dtype dtype, int B, int Hq, int Hkv, int T,
                                int d, int dv, const float *L,
@@ -250,6 +259,28 @@ oal_status oal_group_dims(const float *chi_p, int P, int d, const int32_t *boot_
  * OAL_ERR_CUDA if the synchronisation itself failed.
  */
 oal_status oal_sync_status(cudaStream_t stream);
+
+/*
+ * oal_debug_wait_test -- for tests of the failure path only (the paper has
+ * no counterpart).  Every wait of the library's kernels on an mbarrier (a
+ * copy landing, a tensor-core product completing, another warp's tile) is
+ * bounded: past the limit the block raises its abort flag, records
+ * OAL_ERR_TIMEOUT in the device status word, drains the copies and products
+ * it has in flight, frees its tensor memory and returns.  For kernels
+ * launched afterwards on the current device this call sets
+ *  wait_limit_cycles  that limit in SM cycles (0: the built-in 2^32 cycles,
+ *                     about 2 s; the limit is consulted once a wait has
+ *                     lasted 2^20 cycles, so smaller values act as 2^20);
+ *  starve             0: nothing; 1, 2, 3: the UMMA issuer of the prefill's
+ *                     readout, state or intra-chunk kernel makes its first
+ *                     wait on a barrier that nothing arrives on, so that wait
+ *                     runs out after the limit and the other warps of the
+ *                     block abort mid-pipeline.
+ * A starved prefill leaves Y and the state unspecified, and the next
+ * oal_sync_status() returns OAL_ERR_TIMEOUT.  (0, 0) restores normal
+ * operation.  Synchronous; call it while none of the library's kernels runs.
+ */
+oal_status oal_debug_wait_test(uint64_t wait_limit_cycles, int starve);
 
 /*
  * Launch accounting and per-kernel timing, for benchmarks and tracing.

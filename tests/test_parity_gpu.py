@@ -118,10 +118,14 @@ def sampled_rows(w, n_first=64, n_rand=64, n_last=16, seed=0):
     return np.concatenate(rows)
 
 
-@pytest.mark.parametrize("cfg,layout", [(1, FULL), (1, PACKED), (2, PACKED), (4, PACKED)])
-def test_prefill_full_size_sampled(oal, cfg, layout):
+@pytest.mark.parametrize("cfg,layout,chunk", [(1, FULL, 0), (1, PACKED, 0), (2, PACKED, 0),
+                                              (4, PACKED, 0), (4, PACKED, 64),
+                                              (4, PACKED, 256)])
+def test_prefill_full_size_sampled(oal, cfg, layout, chunk):
+    """Full-size workloads (the long-context one at every chunk size), output
+    rows sampled at the start, at random and at the end of every head."""
     w = inputs.config(cfg)
-    Y, _ = run_prefill(oal, w, layout)
+    Y, _ = run_prefill(oal, w, layout, chunk)
     rows = sampled_rows(w, n_rand=32 if cfg == 2 else 64, n_last=8 if cfg == 2 else 16)
     want = oracle.direct(w.Q, w.K, w.V, w.L, w.group, w.eps, rows=rows)
     got = Y.reshape(-1, w.dv)[rows]
@@ -225,6 +229,41 @@ def test_decode_equals_longer_prefill(oal):
     got = torch.stack(ys, 2).cpu().numpy()
     assert rel_l2(got, Yfull[:, :, 67:].cpu().numpy()) <= 1e-5
     assert rel_l2(S.cpu().numpy(), Sfull.cpu().numpy()) <= 1e-6
+
+
+def test_decode_config3_all_steps(oal):
+    """Decode workload (B=64, Hq=14, Hkv=2, G=4, full fp32 state): a 2048-token
+    prefill, then all 1024 decode steps.  Every step's output of 8 of the 64
+    sequences (all 14 heads) is compared with the oracle's direct sum over
+    all tokens up to that step, and the states of those sequences after the
+    last step with the oracle's recurrence over all 3072 tokens, so drift in
+    the long fp32 accumulation would show."""
+    w = inputs.config(3)
+    Q, K, V = w.torch_inputs("cuda")
+    L, group, a, b, C = dev_params(oal, w, FULL)
+    Tp, steps = w.T_prefill, w.decode_steps
+    _, S = oal.oal_prefill(Q[:, :, :Tp].contiguous(), K[:, :, :Tp].contiguous(),
+                           V[:, :, :Tp].contiguous(), L, group, w.eps, a, b, C, FULL)
+    qd, kd, vd = (t[:, :, Tp:].permute(2, 0, 1, 3).contiguous() for t in (Q, K, V))
+    del Q, K, V
+    y = torch.empty(steps, w.B, w.Hq, 64, dtype=qd.dtype, device="cuda")
+    ws = torch.empty(oal.oal_decode_workspace_bytes(w.B, w.Hq, w.Hkv, layout=FULL),
+                     dtype=torch.uint8, device="cuda")
+    for t in range(steps):
+        oal.oal_decode_step(qd[t], kd[t], vd[t], a, b, C, S, FULL, y=y[t], workspace=ws)
+    oal.oal_sync_status()
+    got = y.float().permute(1, 2, 0, 3).cpu().numpy()           # [B, Hq, steps, 64]
+    bsel = np.sort(np.random.default_rng(2).choice(w.B, 8, replace=False))
+    rows = np.concatenate([((b * w.Hq + h) * w.T + Tp + np.arange(steps))
+                           for b in bsel for h in range(w.Hq)])
+    want = oracle.direct(w.Q, w.K, w.V, w.L, w.group, w.eps, rows=rows)
+    assert np.all(np.isfinite(got))
+    assert rel_l2(got[bsel].reshape(-1, 64), want) <= TOL["bf16"]
+    # the states depend on K and V only: one query head per KV head suffices
+    rho = w.Hq // w.Hkv
+    _, S_ref = oracle.recurrent(w.Q[bsel][:, ::rho], w.K[bsel], w.V[bsel], w.L[::rho],
+                                w.group[::rho], w.eps)
+    assert rel_l2(S.cpu().numpy()[bsel], S_ref) <= 1e-5
 
 
 def test_decode_config3_sampled(oal):

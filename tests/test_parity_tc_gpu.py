@@ -3,14 +3,15 @@
 Each case runs through the C ABI and is compared with the fp64 oracle:
 outputs at rel-L2 <= 2e-2 (bf16 inputs, fp32 states), states at <= 1e-5 (the
 state contraction is exact up to fp32 accumulation).  The cases cover what the
-Qwen/Llama-shaped workloads do not: every group count the library accepts, a
-tail group wider than two dims (the generic kappa path), readout weights
-without the rank-one form or with exception words at the first and last
-rows (the general and the patched builder paths), GQA ratios 1 to 8, a
-sequence split into many parts, continuation through the tensor-core path,
-chunk-boundary lengths, heads of different group counts in one launch
-(empty groups), and both decode reductions (thread-block clusters
-for few sequences, persistent streaming blocks and a finishing kernel for many).
+Qwen/Llama-shaped workloads do not: every group count the library accepts
+(G = 1 is the single global embedding) at every chunk size (64, 128, 256),
+wide tail groups, readout weights without the rank-one form or with exception
+words at the first and last rows (the general and the patched builder paths),
+GQA ratios 1 to 8, sequences split into many parts, continuation through the
+tensor-core path, lengths around every chunk and tile boundary, heads of
+different group counts in one launch (empty groups), and both decode
+reductions (thread-block clusters for few sequences, persistent streaming
+blocks and a finishing kernel for many).
 """
 import numpy as np
 import pytest
@@ -46,10 +47,10 @@ def params(oal, w, layout):
     return L, group, a, b, C
 
 
-def check_prefill(oal, w, layout=PACKED):
+def check_prefill(oal, w, layout=PACKED, chunk=128):
     Q, K, V = w.torch_inputs("cuda")
     L, group, a, b, C = params(oal, w, layout)
-    Y, S = oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, layout, chunk=128)
+    Y, S = oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, layout, chunk=chunk)
     oal.oal_sync_status()
     Yh = Y.float().cpu().numpy()
     assert np.isfinite(Yh).all()
@@ -61,19 +62,23 @@ def check_prefill(oal, w, layout=PACKED):
     assert rel_l2(S.cpu().numpy(), S_ref) <= TOL_S
 
 
-@pytest.mark.parametrize("G", [1, 2, 5, 6, 7])
-def test_tc_prefill_every_group_count(oal, G):
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 7])
+def test_tc_prefill_every_group_count(oal, G, chunk):
     w = inputs.make_workload("tc-G%d" % G, B=1, Hq=4, Hkv=2, T=300, G=G, seed=300 + G)
-    check_prefill(oal, w)
+    check_prefill(oal, w, chunk=chunk)
 
 
-def test_tc_prefill_wide_tail_group(oal):
-    # tail group {3, 17, 40} has three dims: the intra-chunk kappa takes the
-    # generic path (sums straight from the tiles)
+@pytest.mark.parametrize("chunk", [64, 256])
+def test_tc_prefill_wide_tail_group(oal, chunk):
+    # tail group {3, 17, 40} has three dims, the bulk group is not group 1
     w = inputs.make_workload("tc-wide", B=1, Hq=4, Hkv=2, T=260, G=3, seed=311,
                              fixed_outliers=([3, 17, 40, 58], 12.0),
                              fixed_groups=[[3, 17, 40], [58]])
-    check_prefill(oal, w)
+    w.group[w.group == 1] = 4
+    w.group[w.group == 3] = 1
+    w.group[w.group == 4] = 3
+    check_prefill(oal, w, chunk=chunk)
 
 
 def test_tc_prefill_readout_general_weights(oal):
@@ -115,6 +120,9 @@ def test_prefill_heterogeneous_group_counts(oal, dtype):
         w.group[h][w.group[h] > 1 + h % 5] = 1
     check_prefill(oal, w)
     check_prefill(oal, w, FULL)
+    if dtype == "bf16":
+        check_prefill(oal, w, chunk=64)
+        check_prefill(oal, w, FULL, chunk=256)
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (6, 3), (8, 2), (16, 2)])
@@ -123,18 +131,21 @@ def test_tc_prefill_gqa_ratios(oal, Hq, Hkv):
     check_prefill(oal, w, FULL if Hq == 6 else PACKED)
 
 
-@pytest.mark.parametrize("T", [1, 127, 128, 129, 256])
-def test_tc_prefill_chunk_boundaries(oal, T):
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 127, 128, 129, 255, 256, 257, 383])
+def test_tc_prefill_chunk_boundaries(oal, T, chunk):
     w = inputs.make_workload("tc-T", B=1, Hq=2, Hkv=1, T=T, G=4, seed=330 + T)
-    check_prefill(oal, w)
+    check_prefill(oal, w, chunk=chunk)
 
 
-def test_tc_prefill_many_parts(oal):
-    # one (batch, KV head): the state walk splits 20 chunks into 7 parts of 3
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+def test_tc_prefill_many_parts(oal, chunk):
+    # one (batch, KV head): the state walk splits 20 stages of 128 tokens
+    # into parts of 3 (C = 64, 128) or 4 (C = 256) stages
     w = inputs.make_workload("tc-parts", B=1, Hq=2, Hkv=1, T=20 * 128 - 37, G=4, seed=340)
     Q, K, V = w.torch_inputs("cuda")
     L, group, a, b, C = params(oal, w, PACKED)
-    Y, S = oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, PACKED, chunk=128)
+    Y, S = oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, PACKED, chunk=chunk)
     oal.oal_sync_status()
     _, S_ref = oracle.recurrent(w.Q, w.K, w.V, w.L, w.group, w.eps)
     assert rel_l2(S.cpu().numpy(), oracle.full_to_packed_state(S_ref, 64)) <= TOL_S
@@ -144,18 +155,19 @@ def test_tc_prefill_many_parts(oal):
     assert rel_l2(got, want) <= TOL_Y
 
 
-@pytest.mark.parametrize("layout", [FULL, PACKED])
-def test_tc_prefill_continuation(oal, layout):
+@pytest.mark.parametrize("layout,chunk", [(FULL, 128), (PACKED, 128), (PACKED, 64),
+                                          (FULL, 256)])
+def test_tc_prefill_continuation(oal, layout, chunk):
     w = inputs.make_workload("tc-cont", B=2, Hq=4, Hkv=2, T=500, G=4, seed=350)
     Q, K, V = w.torch_inputs("cuda")
     L, group, a, b, C = params(oal, w, layout)
     T1 = 200
     Y1, S = oal.oal_prefill(Q[:, :, :T1].contiguous(), K[:, :, :T1].contiguous(),
                             V[:, :, :T1].contiguous(), L, group, w.eps, a, b, C, layout,
-                            chunk=128)
+                            chunk=chunk)
     Y2, S = oal.oal_prefill(Q[:, :, T1:].contiguous(), K[:, :, T1:].contiguous(),
                             V[:, :, T1:].contiguous(), L, group, w.eps, a, b, C, layout,
-                            state=S, continue_from_state=True, chunk=128)
+                            state=S, continue_from_state=True, chunk=chunk)
     oal.oal_sync_status()
     got = torch.cat([Y1, Y2], 2).float().cpu().numpy()
     want = oracle.direct(w.Q, w.K, w.V, w.L, w.group, w.eps)

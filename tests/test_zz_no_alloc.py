@@ -3,9 +3,10 @@
 oal_prefill_noalloc serves callers that cannot allocate device memory when
 they run a prefill (a host framework that owns all device memory, a runtime
 that forbids allocation after start-up): it uses the library's own fixed
-scratch array instead of a caller workspace.  These checks run two calls in a
-row with different inputs and sizes, so a result that leaned on what an
-earlier call left in the shared array would show up, and compare each with
+scratch array instead of a caller workspace.  Each check first fills that
+array with NaN (a call on all-NaN inputs), then runs calls in a row with
+different inputs, sizes and chunk sizes, so a result that leaned on what an
+earlier call left in the shared array would show up, and compares each with
 oal_prefill on the same inputs at the parity tolerances of the other GPU
 tests (rel-L2 2e-2 for bf16 outputs, 1e-5 for fp32 outputs and for states).
 
@@ -54,17 +55,63 @@ def both_ways(oal, w, layout, chunk=0):
             Y_ref.float().cpu().numpy(), S_ref.cpu().numpy())
 
 
-@pytest.mark.parametrize("dtype,layout", [("bf16", PACKED), ("f32", FULL)])
-def test_noalloc_matches_prefill_on_two_calls(oal, dtype, layout):
+def poison_scratch(oal):
+    """One call whose inputs are all NaN: every scratch byte it writes holds
+    NaN afterwards (its outputs are ignored), so a later call that read
+    scratch it had not written first would produce non-finite or wrong values.
+    Its second half uses the fp32 kernels, whose scratch layout differs."""
+    for dtype in ("bf16", "f32"):
+        w = inputs.make_workload("noalloc-poison", B=2, Hq=8, Hkv=2, T=520, G=4, seed=70,
+                                 dtype=dtype)
+        Q, K, V = (torch.full_like(t, float("nan")) for t in w.torch_inputs("cuda"))
+        L = torch.from_numpy(w.L).cuda()
+        group = torch.from_numpy(w.group).cuda()
+        a, b, C = oal.oal_expand_coeffs(L, group, w.eps, PACKED)
+        S = torch.zeros(w.B, w.Hkv, oal.oal_state_rows(64, PACKED), 65, device="cuda")
+        Y = torch.empty_like(Q)
+        oal.oal_prefill_noalloc(Q, K, V, L, group, w.eps, a, b, C, S, Y, PACKED,
+                                chunk=64 if dtype == "f32" else 0)
+        oal.oal_sync_status()
+
+
+@pytest.mark.parametrize("dtype,layout,chunk", [("bf16", PACKED, 0), ("f32", FULL, 0),
+                                                ("f32", PACKED, 256), ("bf16", PACKED, 64)])
+def test_noalloc_matches_prefill_on_two_calls(oal, dtype, layout, chunk):
+    poison_scratch(oal)
     first = inputs.make_workload("noalloc-a", B=2, Hq=8, Hkv=2, T=333, G=4, seed=71,
                                  dtype=dtype)
     second = inputs.make_workload("noalloc-b", B=1, Hq=4, Hkv=1, T=200, G=3, seed=72,
                                   dtype=dtype)
     for w in (first, second):
-        Y, S, Y_ref, S_ref = both_ways(oal, w, layout)
+        Y, S, Y_ref, S_ref = both_ways(oal, w, layout, chunk)
         assert np.isfinite(Y).all() and np.isfinite(S).all()
         assert rel_l2(Y, Y_ref) <= TOL[dtype]
         assert rel_l2(S, S_ref) <= 1e-5
+
+
+def test_noalloc_continuation_matches_prefill(oal):
+    """A prefill in two calls, the second continuing from the first's state."""
+    poison_scratch(oal)
+    w = inputs.make_workload("noalloc-cont", B=2, Hq=4, Hkv=2, T=300, G=3, seed=73)
+    Q, K, V = w.torch_inputs("cuda")
+    L = torch.from_numpy(w.L).cuda()
+    group = torch.from_numpy(w.group).cuda()
+    a, b, C = oal.oal_expand_coeffs(L, group, w.eps, PACKED)
+    T1 = 170
+    parts = [(t[:, :, :T1].contiguous(), t[:, :, T1:].contiguous()) for t in (Q, K, V)]
+    Y_ref, S_ref = oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, PACKED)
+    S = torch.zeros_like(S_ref)
+    Y1 = torch.empty_like(parts[0][0])
+    Y2 = torch.empty_like(parts[0][1])
+    oal.oal_prefill_noalloc(parts[0][0], parts[1][0], parts[2][0], L, group, w.eps, a, b, C,
+                            S, Y1, PACKED)
+    oal.oal_prefill_noalloc(parts[0][1], parts[1][1], parts[2][1], L, group, w.eps, a, b, C,
+                            S, Y2, PACKED, continue_from_state=True)
+    oal.oal_sync_status()
+    got = torch.cat([Y1, Y2], 2).float().cpu().numpy()
+    assert np.isfinite(got).all()
+    assert rel_l2(got, Y_ref.float().cpu().numpy()) <= TOL["bf16"]
+    assert rel_l2(S.cpu().numpy(), S_ref.cpu().numpy()) <= 1e-5
 
 
 def test_noalloc_rejects_problems_above_its_scratch(oal):
@@ -72,7 +119,7 @@ def test_noalloc_rejects_problems_above_its_scratch(oal):
     # the shortest sequence whose scratch need is above the fixed array
     T = 128
     while oal.oal_prefill_workspace_bytes(B, Hq, Hkv, T, dtype=oal.OAL_BF16,
-                                          layout=PACKED) <= oal.OAL_PREFILL_NOALLOC_SCRATCH_BYTES:
+                                          layout=PACKED) <= oal.oal_prefill_noalloc_scratch_bytes():
         T += 128
     need = oal.oal_prefill_workspace_bytes(B, Hq, Hkv, T, dtype=oal.OAL_BF16, layout=PACKED)
     z = lambda *shape, dt=torch.bfloat16: torch.zeros(*shape, dtype=dt, device="cuda")
