@@ -25,6 +25,8 @@ The JSON line also carries:
                 G=4) measured the same way;
   config4       the long-context prefill (B=1, Hq=14, Hkv=2, T=65536, G=4) at
                 chunk sizes 64, 128 and 256;
+  backward      the prefill backward (dQ, dK, dV, dL) on the Qwen-shaped
+                workload;
   decode        the decode workload (B=64, Hq=14, Hkv=2, 1024 steps after a
                 2048-token prefill): steps/s and achieved HBM bandwidth for the
                 full fp32 state (4161 x 65 per KV head) and the packed one;
@@ -187,6 +189,8 @@ def oracle_sample(w, target_s, max_rows=None):
     import oracle
     total_rows = w.B * w.Hq * w.T_prefill
     probe = np.arange(0, total_rows, max(1, total_rows // 64))
+    oracle.direct(w.Q[:, :, :w.T_prefill], w.K[:, :, :w.T_prefill], w.V[:, :, :w.T_prefill],
+                  w.L, w.group, w.eps, rows=probe[:4])   # load and thread start-up, untimed
     t0 = time.perf_counter()
     oracle.direct(w.Q[:, :, :w.T_prefill], w.K[:, :, :w.T_prefill], w.V[:, :, :w.T_prefill],
                   w.L, w.group, w.eps, rows=probe)
@@ -592,6 +596,7 @@ def run_ours(args, world, rank, local):
         decode = {lay: run_decode(args, world, dev, stream, lib, pks, lay)
                   for lay in ("full", "packed")}
     calib = run_contribution(args, world, dev, stream, lib, pks) if args.contribution else None
+    backward = None if args.no_backward else run_backward(args, world, dev, stream, lib, pks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -605,6 +610,8 @@ def run_ours(args, world, rank, local):
             "e2e": head.get("e2e"), "gpu_launches": head["gpu_launches"],
             "clocks": clk.summary(), "decode": decode, "peaks_source": pks["source"]}
     line.update(subs)
+    if backward is not None:
+        line["backward"] = backward
     if calib is not None:
         line["calibration"] = calib
     line["config"]["launch"] = "one step captured as a CUDA graph, replayed per timed step"
@@ -652,6 +659,60 @@ def run_contribution(args, world, dev, stream, lib, pks):
             "ms_per_call": 1e3 * secs,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / pks["hbm_gbs"], "algorithmic_bytes_per_call": nbytes},
+            "gpu_launches": int(launches)}
+
+
+def run_backward(args, world, dev, stream, lib, pks):
+    """Prefill backward (dQ, dK, dV, dL) on the Qwen2.5-0.5B-shaped workload."""
+    import torch
+    from grouped_quadratic_gb300 import inputs, oal
+    w = inputs.config(1)
+    Q, K, V = w.torch_inputs(dev)
+    g = torch.Generator(device="cpu").manual_seed(20261011)
+    dY = torch.randn(Q.shape, generator=g).to(Q.dtype).to(dev)
+    L = torch.from_numpy(w.L).to(dev)
+    group = torch.from_numpy(w.group).to(dev)
+    dQ = torch.empty(Q.shape, dtype=torch.float32, device=dev)
+    dK = torch.empty(K.shape, dtype=torch.float32, device=dev)
+    dV = torch.empty(V.shape, dtype=torch.float32, device=dev)
+    dL = torch.empty(w.L.shape, dtype=torch.float32, device=dev)
+    ws = torch.empty(oal.oal_prefill_backward_workspace_bytes(w.B, w.Hq, w.Hkv, w.T),
+                     dtype=torch.uint8, device=dev)
+
+    def call():
+        oal.oal_prefill_backward(Q, K, V, dY, L, group, w.eps, dQ, dK, dV, dL, workspace=ws,
+                                 stream=stream)
+
+    for _ in range(2):
+        call()
+    oal.oal_sync_status()
+    n = 3
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    c0 = lib.oal_launch_counter()
+    e0.record(stream)
+    for _ in range(n):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = lib.oal_launch_counter() - c0
+    oal.oal_sync_status()
+    secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world) / n
+    pairs = w.B * w.Hq * w.T * (w.T + 1) / 2
+    # per causal pair: the group sums, dY . v, dQ, dK and dV (5 x 64 multiply-adds) and
+    # the recomputed forward numerator and group sums (2 x 64): 7 x 128 FLOPs
+    flops = pairs * 7 * 128
+    achieved = flops / secs / 1e12
+    return {"workload": "qwen2.5-0.5b-prefill backward B%d Hq%d Hkv%d T%d d64 G%d bf16 "
+                        "(dQ, dK, dV, dL)" % (w.B, w.Hq, w.Hkv, w.T, w.G),
+            "ms_per_call": 1e3 * secs, "tokens_per_s": world * w.B * w.T / secs,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_SIMT_PEAK_TFLOPS,
+                         "unit": "TFLOP/s", "frac": achieved / FP32_SIMT_PEAK_TFLOPS,
+                         "peak_source": "fp32 CUDA-core FMA peak: 152 SMs x 128 lanes x 2 x "
+                                        "2.07 GHz",
+                         "algorithmic_flops_per_call": flops},
             "gpu_launches": int(launches)}
 
 
@@ -733,6 +794,7 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1024)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-sub", action="store_true",
                     help="skip the config-1 and config-4 sub-lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")

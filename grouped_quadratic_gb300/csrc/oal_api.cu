@@ -31,6 +31,12 @@ oal_status launch_decode(const void *q, const void *k, const void *v, int is_bf1
                          int Hq, int Hkv, const float *a, const float *b, const float *C,
                          int packed, float *state, void *y, void *ws, cudaStream_t stream);
 
+size_t backward_workspace_bytes(int B, int Hq, int Hkv, int T);
+oal_status launch_backward(const void *Q, const void *K, const void *V, const void *dY, int is_bf16,
+                           int B, int Hq, int Hkv, int T, const float *L, const int32_t *group,
+                           int G, float eps, float *dQ, float *dK, float *dV, float *dL, void *ws,
+                           cudaStream_t stream);
+
 size_t contrib_workspace_bytes(int P, int Hq, int Hkv, int T);
 oal_status launch_contrib(const void *Q, const void *K, int is_bf16, int P, int Hq, int Hkv,
                           int T, const int32_t *lengths, float *chi, void *ws,
@@ -277,6 +283,51 @@ oal_status oal_prefill(const void *Q, const void *K, const void *V, oal_dtype dt
   return oal::launch_prefill_simt(Q, K, V, dtype == OAL_BF16, B, Hq, Hkv, T, L, group, G,
                                   eps, a, b, C, packed, state, continue_from_state != 0,
                                   Y, chunk, workspace, stream);
+}
+
+size_t oal_prefill_backward_workspace_bytes(int B, int Hq, int Hkv, int T, int d, int dv) {
+  if (check_common(B, Hq, Hkv, d, dv, OAL_F32, OAL_STATE_FULL) != OAL_OK || T < 0) return 0;
+  if (B == 0 || T == 0) return 256;
+  return oal::backward_workspace_bytes(B, Hq, Hkv, T);
+}
+
+oal_status oal_prefill_backward(const void *Q, const void *K, const void *V, const void *dY,
+                                oal_dtype dtype, int B, int Hq, int Hkv, int T, int d, int dv,
+                                const float *L, const int32_t *group, int G, float eps, float *dQ,
+                                float *dK, float *dV, float *dL, void *workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  t_msg[0] = 0;
+  OAL_TRY(check_common(B, Hq, Hkv, d, dv, dtype, OAL_STATE_FULL));
+  if (T < 0) return oal_fail(OAL_ERR_INVALID_ARG, "T=%d", T);
+  if (G < 1 || G > oal::kMaxG)
+    return oal_fail(OAL_ERR_UNSUPPORTED, "G=%d outside 1..%d", G, oal::kMaxG);
+  if (!(eps > 0.f)) return oal_fail(OAL_ERR_INVALID_ARG, "eps must be > 0 (got %g)", eps);
+  OAL_TRY(check_ptr(L, "L"));
+  OAL_TRY(check_ptr(group, "group"));
+  OAL_TRY(check_ptr(dL, "dL"));
+  t_call_launches = 0;
+  if (B == 0 || T == 0) {   // no pairs: every gradient is zero (dQ, dK, dV are empty)
+    const size_t bytes = (size_t)Hq * (G + 1) * (G + 1) * sizeof(float);
+    if (cudaMemsetAsync(dL, 0, bytes, stream) != cudaSuccess) return oal_check_launch("dL reset");
+    return OAL_OK;
+  }
+  OAL_TRY(check_ptr(Q, "Q"));
+  OAL_TRY(check_ptr(K, "K"));
+  OAL_TRY(check_ptr(V, "V"));
+  OAL_TRY(check_ptr(dY, "dY"));
+  OAL_TRY(check_ptr(dQ, "dQ"));
+  OAL_TRY(check_ptr(dK, "dK"));
+  OAL_TRY(check_ptr(dV, "dV"));
+  OAL_TRY(check_ptr(workspace, "workspace"));
+  if (((uintptr_t)workspace & 255u) != 0)
+    return oal_fail(OAL_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  const size_t need = oal_prefill_backward_workspace_bytes(B, Hq, Hkv, T, d, dv);
+  if (workspace_bytes < need)
+    return oal_fail(OAL_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes",
+                    workspace_bytes, need);
+  oal_begin_call(stream);
+  return oal::launch_backward(Q, K, V, dY, dtype == OAL_BF16, B, Hq, Hkv, T, L, group, G, eps, dQ,
+                              dK, dV, dL, workspace, stream);
 }
 
 size_t oal_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int dv,

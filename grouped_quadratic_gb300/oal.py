@@ -60,6 +60,11 @@ def load_library(path: str = LIB_PATH):
     lib.oal_prefill_noalloc.argtypes = ([vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, vp, vp, ci,
                                          cf, vp, vp, vp, ci, vp, ci, vp, ci, vp])
     lib.oal_prefill_noalloc.restype = ci
+    lib.oal_prefill_backward_workspace_bytes.argtypes = [ci] * 6
+    lib.oal_prefill_backward_workspace_bytes.restype = sz
+    lib.oal_prefill_backward.argtypes = ([vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, vp, vp, ci,
+                                          cf, vp, vp, vp, vp, vp, sz, vp])
+    lib.oal_prefill_backward.restype = ci
     lib.oal_decode_workspace_bytes.argtypes = [ci] * 5 + [ci]
     lib.oal_decode_workspace_bytes.restype = sz
     lib.oal_decode_step.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, ci,
@@ -215,6 +220,38 @@ def oal_prefill_noalloc(Q, K, V, L, group, eps, a, b, C, state, Y, layout=OAL_ST
                                    int(bool(continue_from_state)), _ptr(Y), chunk,
                                    _stream(stream)))
     return Y, state
+
+
+def oal_prefill_backward_workspace_bytes(B, Hq, Hkv, T, d=64, dv=64):
+    return int(load_library().oal_prefill_backward_workspace_bytes(B, Hq, Hkv, T, d, dv))
+
+
+def oal_prefill_backward(Q, K, V, dY, L, group, eps, dQ=None, dK=None, dV=None, dL=None,
+                         workspace=None, stream=None):
+    """Gradients of <dY, Y> for Y = oal_prefill(Q, K, V, L, group, eps).
+    Returns (dQ, dK, dV, dL), fp32."""
+    lib = load_library()
+    B, Hq, T, d = Q.shape
+    Hkv, dv = K.shape[1], V.shape[3]
+    G = L.shape[1] - 1
+    dev = Q.device
+    f32 = torch.float32
+    dQ = torch.empty(B, Hq, T, d, dtype=f32, device=dev) if dQ is None else dQ
+    dK = torch.empty(B, Hkv, T, d, dtype=f32, device=dev) if dK is None else dK
+    dV = torch.empty(B, Hkv, T, dv, dtype=f32, device=dev) if dV is None else dV
+    dL = torch.empty(Hq, G + 1, G + 1, dtype=f32, device=dev) if dL is None else dL
+    if workspace is None:
+        need = lib.oal_prefill_backward_workspace_bytes(B, Hq, Hkv, T, d, dv)
+        workspace = torch.empty(max(int(need), 256), dtype=torch.uint8, device=dev)
+    if dY.dtype != Q.dtype:
+        raise OALError(OAL_ERR_INVALID_ARG, "dY must have the dtype of Q")
+    _need_cuda(Q, K, V, dY, L, group, dQ, dK, dV, dL, workspace)
+    _check(lib.oal_prefill_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(dY), _dtype_code(Q), B, Hq,
+                                    Hkv, T, d, dv, _ptr(L), _ptr(group), G, float(eps), _ptr(dQ),
+                                    _ptr(dK), _ptr(dV), _ptr(dL), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream(stream)))
+    return dQ, dK, dV, dL
 
 
 def oal_decode_workspace_bytes(B, Hq, Hkv, d=64, dv=64, layout=OAL_STATE_FULL):

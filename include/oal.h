@@ -179,6 +179,37 @@ oal_status oal_prefill_noalloc(const void *Q, const void *K, const void *V,
                                cudaStream_t stream);
 
 /*
+ * oal_prefill_backward -- gradients of <dY, Y> for the causal prefill output
+ * Y = oal_prefill(Q, K, V, L, group, eps): the step that the coefficient
+ * calibration by output matching ([OAL] App. B, Eq. (20)) and the LoRA
+ * adaptation ([OAL] Sec. 5.2) differentiate through.  With g_ij =
+ * dY_i . (v_j - y_i) / D_i for j <= i (D_i the normaliser of row i):
+ *     dV_j = sum_{i>=j} kappa_ij dY_i / D_i,
+ *     dQ_ir = sum_j 2 g_ij (M s_bar_ij)_{g(r)} k_jr / sqrt(d),
+ *     dK_jr = sum_i 2 g_ij (M s_bar_ij)_{g(r)} q_ir / sqrt(d),
+ *     dL = lower((dM + dM^T) L),  dM = sum_ij g_ij s_bar_ij s_bar_ij^T,
+ * key/value gradients summed over the query heads sharing the KV head.
+ *  Q, K, V, dY: as for oal_prefill (dY [B][Hq][T][dv] in `dtype`).
+ *  L, group, G, eps: the kernel parameters of the forward call.
+ *  dQ [B][Hq][T][d], dK [B][Hkv][T][d], dV [B][Hkv][T][dv],
+ *  dL [Hq][G+1][G+1] (zero above the diagonal): fp32 outputs.
+ *  workspace: at least oal_prefill_backward_workspace_bytes(...) bytes,
+ *    256-byte aligned, contents need not be initialised.
+ * Arithmetic: fp32 on the CUDA cores, every pair formed explicitly
+ * (O(T^2 d) per head); the forward normalisers are recomputed, so the call
+ * needs no saved forward state.  Deterministic: no atomics on the outputs.
+ * B == 0 or T == 0 writes dL = 0 and nothing else.
+ */
+size_t oal_prefill_backward_workspace_bytes(int B, int Hq, int Hkv, int T, int d, int dv);
+oal_status oal_prefill_backward(const void *Q, const void *K, const void *V,
+                                const void *dY, oal_dtype dtype, int B, int Hq,
+                                int Hkv, int T, int d, int dv, const float *L,
+                                const int32_t *group, int G, float eps,
+                                float *dQ, float *dK, float *dV, float *dL,
+                                void *workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
+
+/*
  * oal_decode_step -- one token of [OAL] Algorithm 1 (state update and readout) for every
  * sequence: u = [v; 1]; H0 += u; H1_r += k_r u; H2_rt += k_r k_t u; then the
  * Eq. (6) readout for each query head of the KV head (inclusive: the new
