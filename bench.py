@@ -27,6 +27,8 @@ The JSON line also carries:
                 chunk sizes 64, 128 and 256;
   backward      the prefill backward (dQ, dK, dV, dL) on the Qwen-shaped
                 workload;
+  group_counts  prefill time per head on the Qwen shape for one global group
+                (G = 1), five groups, and heads of 1 to 5 groups in one launch;
   decode        the decode workload (B=64, Hq=14, Hkv=2, 1024 steps after a
                 2048-token prefill): steps/s and achieved HBM bandwidth for the
                 full fp32 state (4161 x 65 per KV head) and the packed one;
@@ -597,6 +599,7 @@ def run_ours(args, world, rank, local):
                   for lay in ("full", "packed")}
     calib = run_contribution(args, world, dev, stream, lib, pks) if args.contribution else None
     backward = None if args.no_backward else run_backward(args, world, dev, stream, lib, pks)
+    groups = None if args.no_sub else run_group_counts(args, world, dev, stream, lib, pks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -612,6 +615,8 @@ def run_ours(args, world, rank, local):
     line.update(subs)
     if backward is not None:
         line["backward"] = backward
+    if groups is not None:
+        line["group_counts"] = groups
     if calib is not None:
         line["calibration"] = calib
     line["config"]["launch"] = "one step captured as a CUDA graph, replayed per timed step"
@@ -660,6 +665,57 @@ def run_contribution(args, world, dev, stream, lib, pks):
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / pks["hbm_gbs"], "algorithmic_bytes_per_call": nbytes},
             "gpu_launches": int(launches)}
+
+
+def run_group_counts(args, world, dev, stream, lib, pks):
+    """Prefill time per head on the Qwen2.5-0.5B shape (B=1, Hq=14, Hkv=2,
+    T=4096, bf16) for one global group (G = 1), the grouped kernel at G = 5, and
+    a launch of G = 5 where heads keep 1 to 5 groups (the others empty)."""
+    import torch
+    from grouped_quadratic_gb300 import inputs, oal
+    out = {}
+    for name, G, mixed in (("G1", 1, False), ("G5", 5, False), ("G5_mixed_1_to_5", 5, True)):
+        w = inputs.make_workload("qwen-shape G%d" % G, B=1, Hq=14, Hkv=2, T=4096, G=G,
+                                 seed=inputs.SEED_BASE + 20 + G)
+        if mixed:
+            for h in range(w.Hq):
+                w.group[h][w.group[h] > 1 + h % 5] = 1
+        Q, K, V = w.torch_inputs(dev)
+        L = torch.from_numpy(w.L).to(dev)
+        group = torch.from_numpy(w.group).to(dev)
+        layout = oal.OAL_STATE_PACKED
+        a, b, C = oal.oal_expand_coeffs(L, group, w.eps, layout)
+        state = torch.empty(w.B, w.Hkv, oal.oal_state_rows(D, layout), U, device=dev)
+        Y = torch.empty_like(Q)
+        ws = torch.empty(oal.oal_prefill_workspace_bytes(w.B, w.Hq, w.Hkv, w.T, layout=layout),
+                         dtype=torch.uint8, device=dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+        def call():
+            oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, layout, state=state, Y=Y,
+                            workspace=ws, stream=stream)
+
+        for _ in range(3):
+            call()
+        oal.oal_sync_status()
+        n = max(3, args.steps)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        barrier(world)
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            call()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        oal.oal_sync_status()
+        ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+        out[name] = {"ms_per_call": ms, "us_per_head": 1e3 * ms / w.Hq,
+                     "tokens_per_s": w.B * w.T / (ms / 1e3)}
+        del Q, K, V, ws, flush
+        torch.cuda.empty_cache()
+    out["workload"] = "qwen2.5-0.5b-shaped prefill B1 Hq14 Hkv2 T4096 bf16, packed state"
+    return out
 
 
 def run_backward(args, world, dev, stream, lib, pks):

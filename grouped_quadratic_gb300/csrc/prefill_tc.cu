@@ -394,6 +394,15 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
   }
   auto Lat = [&](int g, int c) { return c <= g ? sL[g * G1 + c] : 0.f; };
   KPlan *P = plans + h;
+  // tail slots: the non-empty groups other than g*, in group order.  An empty
+  // group's sum is zero for every pair, so it takes no slot and the head's
+  // kappa is a quadratic form in 1 + (its non-empty tail groups) variables.
+  __shared__ int sslot[kMaxG + 1], sntg;
+  if (tid == 0) {
+    int n = 0;
+    for (int g = 1; g <= G; ++g) sslot[g] = (g != gstar && scnt[g] > 0) ? n++ : -1;
+    sntg = n;
+  }
   // first dims of each tail group, one thread per dim: its rank in its group
   // from the groups' ballots over the 64 dims
   __shared__ uint32_t sball[2][kMaxG + 1];
@@ -412,15 +421,15 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
   __syncthreads();
   if (tid < kD && sgrp[tid] != gstar) {
     const int r = tid, g = sgrp[r];
-    const int slot = g < gstar ? g - 1 : g - 2;
+    const int slot = sslot[g];
     const int k = (r < 32 ? 0 : __popc(sball[0][g])) +
                   __popc(sball[r >> 5][g] & ((1u << (r & 31)) - 1u));
     P->gdims[tail_off(g) + k] = r;
     if (k < 2) P->dims[slot][k] = r;
   }
-  if (tid >= 1 && tid <= G && tid != gstar) {
+  if (tid >= 1 && tid <= G && sslot[tid] >= 0) {
     const int g = tid;
-    const int slot = g < gstar ? g - 1 : g - 2;
+    const int slot = sslot[g];
     P->goff[slot] = tail_off(g);
     P->nd[slot] = scnt[g];
     if (scnt[g] < 2) P->dims[slot][1] = 0;
@@ -431,7 +440,7 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
     int fast = 1, tot = 0;
     for (int g = 1; g <= G; ++g)
       if (g != gstar) { fast &= scnt[g] <= 2; tot += scnt[g]; }
-    for (int slot = G - 1; slot < kMaxTailG; ++slot) {
+    for (int slot = sntg; slot < kMaxTailG; ++slot) {
       for (int c = 0; c < 8; ++c) P->beta[slot][c] = 0.f;
       P->nd[slot] = 0;
       P->dims[slot][0] = P->dims[slot][1] = 0;
@@ -439,7 +448,7 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
     }
     P->goff[kMaxTailG] = tot;
     for (int c = 0; c < 8; ++c) P->alpha[c] = c <= G ? Lat(gstar, c) * 0.125f : 0.f;
-    P->ntg = G - 1;
+    P->ntg = sntg;
     P->fast = fast;
     P->L00 = sL[0];
     P->eps = eps;
@@ -454,7 +463,7 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
   if (tid == 0) {
     int slot = 0;
     for (int g = 1; g <= G; ++g)
-      if (g != gstar) slot_group[++slot] = g;   // z index slot (1-based)
+      if (sslot[g] >= 0) slot_group[++slot] = g;   // z index slot (1-based)
   }
   if (tid < G1 * G1) {
     const int g = tid / G1, h2 = tid % G1;
@@ -470,10 +479,11 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
     gs[1] = slot_group[v]; as[1] = 0.125f;
     return 2;
   };
-  const int nq = G * (G + 1) / 2;
+  const int Ge = sntg + 1;   // variables of the quadratic form: s and the tail sums
+  const int nq = Ge * (Ge + 1) / 2;
   if (tid < nq) {
     int v = 0, rem = tid;
-    while (rem >= G - v) { rem -= G - v; ++v; }
+    while (rem >= Ge - v) { rem -= Ge - v; ++v; }
     const int w2 = v + rem;
     int gv[2], gw[2];
     float av[2], aw[2];
@@ -487,7 +497,7 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
   } else if (tid >= 64 && tid < 72) {
     const int v = tid - 64;
     float l = 0.f;
-    if (v < G) {
+    if (v < Ge) {
       int gv[2];
       float av[2];
       const int nv = deps(v, gv, av);
@@ -1355,6 +1365,17 @@ __device__ bool intra_worker(IntraSmem<kWide> &s, const ReadArgs &args, const In
   return true;
 }
 
+// The worker for a head of ge <= G variables (1 + its non-empty tail groups).
+template <int G, bool kWide>
+__device__ bool intra_dispatch(int ge, IntraSmem<kWide> &s, const ReadArgs &args,
+                               const IntraGeom &geo, int nh, int warp, int lane, uint32_t tb,
+                               float (&den_intra)[kIntraNH]) {
+  if constexpr (G > 1) {
+    if (ge < G) return intra_dispatch<G - 1, kWide>(ge, s, args, geo, nh, warp, lane, tb, den_intra);
+  }
+  return intra_worker<G, kWide>(s, args, geo, nh, warp, lane, tb, den_intra);
+}
+
 // ---------------------------------------------------------------- intra kernel
 // Warps 0-3: kappa (thread = query row) and the epilogue; warp 4: UMMA issue
 // (s = Q K^T per 32-key block, then P.V) and tensor memory; warp 5: TMA.
@@ -1466,9 +1487,11 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     __syncwarp();
   } else {
-    // warps 0-3: kappa, then the numerators and denominators to workspace
+    // warps 0-3: kappa, then the numerators and denominators to workspace; a
+    // head whose groups are partly empty takes the worker of its own size
     float den_intra[kIntraNH] = {0.f};
-    const bool ok = intra_worker<G, kWide>(s, args, geo, nh, warp, lane, tb, den_intra);
+    const bool ok = intra_dispatch<G, kWide>(s.plan[0].ntg + 1, s, args, geo, nh, warp, lane,
+                                             tb, den_intra);
     const int m = tid;
     const int i_tok = geo.row0 + m;
     if (ok && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
