@@ -71,7 +71,10 @@ CSRC = os.path.join(ROOT, "grouped_quadratic_gb300", "csrc")
 # the time of the capture.  A record is reported only while that source file
 # is unchanged (otherwise the traffic is null: the counters are stale).
 TRAFFIC = [
-    # (kernel, source file, workload key, bytes per launch, source sha256)
+    # (kernel, source file, workload key (B, Hq, Hkv, T, G, layout, chunk), bytes per
+    #  launch, source sha256)
+    ("tc_readout_kernel", "prefill_tc.cu", (4, 32, 8, 8192, 6, "packed", 128),
+     1000651520 + 121596416, "779dc6da4435133e0338f33d2babcfe2df491d9cc1f191b69de393502ce3a6f8"),
 ]
 
 
