@@ -7,11 +7,13 @@
 //     Kbar_{i,r} = sum_{j <= i} |k_{j,r}|,
 // a prefix sum over the tokens instead of the O(N^2) pair set.  One pass over
 // Q and K: HBM-bound.
-//   contrib_chunk_kernel   per (128-token chunk, KV head, prompt): the chunk's
-//                          |k| total A_c, and per query head of the KV head
-//                          Qs_c = sum_{i in c} |q_i| and
+//   contrib_chunk_kernel   per (query head, 128-token chunk, prompt): the
+//                          chunk's |k| total A_c (written by the first head
+//                          of each KV head), Qs_c = sum_{i in c} |q_i| and
 //                          W_c = sum_{i in c} |q_i| (inclusive |k| prefix
-//                          inside the chunk), per dim
+//                          inside the chunk), per dim.  Thread = 8 dims x a
+//                          run of 4 tokens, 16-byte loads; the run totals are
+//                          scanned across the chunk's 32 runs in shared memory
 //   contrib_finish_kernel  per (prompt, query head), thread = dim: walks the
 //                          chunks, sum_c W_c + Qs_c sum_{c' < c} A_c', and
 //                          divides by |Omega_p| sqrt(d)
@@ -26,12 +28,33 @@ namespace oal {
 namespace {
 
 constexpr int kCC = 128;               // tokens per chunk
-constexpr int kCThreads = 256;         // 64 dims x 4 token quarters of 32
-constexpr int kCQuarter = kCC / 4;
+constexpr int kCThreads = 256;         // 8 dim groups x 32 runs
+constexpr int kRun = 4;                // tokens of a thread's run
+constexpr int kRuns = kCC / kRun;
+constexpr int kRunPitch = kRuns + 1;   // [dim][run] in shared memory: conflict-free per dim
 
-template <typename Tin>
-__device__ __forceinline__ float absval(const Tin *p) {
-  return fabsf(to_f32(*p));
+// |x| of dims 8g .. 8g + 7 of one token row: one 16-byte load (bf16) or two (fp32).
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, bool ok, uint4 (&raw)[2]) {
+  raw[0] = ok ? __ldg(reinterpret_cast<const uint4 *>(p)) : make_uint4(0u, 0u, 0u, 0u);
+  raw[1] = make_uint4(0u, 0u, 0u, 0u);
+}
+__device__ __forceinline__ void load8(const float *p, bool ok, uint4 (&raw)[2]) {
+  raw[0] = ok ? __ldg(reinterpret_cast<const uint4 *>(p)) : make_uint4(0u, 0u, 0u, 0u);
+  raw[1] = ok ? __ldg(reinterpret_cast<const uint4 *>(p) + 1) : make_uint4(0u, 0u, 0u, 0u);
+}
+__device__ __forceinline__ void abs8(const uint4 (&raw)[2], __nv_bfloat16, float (&o)[8]) {
+  const uint32_t w[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    o[2 * e] = __uint_as_float((w[e] << 16) & 0x7FFFFFFFu);
+    o[2 * e + 1] = __uint_as_float(w[e] & 0x7FFF0000u);
+  }
+}
+__device__ __forceinline__ void abs8(const uint4 (&raw)[2], float, float (&o)[8]) {
+  const uint32_t w[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w,
+                         raw[1].x, raw[1].y, raw[1].z, raw[1].w};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(w[e] & 0x7FFFFFFFu);
 }
 
 // Prompt length, clamped to 0..T; a length outside records OAL_ERR_INVALID_ARG.
@@ -45,6 +68,8 @@ __device__ __forceinline__ int prompt_len(const int32_t *lengths, int p, int T, 
   return n;
 }
 
+// Query heads vary fastest in the grid, so the rho blocks that read one K
+// chunk run close together and share it through L2.
 template <typename Tin>
 __global__ void __launch_bounds__(kCThreads)
 contrib_chunk_kernel(const Tin *__restrict__ Q, const Tin *__restrict__ K,
@@ -53,50 +78,68 @@ contrib_chunk_kernel(const Tin *__restrict__ Q, const Tin *__restrict__ K,
                      int *status) {
   pdl_trigger();
   pdl_wait();
-  const int c = blockIdx.x, kv = blockIdx.y, p = blockIdx.z;
-  const int r = threadIdx.x & 63, qq = threadIdx.x >> 6;
-  const int rho = Hq / Hkv;
+  const int h = blockIdx.x, c = blockIdx.y, p = blockIdx.z;
+  const int rho = Hq / Hkv, kv = h / rho;
+  const int tid = threadIdx.x, g = tid & 7, run = tid >> 3;   // a warp: 8 groups x 4 runs
   const int n = prompt_len(lengths, p, T, status);
-  const int t0 = c * kCC + qq * kCQuarter;
-  __shared__ float sq[4][64], sw[4][64];
-  // |k| of this thread's 32 tokens, inclusive prefix inside the quarter
-  float pk[kCQuarter];
-  const Tin *kp = K + (((size_t)p * Hkv + kv) * T + t0) * 64 + r;
-  float run = 0.f;
+  const int t0 = c * kCC + run * kRun;   // first token of the run
+  __shared__ float s_off[64 * kRunPitch];             // run totals of |k|, then their prefixes
+  __shared__ float s_q[64 * kRunPitch], s_w[64 * kRunPitch];
+  const Tin *kp = K + (((size_t)p * Hkv + kv) * T + t0) * 64 + 8 * g;
+  const Tin *qp = Q + (((size_t)p * Hq + h) * T + t0) * 64 + 8 * g;
+  uint4 kr[kRun][2], qr[kRun][2];
 #pragma unroll
-  for (int i = 0; i < kCQuarter; ++i) {
-    run += (t0 + i < n) ? absval(kp + (size_t)i * 64) : 0.f;
-    pk[i] = run;
+  for (int i = 0; i < kRun; ++i) {   // every load of the thread in flight at once
+    load8(kp + (size_t)i * 64, t0 + i < n, kr[i]);
+    load8(qp + (size_t)i * 64, t0 + i < n, qr[i]);
   }
-  sq[qq][r] = run;
+  // inclusive |k| prefix inside the run
+  float pk[kRun][8];
+#pragma unroll
+  for (int i = 0; i < kRun; ++i) {
+    float a[8];
+    abs8(kr[i], Tin(), a);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) pk[i][e] = (i ? pk[i - 1][e] : 0.f) + a[e];
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) s_off[(8 * g + e) * kRunPitch + run] = pk[kRun - 1][e];
   __syncthreads();
-  float off = 0.f, tot = 0.f;   // |k| of the quarters before this one, of the chunk
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    off += j < qq ? sq[j][r] : 0.f;
-    tot += sq[j][r];
+  if (tid < 64) {
+    // exclusive prefix over the runs of dim tid; the total is the chunk's A_c
+    float acc = 0.f;
+    for (int j = 0; j < kRuns; ++j) {
+      const float v = s_off[tid * kRunPitch + j];
+      s_off[tid * kRunPitch + j] = acc;
+      acc += v;
+    }
+    if (h % rho == 0) A[(((size_t)p * Hkv + kv) * nC + c) * 64 + tid] = acc;
   }
-  const size_t cu = ((size_t)p * Hkv + kv) * nC + c;
-  if (qq == 0) A[cu * 64 + r] = tot;
-  for (int hh = 0; hh < rho; ++hh) {
-    const int h = kv * rho + hh;
-    const Tin *qp = Q + (((size_t)p * Hq + h) * T + t0) * 64 + r;
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float off = s_off[(8 * g + e) * kRunPitch + run];
     float qs = 0.f, w = 0.f;
 #pragma unroll
-    for (int i = 0; i < kCQuarter; ++i) {
-      const float a = (t0 + i < n) ? absval(qp + (size_t)i * 64) : 0.f;
-      qs += a;
-      w = fmaf(a, off + pk[i], w);
+    for (int i = 0; i < kRun; ++i) {
+      float a[8];
+      abs8(qr[i], Tin(), a);
+      qs += a[e];
+      w = fmaf(a[e], off + pk[i][e], w);
     }
-    __syncthreads();   // the previous head's sums are read
-    sq[qq][r] = qs;
-    sw[qq][r] = w;
-    __syncthreads();
-    if (qq == 0) {
-      const size_t ch = ((size_t)p * Hq + h) * nC + c;
-      Qs[ch * 64 + r] = sq[0][r] + sq[1][r] + sq[2][r] + sq[3][r];
-      W[ch * 64 + r] = sw[0][r] + sw[1][r] + sw[2][r] + sw[3][r];
-    }
+    s_q[(8 * g + e) * kRunPitch + run] = qs;
+    s_w[(8 * g + e) * kRunPitch + run] = w;
+  }
+  __syncthreads();
+  if (tid < 128) {
+    // the runs' sums per dim, in run order
+    const int r = tid & 63;
+    const float *src = (tid < 64 ? s_q : s_w) + r * kRunPitch;
+    float sum = 0.f;
+    for (int j = 0; j < kRuns; ++j) sum += src[j];
+    const size_t ch = (((size_t)p * Hq + h) * nC + c) * 64 + r;
+    if (tid < 64) Qs[ch] = sum;
+    else W[ch] = sum;
   }
 }
 
@@ -139,7 +182,7 @@ oal_status launch_contrib(const void *Q, const void *K, int is_bf16, int P, int 
   float *Qs = A + (size_t)P * Hkv * nC * 64;
   float *W = Qs + (size_t)P * Hq * nC * 64;
   if (nC > 0) {
-    const dim3 grid(nC, Hkv, P);
+    const dim3 grid(Hq, nC, P);
     if (is_bf16)
       launch_pdl(contrib_chunk_kernel<__nv_bfloat16>, grid, dim3(kCThreads), 0, stream,
                  static_cast<const __nv_bfloat16 *>(Q), static_cast<const __nv_bfloat16 *>(K),

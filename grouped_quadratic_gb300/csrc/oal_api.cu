@@ -381,11 +381,13 @@ oal_status oal_contribution_scores(const void *Q, const void *K, oal_dtype dtype
   OAL_TRY(check_common(P, Hq, Hkv, d, d, dtype, OAL_STATE_FULL));
   if (T < 0) return oal_fail(OAL_ERR_INVALID_ARG, "bad T=%d", T);
   if (P == 0) return OAL_OK;
+  if (P > 65535) return oal_fail(OAL_ERR_UNSUPPORTED, "P=%d above 65535", P);
   OAL_TRY(check_ptr(chi, "chi"));
   OAL_TRY(check_ptr(workspace, "workspace"));
   if (T > 0) {
     OAL_TRY(check_ptr(Q, "Q"));
     OAL_TRY(check_ptr(K, "K"));
+    if ((T + 127) / 128 > 65535) return oal_fail(OAL_ERR_UNSUPPORTED, "T=%d too long", T);
   }
   if (lengths) OAL_TRY(check_ptr(lengths, "lengths"));
   if (((uintptr_t)workspace & 255u) != 0)

@@ -248,7 +248,9 @@ oal_status oal_decode_step(const void *q, const void *k, const void *v,
  *  workspace  >= oal_contribution_workspace_bytes(P, Hq, Hkv, T, d) bytes,
  *           256-byte aligned (device); 0 from the size query means
  *           unsupported or invalid sizes.
- * Supported: d == 64.  P == 0 launches nothing; T == 0 writes zeros.
+ * Supported: d == 64, P <= 65535, T <= 8,388,480 (65,535 chunks of 128
+ * tokens).  P == 0
+ * launches nothing; T == 0 writes zeros.
  */
 size_t oal_contribution_workspace_bytes(int P, int Hq, int Hkv, int T, int d);
 oal_status oal_contribution_scores(const void *Q, const void *K, oal_dtype dtype, int P,
