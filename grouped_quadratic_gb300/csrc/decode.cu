@@ -24,6 +24,8 @@
 // a fixed order and divides.
 #include <cooperative_groups.h>
 
+#include <utility>
+
 #include "oal_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -147,37 +149,53 @@ __device__ __forceinline__ void slice_weights(const float *__restrict__ a,
 
 // Value columns of rows r0 .. r1 - 1 (r0 a multiple of 4): each warp takes 4
 // consecutive rows per step (lane l owns columns l and l + 32), writes the
-// updated rows and accumulates the readout of every head with packed fp32
-// FMAs.  s_rows[i] holds float i of the slice, S the slice in the state.
+// updated rows and accumulates the readout of every head.  The packed fp32
+// FMAs pair two adjacent rows of one column, so the weight pairs come
+// straight from a 16-byte shared load: acc[h][0] holds the partial sums of
+// column l over even and odd rows, acc[h][1] those of column l + 32 (their
+// two halves are added at the end).  s_rows[i] holds float i of the slice, S
+// the slice in the state.  NH: heads the loops are unrolled for (rho <= NH).
+template <int NH>
 __device__ __forceinline__ void rows_step(const float *s_rows, float *S, int r0, int r1, int rho,
                                           const float *s_u, const float *s_wk, const float *s_wq,
-                                          int stride, float2 (&acc)[kMaxRho]) {
+                                          int stride, float2 (&acc)[NH][2]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const float2 u01 = make_float2(s_u[lane], s_u[lane + 32]);
+  const float2 ua = make_float2(s_u[lane], s_u[lane]);
+  const float2 ub = make_float2(s_u[lane + 32], s_u[lane + 32]);
   for (int rb = r0 + 4 * warp; rb < r1; rb += 4 * kWarps) {
     const float4 wk4 = *reinterpret_cast<const float4 *>(&s_wk[rb]);
-    const float wk[4] = {wk4.x, wk4.y, wk4.z, wk4.w};
-    float2 nv[4];
+    // rows past r1 (zero weights) read as zero: they add nothing to the
+    // readout and are not stored
+    float va[4], vb[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int rr = rb + u;
-      nv[u] = make_float2(0.f, 0.f);
-      if (rr < r1) {
-        const float *src = s_rows + rr * kU;
-        nv[u] = make_float2(fmaf(wk[u], u01.x, src[lane]), fmaf(wk[u], u01.y, src[lane + 32]));
-        float *dst = S + (size_t)rr * kU;
-        __stcs(dst + lane, nv[u].x);
-        __stcs(dst + lane + 32, nv[u].y);
+      const bool in = rb + u < r1;
+      va[u] = in ? s_rows[(rb + u) * kU + lane] : 0.f;
+      vb[u] = in ? s_rows[(rb + u) * kU + lane + 32] : 0.f;
+    }
+    const float2 sa[2] = {make_float2(va[0], va[1]), make_float2(va[2], va[3])};
+    const float2 sb[2] = {make_float2(vb[0], vb[1]), make_float2(vb[2], vb[3])};
+    const float2 wk01 = make_float2(wk4.x, wk4.y), wk23 = make_float2(wk4.z, wk4.w);
+    const float2 na0 = ffma2(wk01, ua, sa[0]), nb0 = ffma2(wk01, ub, sb[0]);
+    const float2 na1 = ffma2(wk23, ua, sa[1]), nb1 = ffma2(wk23, ub, sb[1]);
+    const float nvA[4] = {na0.x, na0.y, na1.x, na1.y}, nvB[4] = {nb0.x, nb0.y, nb1.x, nb1.y};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (rb + u < r1) {
+        float *dst = S + (size_t)(rb + u) * kU;
+        __stcs(dst + lane, nvA[u]);
+        __stcs(dst + lane + 32, nvB[u]);
       }
     }
 #pragma unroll
-    for (int hh = 0; hh < kMaxRho; ++hh) {
+    for (int hh = 0; hh < NH; ++hh) {
       if (hh < rho) {
         const float4 wq = *reinterpret_cast<const float4 *>(&s_wq[hh * stride + rb]);
-        acc[hh] = ffma2(make_float2(wq.x, wq.x), nv[0], acc[hh]);
-        acc[hh] = ffma2(make_float2(wq.y, wq.y), nv[1], acc[hh]);
-        acc[hh] = ffma2(make_float2(wq.z, wq.z), nv[2], acc[hh]);
-        acc[hh] = ffma2(make_float2(wq.w, wq.w), nv[3], acc[hh]);
+        const float2 w01 = make_float2(wq.x, wq.y), w23 = make_float2(wq.z, wq.w);
+        acc[hh][0] = ffma2(w01, na0, acc[hh][0]);
+        acc[hh][0] = ffma2(w23, na1, acc[hh][0]);
+        acc[hh][1] = ffma2(w01, nb0, acc[hh][1]);
+        acc[hh][1] = ffma2(w23, nb1, acc[hh][1]);
       }
     }
   }
@@ -187,32 +205,33 @@ __device__ __forceinline__ void rows_step(const float *s_rows, float *S, int r0,
 // partial of every head in a fixed order: into s_out (accumulate: added to
 // it).  s_red is a free buffer of kWarps * kMaxRho * kU floats; the block
 // passes a barrier at the end.
+template <int NH>
 __device__ __forceinline__ void slice_reduce(const float *s_rows, float *S, int nrows, int rho,
                                              const float *s_wk, const float *s_wq, int stride,
-                                             const float2 (&acc)[kMaxRho], float *s_red_buf,
+                                             const float2 (&acc)[NH][2], float *s_red_buf,
                                              float (*s_out)[kU], bool accumulate) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float den[kMaxRho];
+  float den[NH];
 #pragma unroll
-  for (int hh = 0; hh < kMaxRho; ++hh) den[hh] = 0.f;
+  for (int hh = 0; hh < NH; ++hh) den[hh] = 0.f;
   for (int rr = tid; rr < nrows; rr += kThreads) {
     const float n2 = s_rows[rr * kU + kDv] + s_wk[rr];   // u_64 = 1
     __stcs(S + (size_t)rr * kU + kDv, n2);
 #pragma unroll
-    for (int hh = 0; hh < kMaxRho; ++hh)
+    for (int hh = 0; hh < NH; ++hh)
       if (hh < rho) den[hh] = fmaf(s_wq[hh * stride + rr], n2, den[hh]);
   }
 #pragma unroll
-  for (int hh = 0; hh < kMaxRho; ++hh)
+  for (int hh = 0; hh < NH; ++hh)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) den[hh] += __shfl_xor_sync(0xffffffffu, den[hh], o);
   __syncthreads();   // the slice buffer is reused for the block reduction
   float(*s_red)[kMaxRho][kU] = reinterpret_cast<float(*)[kMaxRho][kU]>(s_red_buf);
 #pragma unroll
-  for (int hh = 0; hh < kMaxRho; ++hh) {
+  for (int hh = 0; hh < NH; ++hh) {
     if (hh < rho) {
-      s_red[warp][hh][lane] = acc[hh].x;
-      s_red[warp][hh][lane + 32] = acc[hh].y;
+      s_red[warp][hh][lane] = acc[hh][0].x + acc[hh][0].y;
+      s_red[warp][hh][lane + 32] = acc[hh][1].x + acc[hh][1].y;
       if (lane == 0) s_red[warp][hh][64] = den[hh];
     }
   }
@@ -290,17 +309,18 @@ __device__ __forceinline__ void decode_slice(const Tin *__restrict__ q, const Ti
   slice_weights(a, b, Ctab, packed, h0, rho, f0, nrows, s_k, s_q, s_wk, &s_wq[0][0], kRows);
   __syncthreads();   // (also publishes the head and tail floats)
 
-  float2 acc[kMaxRho];
+  float2 acc[kMaxRho][2];
 #pragma unroll
-  for (int hh = 0; hh < kMaxRho; ++hh) acc[hh] = make_float2(0.f, 0.f);
+  for (int hh = 0; hh < kMaxRho; ++hh) acc[hh][0] = acc[hh][1] = make_float2(0.f, 0.f);
   for (int g = 0; g < kGroups; ++g) {
     if (!oal::tc::mbar_wait(&s_bar[g], 0, &s_abort, status)) break;
-    rows_step(s_rows, S, g * rows_per_group, min(nrows, (g + 1) * rows_per_group), rho, s_u, s_wk,
-              &s_wq[0][0], kRows, acc);
+    rows_step<kMaxRho>(s_rows, S, g * rows_per_group, min(nrows, (g + 1) * rows_per_group), rho,
+                       s_u, s_wk, &s_wq[0][0], kRows, acc);
   }
   // every copy has landed (or timed out) before the buffer is read again
   for (int g = 0; g < kGroups; ++g) oal::tc::mbar_wait_teardown(&s_bar[g], 0, status);
-  slice_reduce(s_rows, S, nrows, rho, s_wk, &s_wq[0][0], kRows, acc, s_buf, s_part, false);
+  slice_reduce<kMaxRho>(s_rows, S, nrows, rho, s_wk, &s_wq[0][0], kRows, acc, s_buf, s_part,
+                        false);
 }
 
 template <typename Tin>
@@ -371,7 +391,7 @@ __device__ __forceinline__ SliceGeom slice_geom(float *state, int F, int rows_pe
   return g;
 }
 
-template <typename Tin>
+template <typename Tin, int RHO>
 __global__ void __launch_bounds__(kThreads, kStreamBlocksPerSM)
 decode_stream_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                      const Tin *__restrict__ v, const float *__restrict__ a,
@@ -388,7 +408,7 @@ decode_stream_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
   __shared__ __align__(8) uint64_t s_bar[2];
   __shared__ int s_abort;
   const int tid = threadIdx.x;
-  const int rho = Hq / Hkv;
+  constexpr int rho = RHO;
   const int i0 = blockIdx.x * per_block, i1 = min(nitems, i0 + per_block);
   if (tid == 0) {
     s_abort = 0;
@@ -444,12 +464,12 @@ decode_stream_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     __syncthreads();
     const bool landed = oal::tc::mbar_wait(&s_bar[bb], (j >> 1) & 1, &s_abort, status);
     if (__syncthreads_or(!landed)) { fail_at = it; break; }   // the same decision in every thread
-    float2 acc[kMaxRho];
+    float2 acc[RHO][2];
 #pragma unroll
-    for (int hh = 0; hh < kMaxRho; ++hh) acc[hh] = make_float2(0.f, 0.f);
-    rows_step(s_rows, g.S, 0, g.nrows, rho, s_u, s_wk, &s_wq[0][0], kStreamRows, acc);
-    slice_reduce(s_rows, g.S, g.nrows, rho, s_wk, &s_wq[0][0], kStreamRows, acc,
-                 s_dyn + bb * kStreamBuf, s_acc, true);
+    for (int hh = 0; hh < RHO; ++hh) acc[hh][0] = acc[hh][1] = make_float2(0.f, 0.f);
+    rows_step<RHO>(s_rows, g.S, 0, g.nrows, RHO, s_u, s_wk, &s_wq[0][0], kStreamRows, acc);
+    slice_reduce<RHO>(s_rows, g.S, g.nrows, RHO, s_wk, &s_wq[0][0], kStreamRows, acc,
+                      s_dyn + bb * kStreamBuf, s_acc, true);
   }
   if (cur_unit >= 0 && fail_at < 0)
     for (int n = tid; n < rho * kU; n += kThreads) pblk[slot * kMaxRho * kU + n] = s_acc[n / kU][n % kU];
@@ -559,6 +579,26 @@ static int decode_cluster_size(int packed) {
   return c;
 }
 
+// The streaming kernel of each query-head count 1..kMaxRho.
+template <typename Tin, int... I>
+static bool set_stream_smem(std::integer_sequence<int, I...>) {
+  return ((cudaFuncSetAttribute(decode_stream_kernel<Tin, I + 1>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(2 * kStreamBuf * sizeof(float))) == cudaSuccess) && ...);
+}
+template <typename Tin, int... I, typename... Args>
+static oal_status launch_stream(std::integer_sequence<int, I...>, int rho, dim3 grid,
+                                cudaStream_t stream, Args... args) {
+  bool done = false;
+  ((rho == I + 1 ? (launch_pdl(decode_stream_kernel<Tin, I + 1>, grid, dim3(kThreads),
+                               2 * kStreamBuf * sizeof(float), stream, args...),
+                    done = true)
+                 : false),
+   ...);
+  if (!done) return oal_fail(OAL_ERR_UNSUPPORTED, "Hq/Hkv=%d", rho);
+  return oal_after_launch("decode_stream_kernel", stream);
+}
+
 template <typename Tin>
 static oal_status launch_decode_t(const Tin *q, const Tin *k, const Tin *v, int B, int Hq, int Hkv,
                                   const float *a, const float *b, const float *C, int packed,
@@ -574,9 +614,7 @@ static oal_status launch_decode_t(const Tin *q, const Tin *k, const Tin *v, int 
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(decode_smem_floats(kClusterRows) * sizeof(float))) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(decode_stream_kernel<Tin>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(2 * kStreamBuf * sizeof(float))) != cudaSuccess)
+        !set_stream_smem<Tin>(std::make_integer_sequence<int, kMaxRho>{}))
       return oal_check_launch("decode: shared memory attribute");
     attr_set[dev] = true;
   }
@@ -603,10 +641,10 @@ static oal_status launch_decode_t(const Tin *q, const Tin *k, const Tin *v, int 
   }
   const StreamPlan p = stream_plan(units, packed);
   float *partial = (float *)ws;
-  launch_pdl(decode_stream_kernel<Tin>, dim3(p.nblocks), dim3(kThreads),
-             2 * kStreamBuf * sizeof(float), stream, q, k, v, a, b, C, state, Hq, Hkv, F, packed,
-             p.nslices, p.nitems, p.per_block, partial, oal_device_status_word());
-  oal_status st = oal_after_launch("decode_stream_kernel", stream);
+  oal_status st = launch_stream<Tin>(std::make_integer_sequence<int, kMaxRho>{}, Hq / Hkv,
+                                     dim3(p.nblocks), stream, q, k, v, a, b, C, state, Hq, Hkv,
+                                     F, packed, p.nslices, p.nitems, p.per_block, partial,
+                                     oal_device_status_word());
   if (st != OAL_OK) return st;
   launch_pdl(decode_finish_kernel<Tin>, dim3((unsigned)units), dim3(kThreads), 0, stream, y,
              (const float *)partial, Hq, Hkv, p.nslices, p.per_block);

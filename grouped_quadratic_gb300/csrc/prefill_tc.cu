@@ -65,7 +65,7 @@ constexpr int kH2P = 2112;       // paired H2 features
 constexpr int kNKB = 35;         // readout K blocks of 64 (the last one has K = 16)
 constexpr int kTiles = 18;       // 128-feature tiles of the state kernel
 constexpr int kN = 80;           // UMMA N of [v | 1]: 64 value columns, the "1" column, 15 zeros
-constexpr int kMaxNH = 1;        // query heads per readout block (three blocks per SM)
+constexpr int kMaxNH = 1;        // query heads per readout block (four blocks per SM)
 constexpr int kMaxTailG = 6;     // tail groups (G - 1 <= 6)
 // Snapshot rows: the 64 value columns and the "1" column; the readout's TMA box
 // is kN = 80 rows high and reads rows 65..79 as zero (out of range).
@@ -952,7 +952,6 @@ constexpr int kNA = 3;           // A half slots (128 x 32 bf16, 16 columns) in 
 template <int NS>
 struct __align__(1024) ReadSmem {
   __nv_bfloat16 q[kMaxNH][kC * 64];    // 128B-swizzled [token][dim], then q^T [dim][token]
-  __nv_bfloat16 qs[kMaxNH][kC * 64];   // bf16(alpha_dim q) [dim][token]
   __nv_bfloat16 b[kNB][NS * kN * 64];  // snapshot K blocks [n][64 features]
   __nv_bfloat16 coef[kMaxNH][kCoefRow];
   uint64_t qkv_full, b_full[kNB], a_full[kNA], a_empty[kNA], d_full;
@@ -961,7 +960,7 @@ struct __align__(1024) ReadSmem {
   int abort_flag;
   int loaded;                          // snapshot K blocks whose load was issued
 };
-static_assert(3 * (sizeof(ReadSmem<1>) + 2048) <= 228 * 1024, "three readout blocks per SM");
+static_assert(4 * (sizeof(ReadSmem<1>) + 1024) <= 228 * 1024, "four readout blocks per SM");
 static_assert(2 * (sizeof(ReadSmem<2>) + 2048) <= 228 * 1024, "two readout blocks per SM");
 
 struct ReadArgs {
@@ -983,11 +982,11 @@ constexpr uint32_t kReadTmemCols = NS == 1 ? 128 : 256;
 
 // ---- readout A block builders (compile-time feature layout)
 // The builder of token row m keeps p = bf16(pw * q) in registers and reads
-// q from transposed copies in shared memory, one conflict-free 16-bit load
-// per value: qs[dim][token] = bf16(alpha_dim q) for the rank-one words,
-// qT[dim][token] = q for the rest.  Rows r of the paired H2 order split into
-// runs of words that share r; a word of a run is qs_r * p_t, the row's first
-// word rescaled (the diagonal entry by 1/2, the duplicate (r, r - 1) by 0).
+// q from the transposed tile qT[dim][token] in shared memory, one
+// conflict-free 16-bit load per value.  Rows r of the paired H2 order split
+// into runs of words that share r; a word of a run is qs_r * p_t with
+// qs_r = bf16(alpha_r q_r) formed once per run, the row's first word
+// rescaled (the diagonal entry by 1/2, the duplicate (r, r - 1) by 0).
 __device__ __forceinline__ uint32_t qt_ld(const __nv_bfloat16 *qcol, int r) {
   return *reinterpret_cast<const uint16_t *>(qcol + r * kC);
 }
@@ -1004,24 +1003,25 @@ __device__ __forceinline__ void h2_run(uint32_t qr, const uint32_t (&p)[32], uin
 }
 
 template <int KB, int H, int P0>
-__device__ __forceinline__ void h2_runs(const __nv_bfloat16 *qscol, const uint32_t (&p)[32],
-                                        uint32_t (&out)[16]) {
+__device__ __forceinline__ void h2_runs(const __nv_bfloat16 *qcol, const float *alpha,
+                                        const uint32_t (&p)[32], uint32_t (&out)[16]) {
   constexpr int r = feat_r(64 * KB + 2 * (16 * H + P0));
   constexpr int end_w = row_off(r + 1) / 2 - 32 * KB - 16 * H;   // run end (word in half)
   constexpr int P1 = end_w < 16 ? end_w : 16;
-  const uint32_t qr = qt_ld(qscol, r) * 0x10001u;   // (qs_r, qs_r)
+  const float sr = alpha[r] * __uint_as_float(qt_ld(qcol, r) << 16);
+  const uint32_t qr = pack_bf16x2(sr, sr);   // (bf16(alpha_r q_r), the same)
   h2_run<KB, H, P0>(qr, p, out, std::make_integer_sequence<int, P1 - P0>{});
-  if constexpr (P1 < 16) h2_runs<KB, H, P1>(qscol, p, out);
+  if constexpr (P1 < 16) h2_runs<KB, H, P1>(qcol, alpha, p, out);
 }
 
 // Words 16 H .. 16 H + 15 of K block KB of one A row (token row of Phi~(Q)),
 // rank-one form; cw = this head's weights of block KB (H1 and H0 blocks).
 template <int KB, int H>
-__device__ __forceinline__ void build_half(const __nv_bfloat16 *qcol, const __nv_bfloat16 *qscol,
+__device__ __forceinline__ void build_half(const __nv_bfloat16 *qcol, const float *alpha,
                                            const uint32_t (&p)[32], const uint32_t *cw,
                                            uint32_t (&out)[16]) {
   if constexpr (KB < 33) {
-    h2_runs<KB, H, 0>(qscol, p, out);
+    h2_runs<KB, H, 0>(qcol, alpha, p, out);
   } else if constexpr (KB < kNKB - 1) {
 #pragma unroll
     for (int w = 0; w < 16; ++w) {
@@ -1078,12 +1078,12 @@ __device__ __noinline__ void patch_exceptions(const RFactor &F, int hb, const __
 
 #define OAL_BUILD_CASE(n) \
   case n:                 \
-    build_half<n, H>(qcol, qscol, p, cw, out); \
+    build_half<n, H>(qcol, alpha, p, cw, out); \
     break;
 
 template <int H>
 __device__ __forceinline__ void build_dispatch(int kb, const __nv_bfloat16 *qcol,
-                                               const __nv_bfloat16 *qscol, const uint32_t (&p)[32],
+                                               const float *alpha, const uint32_t (&p)[32],
                                                const uint32_t *cw, uint32_t (&out)[16]) {
   switch (kb) {
     OAL_BUILD_CASE(0) OAL_BUILD_CASE(1) OAL_BUILD_CASE(2) OAL_BUILD_CASE(3)
@@ -1379,11 +1379,11 @@ __device__ bool intra_dispatch(int ge, IntraSmem<kWide> &s, const ReadArgs &args
 // ---------------------------------------------------------------- intra kernel
 // Warps 0-3: kappa (thread = query row) and the epilogue; warp 4: UMMA issue
 // (s = Q K^T per 32-key block, then P.V) and tensor memory; warp 5: TMA.
-// Blocks per SM by register need: four for small G (the whole grid of a
-// 4096-token, 14-head chunking fits one wave from three up); the 256-key
-// tiles of C = 256 fit two by shared memory.
+// Blocks per SM by register need: four for small G, three up to G = 6 (a
+// few bytes of spill at G = 6 cost less than the third block gains); the
+// 256-key tiles of C = 256 fit two by shared memory.
 template <int G, bool kWide>
-__global__ void __launch_bounds__(kIntraThreads, kWide ? 2 : (G <= 3 ? 4 : (G <= 5 ? 3 : 2)))
+__global__ void __launch_bounds__(kIntraThreads, kWide ? 2 : (G <= 3 ? 4 : (G <= 6 ? 3 : 2)))
 tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, ReadArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -1529,19 +1529,19 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 }
 
 // ---------------------------------------------------------------- readout kernel
-// One block per (query head, chunk, batch x KV head), three blocks per SM
-// (128 tensor-memory columns, ~70 KB of shared memory each): the 448 blocks
-// of a 14-head, 4096-token prefill fill one wave with ~3 heads per SM, and
-// blocks that run independently keep the tensor pipe fed from whichever
-// block has a K block ready.  Warp roles (5 warps):
-//   0-3  A builders (one token row per thread): setup (transposed and scaled
-//        Q tile), every K block of Phi~(Q_c), then the epilogue; warp 0 also
+// One block per (query head, chunk, batch x KV head), four blocks per SM
+// (128 tensor-memory columns, ~52 KB of shared memory and 96 registers a
+// thread each): blocks that run independently keep the tensor pipe fed from
+// whichever block has a K block ready, and the builders of four blocks hide
+// each other's latencies.  Warp roles (5 warps):
+//   0-3  A builders (one token row per thread): setup (transposed Q tile),
+//        every K block of Phi~(Q_c), then the epilogue; warp 0 also
 //        refills the snapshot stages (3) by TMA as soon as the wait for an A
 //        slot shows that the MMAs reading a stage are complete
 //   4    UMMA issuer (warp-uniform loop, elected lane), tensor memory owner,
 //        loads the first snapshot K blocks
 template <int NS>
-__global__ void __launch_bounds__(kReadThreads, NS == 1 ? 3 : 2)
+__global__ void __launch_bounds__(kReadThreads, NS == 1 ? 4 : 2)
 tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS,
                   ReadArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -1672,7 +1672,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     const int hh = warp >> 2;
     // q^T [64 dims][128 tokens] replaces the swizzled Q tile of head hh
     __nv_bfloat16 *qT = s.q[hh];
-    const __nv_bfloat16 *qcol = qT + m, *qscol = s.qs[hh] + m;
+    const __nv_bfloat16 *qcol = qT + m;
     const RFactor &F = *reinterpret_cast<const RFactor *>(s.coef[hh] + kKP);
     const bool ok = hh < nh && mbar_wait(&s.qkv_full, 0, abort_flag, args.status);
     uint32_t p[32], q[32];
@@ -1692,18 +1692,13 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     if (hh < nh) {   // all four warps of the group pass both barriers, ok or not
       named_bar(1 + hh, 128);   // every row of the tile read
       if (ok) {
-        uint16_t *qs = reinterpret_cast<uint16_t *>(s.qs[hh]);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float q0 = __uint_as_float(q[i] << 16), q1 = __uint_as_float(q[i] & 0xffff0000u);
           reinterpret_cast<uint16_t *>(qT)[(2 * i) * kC + m] = (uint16_t)(q[i] & 0xffffu);
           reinterpret_cast<uint16_t *>(qT)[(2 * i + 1) * kC + m] = (uint16_t)(q[i] >> 16);
-          const uint32_t sc = pack_bf16x2(F.alpha[2 * i] * q0, F.alpha[2 * i + 1] * q1);
-          qs[(2 * i) * kC + m] = (uint16_t)(sc & 0xffffu);
-          qs[(2 * i + 1) * kC + m] = (uint16_t)(sc >> 16);
         }
       }
-      named_bar(1 + hh, 128);   // q^T and qs complete
+      named_bar(1 + hh, 128);   // q^T complete
     }
     if (ok) {
       const bool factored = F.factored != 0;
@@ -1727,8 +1722,8 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(p[i]));
         uint32_t out0[16], out1[16];
         if (factored) {
-          build_dispatch<0>(kb, qcol, qscol, p, cw, out0);
-          build_dispatch<1>(kb, qcol, qscol, p, cw, out1);
+          build_dispatch<0>(kb, qcol, F.alpha, p, cw, out0);
+          build_dispatch<1>(kb, qcol, F.alpha, p, cw, out1);
         } else {
           build_half_general(kb, 0, qcol, cw, out0);
           build_half_general(kb, 1, qcol, cw, out1);
