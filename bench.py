@@ -74,7 +74,7 @@ TRAFFIC = [
     # (kernel, source file, workload key (B, Hq, Hkv, T, G, layout, chunk), bytes per
     #  launch, source sha256)
     ("tc_readout_kernel", "prefill_tc.cu", (4, 32, 8, 8192, 6, "packed", 128),
-     1000651520 + 121596416, "779dc6da4435133e0338f33d2babcfe2df491d9cc1f191b69de393502ce3a6f8"),
+     1107291648 + 134631168, "6304ebd7a219a92fd04a53b21430c34e55343390bb2ae8ff1976e3d24e94331d"),
 ]
 
 
