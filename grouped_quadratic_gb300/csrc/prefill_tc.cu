@@ -154,6 +154,16 @@ __device__ __forceinline__ bool is_duplicate(uint16_t code) {
 // where s = q.k (unscaled) and s_g' = sum over the dims of tail group g' of
 // q_r k_r.  The bulk group g* (largest) is eliminated through
 // s_{g*} = s - sum_{g != g*} s_g; alpha/beta carry the 1/sqrt(64) scale.
+// Features of the tensor-core kappa of tc_intra_tk_kernel: the linear feature
+// of tail dim i at position i (i < kTkMaxLin), the pair (i, j), i <= j, at
+// kTkMaxLin + tk_pair(i, j); 54 of the 64 columns of a 128-byte row.
+constexpr int kTkMaxLin = 9;
+constexpr int kTkFeat = kTkMaxLin + kTkMaxLin * (kTkMaxLin + 1) / 2;
+__host__ __device__ constexpr int tk_pair(int i, int j) {
+  return i * kTkMaxLin - i * (i - 1) / 2 + (j - i);
+}
+static_assert(kTkFeat <= 64, "tensor-core kappa features fit one K = 64 row");
+
 struct KPlan {
   float alpha[8];
   float beta[kMaxTailG][8];
@@ -170,6 +180,13 @@ struct KPlan {
   int goff[kMaxTailG + 1];     // generic path: dims of tail group g' in gdims[goff[g']..]
   int gdims[64];
   int G;
+  // tensor-core kappa (tc_intra_tk_kernel): 1 when every tail dim has a
+  // feature (a fast plan with at most kTkMaxLin tail dims); the dims in slot
+  // order; the coefficients of each feature for T and for U (zero past nlin)
+  int tk_mode, tk_nlin;
+  int tk_dim[kTkMaxLin];
+  float tk_cT[kTkFeat];
+  float tk_cU[kTkMaxLin];
 };
 
 // The dynamic shared memory rounded up to a 1024-byte boundary (swizzled
@@ -506,6 +523,40 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
     P->lin[v] = l;
   } else if (tid == 96) {
     P->c0 = eps + sM[0][0];
+  }
+  __syncthreads();   // every field of the plan above is written
+  if (tid == 0) {
+    // the tail dims in slot order, then the coefficients of kappa's terms in
+    // them: U = sum_r quad[0][1+a(r)] q_r k_r; T = sum_r lin[1+a(r)] q_r k_r +
+    // sum_{r <= r'} w q_r q_r' k_r k_r' (w = quad[v][w], doubled for two dims
+    // of one group)
+    int nlin = 0, slot[kTkMaxLin];
+    bool ok = P->fast != 0;
+    for (int a2 = 0; a2 < P->ntg && ok; ++a2)
+      for (int d = 0; d < P->nd[a2]; ++d) {
+        if (nlin == kTkMaxLin) { ok = false; break; }
+        P->tk_dim[nlin] = P->dims[a2][d];
+        slot[nlin++] = a2;
+      }
+    auto qi = [&](int v, int w) { return v * Ge - v * (v - 1) / 2 + (w - v); };
+    for (int f = 0; f < kTkFeat; ++f) P->tk_cT[f] = 0.f;
+    for (int i = 0; i < kTkMaxLin; ++i) {
+      P->tk_cU[i] = 0.f;
+      if (i >= nlin) P->tk_dim[i] = 0;
+    }
+    if (ok) {
+      for (int i = 0; i < nlin; ++i) {
+        P->tk_cT[i] = P->lin[1 + slot[i]];
+        P->tk_cU[i] = P->quad[qi(0, 1 + slot[i])];
+        for (int j = i; j < nlin; ++j) {
+          const int v = 1 + slot[i], w = 1 + slot[j];
+          const float qvw = P->quad[qi(v, w)];
+          P->tk_cT[kTkMaxLin + tk_pair(i, j)] = v == w && i != j ? 2.f * qvw : qvw;
+        }
+      }
+    }
+    P->tk_mode = ok ? 1 : 0;
+    P->tk_nlin = ok ? nlin : 0;
   }
 }
 
@@ -1106,7 +1157,9 @@ __device__ __forceinline__ void build_dispatch(int kb, const __nv_bfloat16 *qcol
 // the readout's epilogue.  One block per (query head, 128-row tile, batch x KV
 // head).  The keys of a tile are those of its chunk up to the tile's last row:
 // 128 (C = 64, 128; for C = 64 the tile's two chunks are told apart by the
-// mask), or 256 for the second half of a 256-token chunk.  Per 32-key block:
+// mask), or 256 for the second half of a 256-token chunk.  The chunk sizes of
+// 64 and 128 run tc_intra_tk_kernel below; this kernel serves C = 256 (256
+// keys a tile, templated on the group count).  Per 32-key block:
 // s = Q K^T by UMMA into tensor memory, the tail-group sums and kappa in fp32
 // on the CUDA cores, P = bf16(kappa) masked to the chunk's causal pairs written
 // back over s, numerators += P V by UMMA.
@@ -1130,7 +1183,6 @@ struct __align__(1024) IntraSmem {
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(IntraSmem<false>) + 1024 <= 56 * 1024, "four intra blocks per SM");
 static_assert(sizeof(IntraSmem<true>) + 1024 <= 113 * 1024, "two wide intra blocks per SM");
 
 // Geometry of a tile's keys and of one warp's rows.
@@ -1525,6 +1577,327 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (warp == kIss) {
     tc_fence_after();
     tmem_dealloc(tb, kIntraTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- intra kernel, tensor-core kappa
+// For chunks of 64 and 128 tokens.  With z_0 = s = q.k and z_g the tail-group
+// sums, the quadratic form of kappa splits into
+//     kappa = (c0 + T) + s (lin_0 + U + quad_00 s),
+//     U = sum_g quad_0g z_g = sum_r quad_{0 g(r)} q_r k_r,
+//     T = sum_g lin_g z_g + sum_{g <= h} quad_gh z_g z_h
+//       = sum_r lin_{g(r)} q_r k_r + sum_{r <= r'} w_{r r'} q_r q_r' k_r k_r'
+// over the tail dims r (w_{r r'} = quad_gh for dims of different groups,
+// 2 quad_gg for two dims of one group, quad_gg for r = r').  T and U are
+// contractions of per-query and per-key features over F <= 64 features, so
+// they run on the tensor cores beside s: per 32-key block, S = Q K^T, T =
+// A_T B^T, U = A_U B^T into tensor memory, with B = [k_r, k_r k_r'] (key
+// side) and A_T, A_U the query rows times the coefficients.  The CUDA cores
+// keep three FMAs per pair.  Heads whose features do not fit (more than 9
+// tail dims, or a group of more than two dims) evaluate kappa from the
+// tiles as the generic path of tc_intra_kernel does.
+constexpr int kTkThreads = 192;          // warps 0-3: features, kappa, epilogue; 4: UMMA; 5: TMA
+constexpr int kTkS = 0;                  // s / P sub-tiles at 0 and 32
+constexpr int kTkT = 64;                 // T sub-tiles at 64 and 96
+constexpr int kTkU = 128;                // U sub-tiles at 128 and 160
+constexpr int kTkI = 192;                // numerators at [192, 256)
+constexpr uint32_t kTkTmemCols = 256;
+struct __align__(1024) TkSmem {
+  __nv_bfloat16 q[kC * 64];   // 128B-swizzled [row][64] tiles
+  __nv_bfloat16 k[kC * 64];
+  __nv_bfloat16 v[kC * 64];
+  __nv_bfloat16 aT[kC * 64];  // query features for T, K-major, features past nfeat zero
+  __nv_bfloat16 aU[kC * 64];  // query features for U
+  __nv_bfloat16 bk[kC * 64];  // key features
+  KPlan plan;
+  uint64_t qkv_full, phi_full, s_full[2], p_full[2], s_free[2], d_full;
+  uint64_t never;             // failure-path tests: nothing arrives
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(2 * (sizeof(TkSmem) + 1024) <= 228 * 1024, "two intra blocks per SM");
+
+// Pair (i, j) of feature position f >= kTkMaxLin (folded at compile time
+// once the loops over f are unrolled).
+__host__ __device__ constexpr int tk_pair_i(int f) {
+  int i = 0;
+  while (i + 1 < kTkMaxLin && kTkMaxLin + tk_pair(i + 1, i + 1) <= f) ++i;
+  return i;
+}
+__host__ __device__ constexpr int tk_pair_j(int f) {
+  return f - kTkMaxLin - tk_pair(tk_pair_i(f), tk_pair_i(f)) + tk_pair_i(f);
+}
+static_assert(tk_pair_i(kTkMaxLin + tk_pair(3, 7)) == 3 && tk_pair_j(kTkMaxLin + tk_pair(3, 7)) == 7,
+              "feature position of a pair");
+
+// Feature row of 8 features starting at F0 from the row's tail values:
+// key side k_i (k_i k_j), query side cT_f q_i (q_j), and (kU) cU_f q_i.
+template <int F0>
+__device__ __forceinline__ void tk_row_chunk(const float (&qv)[kTkMaxLin], const float (&kv)[kTkMaxLin],
+                                             const float *cT, uint4 &at, uint4 &bk) {
+  float a[8], b[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int f = F0 + e;
+    if (f < kTkMaxLin) {
+      a[e] = cT[f] * qv[f];
+      b[e] = kv[f];
+    } else if (f < kTkFeat) {
+      const int fi = tk_pair_i(f), fj = tk_pair_j(f);
+      a[e] = cT[f] * qv[fi] * qv[fj];
+      b[e] = kv[fi] * kv[fj];
+    } else {
+      a[e] = 0.f;
+      b[e] = 0.f;
+    }
+  }
+  at = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                  pack_bf16x2(a[6], a[7]));
+  bk = make_uint4(pack_bf16x2(b[0], b[1]), pack_bf16x2(b[2], b[3]), pack_bf16x2(b[4], b[5]),
+                  pack_bf16x2(b[6], b[7]));
+}
+
+__global__ void __launch_bounds__(kTkThreads, 2)
+tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, ReadArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  TkSmem &s = *reinterpret_cast<TkSmem *>(smem_align1024(smem_raw));
+  const int hg = blockIdx.x, t = blockIdx.y, unit = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bidx = unit / args.Hkv, kv = unit % args.Hkv;
+  const int h = kv * args.rho + hg;
+  const IntraGeom geo = intra_geom(t, args.chunk);   // 4 key blocks (C <= 128)
+  constexpr int kIss = 4, kTma = 5;
+  pdl_trigger();
+
+  if (tid == 0) {
+    s.abort_flag = 0;
+    mbar_init(&s.qkv_full, 1);
+    mbar_init(&s.phi_full, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.p_full[i], 4);
+      mbar_init(&s.s_free[i], 1);
+    }
+    mbar_init(&s.d_full, 1);
+    mbar_init(&s.never, 1);
+    fence_mbar_init();
+  }
+  if (warp == kIss) {
+    tmem_alloc(&s.tmem_base, kTkTmemCols);
+    tmem_relinquish();
+  }
+  pdl_wait();   // plans of the prep kernel; the intra rows of the previous call
+  for (int n = tid; n < (int)(sizeof(KPlan) / 4); n += kTkThreads)
+    reinterpret_cast<int *>(&s.plan)[n] = reinterpret_cast<const int *>(&args.plans[h])[n];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = s.tmem_base;
+  volatile int *abort_flag = &s.abort_flag;
+  const int mode = s.plan.tk_mode;
+
+  if (warp == kIss) {
+    if (lane == 0) {
+      const uint32_t id32k = idesc_bf16_f32(128, 32, 0);
+      const uint32_t id64mn = idesc_bf16_f32(128, 64, 1);
+      const uint64_t qdesc = sdesc_sw128(smem_u32(s.q), 16, 1024);
+      const uint64_t kdesc0 = sdesc_sw128(smem_u32(s.k), 16, 1024);
+      const uint64_t vdesc0 = sdesc_sw128(smem_u32(s.v), 16, 1024);
+      const uint64_t atdesc = sdesc_sw128(smem_u32(s.aT), 16, 1024);
+      const uint64_t audesc = sdesc_sw128(smem_u32(s.aU), 16, 1024);
+      const uint64_t bdesc0 = sdesc_sw128(smem_u32(s.bk), 16, 1024);
+      const bool tu = mode && s.plan.tk_nlin > 0;
+      // S = Q K^T of 32-key block kb, then (tu) T and U: K = 64 and 16 features
+      auto issue_s = [&](int kb) {
+        const uint64_t koff = (uint64_t)((32 * kb * 128) >> 4);
+        const uint32_t b = kb & 1;
+        umma_ss(tb + kTkS + 32 * b, qdesc, kdesc0 + koff, id32k, 0u);
+        umma_ss(tb + kTkS + 32 * b, qdesc + 2, kdesc0 + koff + 2, id32k, 1u);
+        umma_ss(tb + kTkS + 32 * b, qdesc + 4, kdesc0 + koff + 4, id32k, 1u);
+        umma_ss(tb + kTkS + 32 * b, qdesc + 6, kdesc0 + koff + 6, id32k, 1u);
+      };
+      auto issue_tu = [&](int kb) {
+        const uint64_t koff = (uint64_t)((32 * kb * 128) >> 4);
+        const uint32_t b = kb & 1;
+        if (tu) {
+#pragma unroll
+          for (int k2 = 0; k2 < 4; ++k2)
+            umma_ss(tb + kTkT + 32 * b, atdesc + 2 * k2, bdesc0 + koff + 2 * k2, id32k, k2 > 0 ? 1u : 0u);
+          umma_ss(tb + kTkU + 32 * b, audesc, bdesc0 + koff, id32k, 0u);
+        }
+        umma_commit(&s.s_full[b]);
+      };
+      const bool starve = args.status[1] == kStarveIntra;   // failure-path test only
+      bool ok = mbar_wait(starve ? &s.never : &s.qkv_full, 0, abort_flag, args.status);
+      if (ok) {
+        // the first two S blocks need only Q and K: they run while the
+        // feature rows are built
+        tc_fence_after();
+        issue_s(0);
+        if (geo.nkb > 1) issue_s(1);
+        ok = !tu || mbar_wait(&s.phi_full, 0, abort_flag, args.status);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_tu(0);
+        if (geo.nkb > 1) issue_tu(1);
+      }
+      for (int kb = 0; kb < geo.nkb && ok; ++kb) {
+        if (!mbar_wait(&s.p_full[kb & 1], (kb >> 1) & 1, abort_flag, args.status)) break;
+        tc_fence_after();
+        const uint32_t at = tb + kTkS + 32 * (kb & 1);
+        const uint64_t vd = vdesc0 + (uint64_t)((32 * kb * 128) >> 4);
+        umma_ts(tb + kTkI, at, vd, id64mn, kb > 0 ? 1u : 0u);
+        umma_ts(tb + kTkI, at + 8, vd + (2048 >> 4), id64mn, 1u);
+        umma_commit(&s.s_free[kb & 1]);
+        if (kb + 2 < geo.nkb) {
+          if (!mbar_wait(&s.s_free[kb & 1], (kb >> 1) & 1, abort_flag, args.status)) break;
+          tc_fence_after();
+          issue_s(kb + 2);
+          issue_tu(kb + 2);
+        }
+      }
+      umma_commit(&s.d_full);
+      mbar_wait_teardown(&s.d_full, 0, args.status);   // no MMA in flight at exit
+    }
+    __syncwarp();
+  } else if (warp == kTma) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      mbar_arrive_expect_tx(&s.qkv_full, 3u * kC * 64 * 2);
+      tma_load_3d(s.q, &tmQ, &s.qkv_full, 0, geo.row0, bidx * args.Hq + h);
+      tma_load_3d(s.k, &tmK, &s.qkv_full, 0, geo.ks, unit);
+      tma_load_3d(s.v, &tmV, &s.qkv_full, 0, geo.ks, unit);
+      mbar_wait_teardown(&s.qkv_full, 0, args.status);
+    }
+    __syncwarp();
+  } else {
+    // warps 0-3, thread = query row m and key row m of the tile
+    const int m = tid;
+    const int C = args.chunk;
+    const int i_tok = geo.row0 + m;
+    const int cs = (i_tok / C) * C;                  // this row's chunk starts here
+    const int rw0 = geo.row0 + 32 * warp, rw1 = rw0 + 31;
+    const int csw = (rw0 / C) * C;                   // the warp's rows share one chunk (C >= 64)
+    const KPlan &p = s.plan;
+    const bool tu = mode && p.tk_nlin > 0;   // (no tail dims: T = U = 0)
+    bool ok = mbar_wait(&s.qkv_full, 0, abort_flag, args.status);
+    if (ok && tu) {
+      // the query and key features of row m: the row's tail values, then the
+      // 64-feature rows in registers, eight 16-byte stores per tile
+      float qv[kTkMaxLin], kv[kTkMaxLin];
+#pragma unroll
+      for (int i = 0; i < kTkMaxLin; ++i) {
+        const bool in = i < p.tk_nlin;
+        qv[i] = in ? bf16_at(s.q, m, p.tk_dim[i]) : 0.f;
+        kv[i] = in ? bf16_at(s.k, m, p.tk_dim[i]) : 0.f;
+      }
+      uint8_t *rt = reinterpret_cast<uint8_t *>(s.aT), *ru = reinterpret_cast<uint8_t *>(s.aU);
+      uint8_t *rb = reinterpret_cast<uint8_t *>(s.bk);
+      uint4 at, bk;
+#define OAL_TK_CHUNK(c)                                                  \
+  tk_row_chunk<8 * (c)>(qv, kv, p.tk_cT, at, bk);                        \
+  *reinterpret_cast<uint4 *>(rt + sw128(m, c)) = at;                     \
+  *reinterpret_cast<uint4 *>(rb + sw128(m, c)) = bk;
+      OAL_TK_CHUNK(0) OAL_TK_CHUNK(1) OAL_TK_CHUNK(2) OAL_TK_CHUNK(3)
+      OAL_TK_CHUNK(4) OAL_TK_CHUNK(5) OAL_TK_CHUNK(6) OAL_TK_CHUNK(7)
+#undef OAL_TK_CHUNK
+      // U: the linear features (positions < 16; the rest of the row is unread)
+      float u[16];
+#pragma unroll
+      for (int f = 0; f < 16; ++f) u[f] = f < kTkMaxLin ? p.tk_cU[f < kTkMaxLin ? f : 0] * qv[f < kTkMaxLin ? f : 0] : 0.f;
+      *reinterpret_cast<uint4 *>(ru + sw128(m, 0)) =
+          make_uint4(pack_bf16x2(u[0], u[1]), pack_bf16x2(u[2], u[3]), pack_bf16x2(u[4], u[5]),
+                     pack_bf16x2(u[6], u[7]));
+      *reinterpret_cast<uint4 *>(ru + sw128(m, 1)) =
+          make_uint4(pack_bf16x2(u[8], u[9]), pack_bf16x2(u[10], u[11]), pack_bf16x2(u[12], u[13]),
+                     pack_bf16x2(u[14], u[15]));
+      fence_proxy_async();   // the features are read by the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.phi_full);
+    }
+    const float c0 = p.c0, lin0 = p.lin[0], q00 = p.quad[0], eps = p.eps;
+    float dsum = 0.f;
+    for (int kb = 0; kb < geo.nkb && ok; ++kb) {
+      const int b = kb & 1;
+      if (!mbar_wait(&s.s_full[b], (kb >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
+      tc_fence_after();
+      const int jbase = 32 * kb, jg0 = geo.ks + jbase;
+      uint32_t pk[16];
+      if (jg0 + 31 >= csw && jg0 <= rw1) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t sv[16], tv[16], uv[16];
+          tmem_ld16(tmem_lane_addr(tb, warp, kTkS + 32 * b + 16 * half), sv);
+          if (tu) {
+            tmem_ld16(tmem_lane_addr(tb, warp, kTkT + 32 * b + 16 * half), tv);
+            tmem_ld16(tmem_lane_addr(tb, warp, kTkU + 32 * b + 16 * half), uv);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) tv[e] = uv[e] = 0u;
+          }
+          tmem_wait_ld();
+#pragma unroll
+          for (int jj = 0; jj < 16; jj += 2) {
+            const int j0 = jbase + 16 * half + jj, jg = geo.ks + j0;
+            float kap[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float sx = __uint_as_float(sv[jj + e]);
+              if (mode) {
+                const float tx = __uint_as_float(tv[jj + e]), ux = __uint_as_float(uv[jj + e]);
+                kap[e] = fmaxf(fmaf(sx, fmaf(q00, sx, lin0 + ux), c0 + tx), eps);
+              } else {
+                kap[e] = (jg + e >= cs && jg + e <= i_tok)
+                             ? kappa_generic(p, sx, s.q, s.k, m, j0 + e) : 0.f;
+              }
+            }
+            pk[8 * half + (jj >> 1)] = pack_bf16x2((jg >= cs && jg <= i_tok) ? kap[0] : 0.f,
+                                                   (jg + 1 >= cs && jg + 1 <= i_tok) ? kap[1] : 0.f);
+          }
+        }
+        // denominator from the same rounded weights the P.V product uses
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162 *>(&pk[e]);
+          dsum += __low2float(pb) + __high2float(pb);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = 0u;
+      }
+      tmem_st16(tmem_lane_addr(tb, warp, kTkS + 32 * b), pk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.p_full[b]);
+    }
+    if (ok && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
+      tc_fence_after();
+      uint32_t d[64];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t r[16];
+        tmem_ld16(tmem_lane_addr(tb, warp, kTkI + 16 * q4), r);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) d[16 * q4 + e] = r[e];
+      }
+      tmem_wait_ld();
+      if (i_tok < args.T) {
+        const size_t row = ((size_t)bidx * args.Hq + h) * args.T + i_tok;
+        uint4 *dst = reinterpret_cast<uint4 *>(args.intra_num + row * 64);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) dst[e] = make_uint4(d[4 * e], d[4 * e + 1], d[4 * e + 2], d[4 * e + 3]);
+        args.intra_den[row] = dsum;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kIss) {
+    tc_fence_after();
+    tmem_dealloc(tb, kTkTmemCols);
   }
 }
 
@@ -1945,7 +2318,7 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   const size_t ssmem = sizeof(StateSmem) + 1024;
   const size_t rsmem1 = sizeof(ReadSmem<1>) + 1024;
   const size_t rsmem2 = sizeof(ReadSmem<2>) + 1024;
-  const size_t ismem = sizeof(IntraSmem<false>) + 1024;
+  const size_t tksmem = sizeof(TkSmem) + 1024;
   const size_t ismem_w = sizeof(IntraSmem<true>) + 1024;
   // shared-memory limits above 48 KB: a function attribute of each device
   static std::mutex attr_mutex;
@@ -1969,12 +2342,10 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
           cudaFuncSetAttribute(tc_readout_kernel<2>,
                                cudaFuncAttributePreferredSharedMemoryCarveout, 100) ==
               cudaSuccess &&
-          true;
+          cudaFuncSetAttribute(tc_intra_tk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tksmem) == cudaSuccess;
       for (int g = 1; ok && g <= kMaxG; ++g)
-        ok = cudaFuncSetAttribute(intra_kernel_for<false>(g),
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)ismem) == cudaSuccess &&
-             cudaFuncSetAttribute(intra_kernel_for<true>(g),
+        ok = cudaFuncSetAttribute(intra_kernel_for<true>(g),
                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)ismem_w) == cudaSuccess;
       if (!ok) {
@@ -2010,13 +2381,14 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   ra.intra_den = reinterpret_cast<float *>(w + lay.iden_off);
   ra.nh_per_block = kIntraNH;
   dim3 gi((ra.rho + kIntraNH - 1) / kIntraNH, lay.nS, lay.U);
-  if (chunk == 256)
+  if (chunk == 256) {
     launch_pdl(intra_kernel_for<true>(G), gi, dim3(kIntraThreads), ismem_w, stream, tmQ, tmKn, tmV,
                ra);
-  else
-    launch_pdl(intra_kernel_for<false>(G), gi, dim3(kIntraThreads), ismem, stream, tmQ, tmKn, tmV,
-               ra);
-  st = oal_after_launch("tc_intra_kernel", stream);
+    st = oal_after_launch("tc_intra_kernel", stream);
+  } else {
+    launch_pdl(tc_intra_tk_kernel, gi, dim3(kTkThreads), tksmem, stream, tmQ, tmKn, tmV, ra);
+    st = oal_after_launch("tc_intra_tk_kernel", stream);
+  }
   if (st != OAL_OK) return st;
   ra.nh_per_block = kMaxNH;
   dim3 g2((ra.rho + kMaxNH - 1) / kMaxNH, lay.nS, lay.U);
