@@ -317,8 +317,12 @@ class PrefillBench:
         self.y1 = torch.empty(B, Hq, D, dtype=self.Q.dtype, device=dev)
         self.ws_p = torch.empty(max(256, oal.oal_prefill_workspace_bytes(
             B, Hq, Hkv, Tp, D, D, self.dt, self.layout, chunk)), dtype=torch.uint8, device=dev)
-        self.ws_p1 = torch.empty(max(256, oal.oal_prefill_workspace_bytes(
-            1, Hq, Hkv, Tp, D, D, self.dt, self.layout, chunk)), dtype=torch.uint8, device=dev)
+        # the end-to-end pipeline's pieces: one sequence x kv_piece KV heads
+        # (a multiple of 4 KV heads keeps every state slice 16-byte aligned)
+        self.kv_piece = 4 if Hkv % 4 == 0 else Hkv
+        self.ws_e2e = [torch.empty(max(256, oal.oal_prefill_workspace_bytes(
+            1, Hq // Hkv * self.kv_piece, self.kv_piece, Tp, D, D, self.dt, self.layout, chunk)),
+            dtype=torch.uint8, device=dev) for _ in range(2)]
         self.ws_d = torch.empty(max(256, oal.oal_decode_workspace_bytes(B, Hq, Hkv, D, D,
                                                                         self.layout)),
                                 dtype=torch.uint8, device=dev)
@@ -452,9 +456,11 @@ class PrefillBench:
     def e2e(self, steps, warmup, world):
         """Step through the C ABI with host buffers: pinned host->device copies
         of every input and device->host copies of the outputs inside the timed
-        region.  The prefill runs one call per sequence (sequences are
-        independent), so sequence b+1's inputs copy in on one stream and
-        sequence b-1's output copies out on another while sequence b computes."""
+        region.  The prefill runs one call per piece of one sequence and
+        kv_piece KV heads (with their query heads; pieces are independent), on
+        two compute streams in turn, so later pieces' inputs copy in on one
+        stream and earlier pieces' outputs copy out on another while pieces
+        compute."""
         import torch
         oal, w = self.oal, self.w
         stream, Tp, B = self.stream, self.Tp, w.B
@@ -468,6 +474,10 @@ class PrefillBench:
         h2d = sum(t.numel() * t.element_size() for t in (Qp, Kp, Vp, q1p, k1p, v1p, Lp, gp))
         d2h = Yp.numel() * Yp.element_size() + y1p.numel() * y1p.element_size()
         cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+        sc = [torch.cuda.Stream(), torch.cuda.Stream()]
+        nk = self.kv_piece
+        nq = w.Hq // w.Hkv * nk
+        pieces = [(bb, g) for bb in range(B) for g in range(w.Hkv // nk)]
 
         def e2e_step(ev_start):
             cin.wait_event(ev_start)
@@ -477,9 +487,11 @@ class PrefillBench:
                 e_par = torch.cuda.Event()
                 e_par.record(cin)
                 e_in = []
-                for bb in range(B):
-                    for dst, src in ((self.Q, Qp), (self.K, Kp), (self.V, Vp)):
-                        dst[bb].copy_(src[bb], non_blocking=True)
+                for bb, g in pieces:
+                    hs, ks = slice(g * nq, (g + 1) * nq), slice(g * nk, (g + 1) * nk)
+                    self.Q[bb, hs].copy_(Qp[bb, hs], non_blocking=True)
+                    self.K[bb, ks].copy_(Kp[bb, ks], non_blocking=True)
+                    self.V[bb, ks].copy_(Vp[bb, ks], non_blocking=True)
                     e = torch.cuda.Event()
                     e.record(cin)
                     e_in.append(e)
@@ -490,17 +502,27 @@ class PrefillBench:
             stream.wait_event(e_par)
             oal.oal_expand_coeffs(self.L, self.group, w.eps, self.layout, self.a, self.b,
                                   self.C, stream=stream)
-            for bb in range(B):
-                stream.wait_event(e_in[bb])
-                oal.oal_prefill(self.Q[bb:bb + 1], self.K[bb:bb + 1], self.V[bb:bb + 1],
-                                self.L, self.group, w.eps, self.a, self.b, self.C, self.layout,
-                                state=self.state[bb:bb + 1], Y=self.Y[bb:bb + 1],
-                                chunk=self.chunk, workspace=self.ws_p1, stream=stream)
+            e_coef = torch.cuda.Event()
+            e_coef.record(stream)
+            e_done = []
+            for i, (bb, g) in enumerate(pieces):
+                s2 = sc[i % 2]
+                hs, ks = slice(g * nq, (g + 1) * nq), slice(g * nk, (g + 1) * nk)
+                s2.wait_event(e_coef)
+                s2.wait_event(e_in[i])
+                oal.oal_prefill(self.Q[bb:bb + 1, hs], self.K[bb:bb + 1, ks],
+                                self.V[bb:bb + 1, ks], self.L[hs], self.group[hs], w.eps,
+                                self.a[hs], self.b[hs], self.C[hs], self.layout,
+                                state=self.state[bb:bb + 1, ks], Y=self.Y[bb:bb + 1, hs],
+                                chunk=self.chunk, workspace=self.ws_e2e[i % 2], stream=s2)
                 e = torch.cuda.Event()
-                e.record(stream)
+                e.record(s2)
+                e_done.append(e)
                 cout.wait_event(e)
                 with torch.cuda.stream(cout):
-                    Yp[bb].copy_(self.Y[bb], non_blocking=True)
+                    Yp[bb, hs].copy_(self.Y[bb, hs], non_blocking=True)
+            for e in e_done[-2:]:
+                stream.wait_event(e)
             stream.wait_event(e_tok)
             oal.oal_decode_step(self.q1, self.k1, self.v1, self.a, self.b, self.C, self.state,
                                 self.layout, y=self.y1, workspace=self.ws_d, stream=stream)
@@ -533,8 +555,8 @@ class PrefillBench:
         return {"value": self.tokens_per_step * world * steps / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": 1e3 * e2e_s / steps,
-                "pipeline": "one prefill call per sequence; copies in and out on two "
-                            "streams beside the compute stream"}
+                "pipeline": "one prefill call per (sequence, %d KV heads) on two compute "
+                            "streams in turn; copies in and out on two more streams" % nk}
 
 
 def measure_prefill(cfg_idx, chunk, layout, steps, warmup, dev, stream, lib, pks, world=1,

@@ -81,6 +81,22 @@ def test_tc_prefill_wide_tail_group(oal, chunk):
     check_prefill(oal, w, chunk=chunk)
 
 
+@pytest.mark.parametrize("chunk", [64, 128])
+def test_tc_prefill_many_tail_dims_of_two(oal, chunk):
+    # five tail groups of two dims each: ten tail dims, every group within the
+    # fast form but more tail dims than the tensor-core kappa has features for
+    # (the intra-chunk kernel evaluates these heads from the Q and K tiles);
+    # a second launch keeps nine of them (the largest tensor-core case)
+    ten = [[1, 7], [12, 20], [33, 41], [47, 52], [58, 63]]
+    w = inputs.make_workload("tc-10", B=1, Hq=4, Hkv=2, T=300, G=6, seed=318,
+                             fixed_outliers=([7, 20, 41, 63], 9.0), fixed_groups=ten)
+    check_prefill(oal, w, chunk=chunk)
+    nine = [[1, 7], [12, 20], [33, 41], [47, 52], [58]]
+    w = inputs.make_workload("tc-9", B=1, Hq=4, Hkv=2, T=300, G=6, seed=319,
+                             fixed_outliers=([7, 20, 41, 58], 9.0), fixed_groups=nine)
+    check_prefill(oal, w, chunk=chunk)
+
+
 def test_tc_prefill_readout_general_weights(oal):
     # heads 0 and 2: the bulk row of L is zero, so M_bb = 0 and the readout
     # weights have no rank-one form; those heads take the general builder
