@@ -74,7 +74,7 @@ TRAFFIC = [
     # (kernel, source file, workload key (B, Hq, Hkv, T, G, layout, chunk), bytes per
     #  launch, source sha256)
     ("tc_readout_kernel", "prefill_tc.cu", (4, 32, 8, 8192, 6, "packed", 128),
-     1107291648 + 134631168, "6304ebd7a219a92fd04a53b21430c34e55343390bb2ae8ff1976e3d24e94331d"),
+     1103427328 + 134473216, "5a3ab21d71721ed7c67ddfe043f1487e11023e575f03c0253d47a38bb0154397"),
 ]
 
 
