@@ -1127,15 +1127,17 @@ __device__ __noinline__ void patch_exceptions(const RFactor &F, int hb, const __
   }
 }
 
-#define OAL_BUILD_CASE(n) \
-  case n:                 \
-    build_half<n, H>(qcol, alpha, p, cw, out); \
+#define OAL_BUILD_CASE(n)                     \
+  case n:                                     \
+    build_half<n, 0>(qcol, alpha, p, cw, out0); \
+    build_half<n, 1>(qcol, alpha, p, cw, out1); \
     break;
 
-template <int H>
+// Both halves of K block kb (one dispatch per K block).
 __device__ __forceinline__ void build_dispatch(int kb, const __nv_bfloat16 *qcol,
                                                const float *alpha, const uint32_t (&p)[32],
-                                               const uint32_t *cw, uint32_t (&out)[16]) {
+                                               const uint32_t *cw, uint32_t (&out0)[16],
+                                               uint32_t (&out1)[16]) {
   switch (kb) {
     OAL_BUILD_CASE(0) OAL_BUILD_CASE(1) OAL_BUILD_CASE(2) OAL_BUILD_CASE(3)
     OAL_BUILD_CASE(4) OAL_BUILD_CASE(5) OAL_BUILD_CASE(6) OAL_BUILD_CASE(7)
@@ -2095,8 +2097,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(p[i]));
         uint32_t out0[16], out1[16];
         if (factored) {
-          build_dispatch<0>(kb, qcol, F.alpha, p, cw, out0);
-          build_dispatch<1>(kb, qcol, F.alpha, p, cw, out1);
+          build_dispatch(kb, qcol, F.alpha, p, cw, out0, out1);
         } else {
           build_half_general(kb, 0, qcol, cw, out0);
           build_half_general(kb, 1, qcol, cw, out1);
