@@ -218,3 +218,26 @@ def test_decode_reductions(oal, B, Hq, Hkv):
         if layout == PACKED:
             S_ref = oracle.full_to_packed_state(S_ref, 64)
         assert rel_l2(S.cpu().numpy(), S_ref) <= TOL_S
+
+
+@pytest.mark.parametrize("layout", [FULL, PACKED])
+def test_prefill_slices_equal_one_call(oal, layout):
+    # every (batch, KV head) unit is independent: calls on slices of one
+    # sequence and four KV heads (with their query heads, the coefficient rows
+    # and the state slice) give the single call's outputs bit for bit (the
+    # end-to-end pipeline of bench.py runs the prefill this way)
+    w = inputs.make_workload("slices", B=2, Hq=16, Hkv=8, T=300, G=5, seed=340)
+    Q, K, V = w.torch_inputs("cuda")
+    L, group, a, b, C = params(oal, w, layout)
+    Y, S = oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, layout)
+    Y2, S2 = torch.empty_like(Y), torch.empty_like(S)
+    nk, nq = 4, 8
+    for bb in range(w.B):
+        for g in range(w.Hkv // nk):
+            hs, ks = slice(g * nq, (g + 1) * nq), slice(g * nk, (g + 1) * nk)
+            oal.oal_prefill(Q[bb:bb + 1, hs], K[bb:bb + 1, ks], V[bb:bb + 1, ks], L[hs], group[hs],
+                            w.eps, a[hs], b[hs], C[hs], layout, state=S2[bb:bb + 1, ks],
+                            Y=Y2[bb:bb + 1, hs])
+    oal.oal_sync_status()
+    assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))
+    assert torch.equal(S, S2)
