@@ -88,6 +88,7 @@ struct RFactor {
   float exc_wlo[kExcMax];      // weights of the low / high feature of each exception word
   float exc_whi[kExcMax];
   uint16_t exc_word[kExcMax];  // word index in the paired H2 order, ascending
+  uint16_t exc_rt[kExcMax];    // its row r and low feature t (r << 8 | t): features (r, t), (r, t + 1)
   uint8_t exc_start[72];       // exceptions of half block hb: [exc_start[hb], exc_start[hb + 1])
   int factored;
   int nexc;
@@ -384,17 +385,19 @@ tc_prep_kernel(const float *__restrict__ a, const float *__restrict__ b,
     if (tid >= 128 && tid < 128 + kExcMax) {
       const int i = tid - 128;
       float wl = 0.f, wh = 0.f;
-      uint16_t wd = 0;
+      uint16_t wd = 0, rt = 0;
       if (i < nlist) {
         wd = slist[i];
         const uint16_t cl = scode[2 * wd], ch = scode[2 * wd + 1];
         const int r = cl >> 8, tl = cl & 0xff, th = ch & 0xff;
         wl = tl < r ? 0.f : h2ws(r, tl);
         wh = th < r ? 0.f : h2ws(r, th);
+        rt = cl;
       }
       F->exc_wlo[i] = wl;
       F->exc_whi[i] = wh;
       F->exc_word[i] = wd;
+      F->exc_rt[i] = rt;
     }
     if (tid >= 160 && tid < 160 + 72) {
       const int hb = tid - 160;
@@ -1114,12 +1117,11 @@ __device__ __forceinline__ void build_half_general(int kb, int H, const __nv_bfl
 
 // Exception words of half block hb: their exact value q_r q_t w(r, t), stored
 // over the rank-one words already in tensor memory.
-__device__ __noinline__ void patch_exceptions(const RFactor &F, int hb, const __nv_bfloat16 *qcol,
+__device__ __forceinline__ void patch_exceptions(const RFactor &F, int hb, const __nv_bfloat16 *qcol,
                                               uint32_t taddr) {
   for (int e = F.exc_start[hb]; e < F.exc_start[hb + 1]; ++e) {
     const int wd = F.exc_word[e];
-    const uint16_t code = g_feat.code[2 * wd];
-    const int r = code >> 8, t = code & 0xff;
+    const int r = F.exc_rt[e] >> 8, t = F.exc_rt[e] & 0xff;
     const float qr = __uint_as_float(qt_ld(qcol, r) << 16);
     const float lo = qr * __uint_as_float(qt_ld(qcol, t) << 16) * F.exc_wlo[e];
     const float hi = qr * __uint_as_float(qt_ld(qcol, t + 1) << 16) * F.exc_whi[e];
