@@ -74,7 +74,7 @@ TRAFFIC = [
     # (kernel, source file, workload key (B, Hq, Hkv, T, G, layout, chunk), bytes per
     #  launch, source sha256)
     ("tc_readout_kernel", "prefill_tc.cu", (4, 32, 8, 8192, 6, "packed", 128),
-     1103427328 + 134473216, "5a3ab21d71721ed7c67ddfe043f1487e11023e575f03c0253d47a38bb0154397"),
+     1089952768 + 137383168, "9a4415e126204229dd9acf74ade384be5608be73ea7112ed6aa8080e7e6a0e82"),
     ("decode_stream_kernel", "decode.cu", (64, 14, 2, "full"),
      138927872 + 81893888, "dc614f7d1a9e9e3d434943fd0ae840ee4b469c5772d25043856ef3c21b3283a4"),
 ]
