@@ -24,9 +24,9 @@
 //
 // Launches per call:
 //   tc_prep_kernel      per query head: readout weights in the feature order
-//                       above (bf16) and their rank-one record, the
-//                       constants of the intra-chunk kernel evaluation; K^T
-//                       for the state kernel.
+//                       above (bf16) and their rank-one record, the plan of
+//                       the intra-chunk kappa (its quadratic form and the
+//                       tensor-core feature table); K^T for the state kernel.
 //   tc_state_kernel     mode 0 (only when the sequence is split into parts):
 //                       per (feature tile, part): the part's total
 //                       Delta S = sum phi(k_j) u_j^T.
@@ -34,10 +34,13 @@
 //                       stages with the fp32 running state in registers;
 //                       before each chunk write its bf16 snapshot S_{c-1};
 //                       the last part writes the final fp32 state.
-//   tc_intra_kernel     per (query head, 128-row tile): intra-chunk kappa
-//                       from s = Q K^T (UMMA) plus the tail-group sums (fp32
-//                       FMA) over the keys of each row's chunk, P.V by UMMA;
+//   tc_intra_tk_kernel  (C = 64, 128) per (query head, 128-row tile):
+//                       intra-chunk kappa from three UMMA products per
+//                       32-key block (s = Q K^T and the tail-dim feature
+//                       contractions T, U), three FMAs a pair, P.V by UMMA;
 //                       numerators and denominators to the workspace.
+//   tc_intra_kernel     (C = 256) the same with 256 keys a tile and the
+//                       tail-group sums and kappa in fp32 FMA.
 //   tc_readout_kernel   per (query head, 128-row tile, batch x KV head):
 //                       inter-chunk readout Phi~(Q) S_{c-1} as a
 //                       128 x 80 x 2192 UMMA (128 x 160 for C = 64: the
