@@ -1689,6 +1689,13 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     mbar_init(&s.d_full, 1);
     mbar_init(&s.never, 1);
     fence_mbar_init();
+    // Q, K and V are inputs of the call that no kernel of it writes: their
+    // loads start before the wait on the previous kernels
+    tma_prefetch_desc(&tmQ);
+    mbar_arrive_expect_tx(&s.qkv_full, 3u * kC * 64 * 2);
+    tma_load_3d(s.q, &tmQ, &s.qkv_full, 0, geo.row0, bidx * args.Hq + h);
+    tma_load_3d(s.k, &tmK, &s.qkv_full, 0, geo.ks, unit);
+    tma_load_3d(s.v, &tmV, &s.qkv_full, 0, geo.ks, unit);
   }
   if (warp == kIss) {
     tmem_alloc(&s.tmem_base, kTkTmemCols);
@@ -1770,14 +1777,8 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
     __syncwarp();
   } else if (warp == kTma) {
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      mbar_arrive_expect_tx(&s.qkv_full, 3u * kC * 64 * 2);
-      tma_load_3d(s.q, &tmQ, &s.qkv_full, 0, geo.row0, bidx * args.Hq + h);
-      tma_load_3d(s.k, &tmK, &s.qkv_full, 0, geo.ks, unit);
-      tma_load_3d(s.v, &tmV, &s.qkv_full, 0, geo.ks, unit);
-      mbar_wait_teardown(&s.qkv_full, 0, args.status);
-    }
+    // the loads issued at the start land before the block exits
+    if (lane == 0) mbar_wait_teardown(&s.qkv_full, 0, args.status);
     __syncwarp();
   } else {
     // warps 0-3, thread = query row m and key row m of the tile
