@@ -2316,7 +2316,7 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   kta.K = static_cast<const __nv_bfloat16 *>(K); kta.Kt = Kt;
   kta.T = T; kta.Tpad = Tpad; kta.U = lay.U; kta.nC = lay.nS;
   const int ntiles = lay.U * lay.nS;
-  const int ntr = (std::min(ntiles, 2 * 152) + Hq - 1) / Hq;   // block rows of transposes
+  const int ntr = (std::min(ntiles, 4 * 152) + Hq - 1) / Hq;   // block rows of transposes
   launch_pdl(tc_prep_kernel, dim3(Hq, (kKP + 255) / 256 + 2 + ntr), dim3(kPrepThreads), 0, stream, a, b, C,
              L, group, G, eps, packed, coef, plans, status, kta);
   oal_status st = oal_after_launch("tc_prep_kernel", stream);
