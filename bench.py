@@ -74,7 +74,7 @@ TRAFFIC = [
     # (kernel, source file, workload key (B, Hq, Hkv, T, G, layout, chunk), bytes per
     #  launch, source sha256)
     ("tc_readout_kernel", "prefill_tc.cu", (4, 32, 8, 8192, 6, "packed", 128),
-     1089952768 + 137383168, "adb329fc7c60013444ff412f33a047ee265ffd020cd8130c8842292a28108bab"),
+     1086846208 + 134253312, "d6c86669854815a1f0d7886a35a30e5a18bbf50cc433d448934f398005b3df65"),
     ("decode_stream_kernel", "decode.cu", (64, 14, 2, "full"),
      138927872 + 81893888, "dc614f7d1a9e9e3d434943fd0ae840ee4b469c5772d25043856ef3c21b3283a4"),
 ]
