@@ -1023,7 +1023,7 @@ static_assert(2 * (sizeof(ReadSmem<2>) + 2048) <= 228 * 1024, "two readout block
 struct ReadArgs {
   int T, nC, chunk, Hq, Hkv, rho, nh_per_block;
   __nv_bfloat16 *Y;
-  float *intra_num;            // [B*Hq][T][64] intra-chunk numerators
+  float *intra_num;            // intra-chunk numerators, per (B*Hq, 128-row tile) [16][128][4]
   float *intra_den;            // [B*Hq][T]     intra-chunk denominators
   const __nv_bfloat16 *coef;   // [Hq][kCoefRow]
   const KPlan *plans;          // [Hq]
@@ -1193,6 +1193,15 @@ struct __align__(1024) IntraSmem {
 static_assert(sizeof(IntraSmem<true>) + 1024 <= 113 * 1024, "two wide intra blocks per SM");
 
 // Geometry of a tile's keys and of one warp's rows.
+// Intra-chunk numerators in workspace: per (batch x query head, 128-row tile)
+// one 32 KB block [16][128][4] fp32, the 16-byte chunk e of tile row m at
+// [e][m], so the 32 rows of a warp write or read one chunk as 512 contiguous
+// bytes.  Denominators: [batch x query head][T] fp32.
+__device__ __forceinline__ uint4 *intra_tile(float *num, size_t bh, int T, int tile) {
+  const int nS = (T + kC - 1) / kC;
+  return reinterpret_cast<uint4 *>(num + (bh * nS + tile) * (size_t)(kC * 64));
+}
+
 struct IntraGeom {
   int row0;   // first query row of the tile
   int ks;     // first key: the start of row0's chunk
@@ -1570,11 +1579,12 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int e = 0; e < kIntraNH; ++e)
           if (e == hh) dsum = den_intra[e];
         if (i_tok < args.T) {
-          const size_t row = ((size_t)bidx * args.Hq + h0 + hh) * args.T + i_tok;
-          uint4 *dst = reinterpret_cast<uint4 *>(args.intra_num + row * 64);
+          const size_t bh = (size_t)bidx * args.Hq + h0 + hh;
+          uint4 *dst = intra_tile(args.intra_num, bh, args.T, geo.row0 / kC) + m;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) dst[e] = make_uint4(d[4 * e], d[4 * e + 1], d[4 * e + 2], d[4 * e + 3]);
-          args.intra_den[row] = dsum;
+          for (int e = 0; e < 16; ++e)
+            dst[kC * e] = make_uint4(d[4 * e], d[4 * e + 1], d[4 * e + 2], d[4 * e + 3]);
+          args.intra_den[bh * args.T + i_tok] = dsum;
         }
       }
     }
@@ -1893,11 +1903,12 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       }
       tmem_wait_ld();
       if (i_tok < args.T) {
-        const size_t row = ((size_t)bidx * args.Hq + h) * args.T + i_tok;
-        uint4 *dst = reinterpret_cast<uint4 *>(args.intra_num + row * 64);
+        const size_t bh = (size_t)bidx * args.Hq + h;
+        uint4 *dst = intra_tile(args.intra_num, bh, args.T, t) + m;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) dst[e] = make_uint4(d[4 * e], d[4 * e + 1], d[4 * e + 2], d[4 * e + 3]);
-        args.intra_den[row] = dsum;
+        for (int e = 0; e < 16; ++e)
+          dst[kC * e] = make_uint4(d[4 * e], d[4 * e + 1], d[4 * e + 2], d[4 * e + 3]);
+        args.intra_den[bh * args.T + i_tok] = dsum;
       }
     }
   }
@@ -1965,8 +1976,9 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     // the intra-chunk rows the epilogue reads, into L2 while the contraction runs
     const int rows = min(kC, args.T - c * kC);
     for (int h = 0; h < nh; ++h) {
-      const size_t row0 = ((size_t)bidx * args.Hq + h0 + h) * args.T + (size_t)c * kC;
-      prefetch_l2(args.intra_num + row0 * 64, (uint32_t)rows * 256u);
+      const size_t bh = (size_t)bidx * args.Hq + h0 + h;
+      const size_t row0 = bh * args.T + (size_t)c * kC;
+      prefetch_l2(intra_tile(args.intra_num, bh, args.T, c), kC * 64 * 4);
       const uintptr_t d0 = (reinterpret_cast<uintptr_t>(args.intra_den + row0) + 15) & ~uintptr_t(15);
       const uintptr_t d1 = reinterpret_cast<uintptr_t>(args.intra_den + row0 + rows) & ~uintptr_t(15);
       if (d1 > d0) prefetch_l2(reinterpret_cast<const void *>(d0), (uint32_t)(d1 - d0));
@@ -2153,12 +2165,14 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       // accumulator is read 16 columns at a time
       const int i_tok = c * kC + m;
       const bool row_ok = i_tok < args.T;
-      const size_t row = ((size_t)bidx * args.Hq + h0 + hh) * args.T + i_tok;
-      const float4 *src = reinterpret_cast<const float4 *>(args.intra_num + row * 64);
+      const size_t bh = (size_t)bidx * args.Hq + h0 + hh;
+      const size_t row = bh * args.T + i_tok;
+      const float4 *src = reinterpret_cast<const float4 *>(intra_tile(args.intra_num, bh, args.T, c) + m);
       float4 nv[16];
       float iden = 0.f;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) nv[e] = row_ok ? __ldg(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int e = 0; e < 16; ++e)
+        nv[e] = row_ok ? __ldg(src + kC * e) : make_float4(0.f, 0.f, 0.f, 0.f);
       if (row_ok) iden = __ldg(args.intra_den + row);
       // this row's columns of D: the second snapshot's (80 ..) for rows 64..127 when NS = 2
       const int dcol = kTmemD + 80 * hh + ((NS == 2 && m >= 64) ? kN : 0);
@@ -2257,7 +2271,7 @@ static Layout plan_layout(int B, int Hq, int Hkv, int T, int chunk) {
   L.ptot_off = o; o = al(o + (size_t)L.U * L.nparts * kTiles * 128 * kN * sizeof(float));
   L.coef_off = o; o = al(o + (size_t)Hq * kCoefRow * 2);
   L.plan_off = o; o = al(o + (size_t)Hq * sizeof(KPlan));
-  L.inum_off = o; o = al(o + (size_t)B * Hq * T * 64 * sizeof(float));
+  L.inum_off = o; o = al(o + (size_t)B * Hq * L.nS * kC * 64 * sizeof(float));
   L.iden_off = o; o = al(o + (size_t)B * Hq * T * sizeof(float));
   L.kt_off = o; o = al(o + (size_t)L.U * 64 * L.nS * kC * 2);
   L.total = o;
