@@ -20,6 +20,7 @@ oal_status launch_prefill_simt(const void *Q, const void *K, const void *V, int 
                                const float *b, const float *C, int packed, float *state,
                                int cont, void *Y, int chunk, void *ws, cudaStream_t stream);
 size_t tc_prefill_workspace_bytes(int B, int Hq, int Hkv, int T, int chunk);
+void set_intra_heads(int heads);
 oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B, int Hq,
                              int Hkv, int T, const float *L, const int32_t *group, int G,
                              float eps, const float *a, const float *b, const float *C,
@@ -438,6 +439,13 @@ oal_status oal_debug_wait_test(uint64_t wait_limit_cycles, int starve) {
   }
   if (e != cudaSuccess)
     return oal_fail(OAL_ERR_CUDA, "setting the wait test: %s", cudaGetErrorString(e));
+  return OAL_OK;
+}
+
+oal_status oal_debug_intra_heads(int heads) {
+  t_msg[0] = 0;
+  if (heads < 0 || heads > 2) return oal_fail(OAL_ERR_INVALID_ARG, "heads=%d", heads);
+  oal::set_intra_heads(heads);
   return OAL_OK;
 }
 

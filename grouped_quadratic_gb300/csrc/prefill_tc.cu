@@ -34,7 +34,7 @@
 //                       stages with the fp32 running state in registers;
 //                       before each chunk write its bf16 snapshot S_{c-1};
 //                       the last part writes the final fp32 state.
-//   tc_intra_tk_kernel  (C = 64, 128) per (query head, 128-row tile):
+//   tc_intra_tk_kernel  (C = 64, 128) per (one or two query heads, 128-row tile):
 //                       intra-chunk kappa from three UMMA products per
 //                       32-key block (s = Q K^T and the tail-dim feature
 //                       contractions T, U), three FMAs a pair, P.V by UMMA;
@@ -51,6 +51,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <utility>
 
@@ -158,15 +159,18 @@ __device__ __forceinline__ bool is_duplicate(uint16_t code) {
 // where s = q.k (unscaled) and s_g' = sum over the dims of tail group g' of
 // q_r k_r.  The bulk group g* (largest) is eliminated through
 // s_{g*} = s - sum_{g != g*} s_g; alpha/beta carry the 1/sqrt(64) scale.
-// Features of the tensor-core kappa of tc_intra_tk_kernel: the linear feature
-// of tail dim i at position i (i < kTkMaxLin), the pair (i, j), i <= j, at
-// kTkMaxLin + tk_pair(i, j); 54 of the 64 columns of a 128-byte row.
-constexpr int kTkMaxLin = 9;
+// Features of the tensor-core kappa of tc_intra_tk_kernel in a 64-column row:
+// T's linear feature of tail dim i at column i (i < kTkMaxLin), its pair
+// (i, j), i <= j, at kTkMaxLin + tk_pair(i, j) (44 columns, zero up to 48),
+// then U's linear feature of tail dim i at column kTkU0 + i.
+constexpr int kTkMaxLin = 8;
 constexpr int kTkFeat = kTkMaxLin + kTkMaxLin * (kTkMaxLin + 1) / 2;
+constexpr int kTkU0 = 48;
 __host__ __device__ constexpr int tk_pair(int i, int j) {
   return i * kTkMaxLin - i * (i - 1) / 2 + (j - i);
 }
-static_assert(kTkFeat <= 64, "tensor-core kappa features fit one K = 64 row");
+static_assert(kTkFeat <= kTkU0 && kTkU0 % 16 == 0 && kTkU0 + kTkMaxLin <= 64,
+              "T over K = 48 and U over K = 16 of one 64-column feature row");
 
 struct KPlan {
   float alpha[8];
@@ -1606,29 +1610,37 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 //       = sum_r lin_{g(r)} q_r k_r + sum_{r <= r'} w_{r r'} q_r q_r' k_r k_r'
 // over the tail dims r (w_{r r'} = quad_gh for dims of different groups,
 // 2 quad_gg for two dims of one group, quad_gg for r = r').  T and U are
-// contractions of per-query and per-key features over F <= 64 features, so
-// they run on the tensor cores beside s: per 32-key block, S = Q K^T, T =
-// A_T B^T, U = A_U B^T into tensor memory, with B = [k_r, k_r k_r'] (key
-// side) and A_T, A_U the query rows times the coefficients.  The CUDA cores
-// keep three FMAs per pair.  Heads whose features do not fit (more than 9
-// tail dims, or a group of more than two dims) evaluate kappa from the
-// tiles as the generic path of tc_intra_kernel does.
+// contractions of per-query and per-key features, so they run on the tensor
+// cores beside s: per 32-key block, S = Q K^T, T = A B^T over the feature
+// columns 0..47 and U = A B^T over the columns 48..63 into tensor memory,
+// with B = [k_r, k_r k_r' | k_r] (key side) and A the query rows times the
+// coefficients of T, then of U.  The CUDA cores keep three FMAs per pair.
+// Heads whose features do not fit (more than 8 tail dims, or a group of more
+// than two dims) evaluate kappa from the tiles as the generic path of
+// tc_intra_kernel does.
+//
+// A block serves one or two query heads of one KV head (nh_per_block; two
+// when the grid of one head a block would still fill the GPU several times),
+// one after the other: K, V and the key features are loaded or built once,
+// the query tiles arrive with them, and the second head's query features are
+// built while the first head's last P V products run.
 constexpr int kTkThreads = 192;          // warps 0-3: features, kappa, epilogue; 4: UMMA; 5: TMA
+constexpr int kTkHeads = 2;              // query heads per block at most
 constexpr int kTkS = 0;                  // s / P sub-tiles at 0 and 32
 constexpr int kTkT = 64;                 // T sub-tiles at 64 and 96
 constexpr int kTkU = 128;                // U sub-tiles at 128 and 160
 constexpr int kTkI = 192;                // numerators at [192, 256)
 constexpr uint32_t kTkTmemCols = 256;
+constexpr int kTkKB = 4;                 // 32-key blocks per head (C <= 128)
 struct __align__(1024) TkSmem {
-  __nv_bfloat16 q[kC * 64];   // 128B-swizzled [row][64] tiles
+  __nv_bfloat16 q[kTkHeads][kC * 64];  // 128B-swizzled [row][64] tiles
   __nv_bfloat16 k[kC * 64];
   __nv_bfloat16 v[kC * 64];
-  __nv_bfloat16 aT[kC * 64];  // query features for T, K-major, features past nfeat zero
-  __nv_bfloat16 aU[kC * 64];  // query features for U
-  __nv_bfloat16 bk[kC * 64];  // key features
-  KPlan plan;
-  uint64_t qkv_full, phi_full, s_full[2], p_full[2], s_free[2], d_full;
-  uint64_t never;             // failure-path tests: nothing arrives
+  __nv_bfloat16 a[kC * 64];            // query features, K-major: T at 0.., U at kTkU0..
+  __nv_bfloat16 bk[kC * 64];           // key features
+  KPlan plan[kTkHeads];
+  uint64_t qkv_full, phi_full, s_full[2], p_full[2], s_free[2], d_full, i_free, drain;
+  uint64_t never;                      // failure-path tests: nothing arrives
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -1647,11 +1659,12 @@ __host__ __device__ constexpr int tk_pair_j(int f) {
 static_assert(tk_pair_i(kTkMaxLin + tk_pair(3, 7)) == 3 && tk_pair_j(kTkMaxLin + tk_pair(3, 7)) == 7,
               "feature position of a pair");
 
-// Feature row of 8 features starting at F0 from the row's tail values:
-// key side k_i (k_i k_j), query side cT_f q_i (q_j), and (kU) cU_f q_i.
+// Eight features starting at F0 of the query row (a) and of the key row (b)
+// from the rows' tail values: T columns cT_f q_i (q_j) / k_i (k_j), U columns
+// cU_i q_i / k_i, zero elsewhere.
 template <int F0>
 __device__ __forceinline__ void tk_row_chunk(const float (&qv)[kTkMaxLin], const float (&kv)[kTkMaxLin],
-                                             const float *cT, uint4 &at, uint4 &bk) {
+                                             const float *cT, const float *cU, uint4 &at, uint4 &bk) {
   float a[8], b[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -1663,6 +1676,9 @@ __device__ __forceinline__ void tk_row_chunk(const float (&qv)[kTkMaxLin], const
       const int fi = tk_pair_i(f), fj = tk_pair_j(f);
       a[e] = cT[f] * qv[fi] * qv[fj];
       b[e] = kv[fi] * kv[fj];
+    } else if (f >= kTkU0 && f < kTkU0 + kTkMaxLin) {
+      a[e] = cU[f - kTkU0] * qv[f - kTkU0];
+      b[e] = kv[f - kTkU0];
     } else {
       a[e] = 0.f;
       b[e] = 0.f;
@@ -1674,6 +1690,27 @@ __device__ __forceinline__ void tk_row_chunk(const float (&qv)[kTkMaxLin], const
                   pack_bf16x2(b[6], b[7]));
 }
 
+// Query (and, with keys, key) feature rows of row m for plan p.
+__device__ __forceinline__ void tk_build_rows(TkSmem &s, const KPlan &p, const __nv_bfloat16 *qt,
+                                              int m, bool keys) {
+  float qv[kTkMaxLin], kv[kTkMaxLin];
+#pragma unroll
+  for (int i = 0; i < kTkMaxLin; ++i) {
+    const bool in = i < p.tk_nlin;
+    qv[i] = in ? bf16_at(qt, m, p.tk_dim[i]) : 0.f;
+    kv[i] = in ? bf16_at(s.k, m, p.tk_dim[i]) : 0.f;
+  }
+  uint8_t *ra = reinterpret_cast<uint8_t *>(s.a), *rb = reinterpret_cast<uint8_t *>(s.bk);
+  uint4 at, bk;
+#define OAL_TK_CHUNK(c)                                                       \
+  tk_row_chunk<8 * (c)>(qv, kv, p.tk_cT, p.tk_cU, at, bk);                   \
+  *reinterpret_cast<uint4 *>(ra + sw128(m, c)) = at;                          \
+  if (keys) *reinterpret_cast<uint4 *>(rb + sw128(m, c)) = bk;
+  OAL_TK_CHUNK(0) OAL_TK_CHUNK(1) OAL_TK_CHUNK(2) OAL_TK_CHUNK(3)
+  OAL_TK_CHUNK(4) OAL_TK_CHUNK(5) OAL_TK_CHUNK(6) OAL_TK_CHUNK(7)
+#undef OAL_TK_CHUNK
+}
+
 __global__ void __launch_bounds__(kTkThreads, 2)
 tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, ReadArgs args) {
@@ -1682,8 +1719,10 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   const int hg = blockIdx.x, t = blockIdx.y, unit = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bidx = unit / args.Hkv, kv = unit % args.Hkv;
-  const int h = kv * args.rho + hg;
-  const IntraGeom geo = intra_geom(t, args.chunk);   // 4 key blocks (C <= 128)
+  const int hpb = args.nh_per_block;               // 1 or 2 (<= kTkHeads)
+  const int h0 = kv * args.rho + hg * hpb;
+  const int nh = min(hpb, args.rho - hg * hpb);
+  const IntraGeom geo = intra_geom(t, args.chunk);   // kTkKB key blocks (C <= 128)
   constexpr int kIss = 4, kTma = 5;
   pdl_trigger();
 
@@ -1697,13 +1736,16 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_init(&s.s_free[i], 1);
     }
     mbar_init(&s.d_full, 1);
+    mbar_init(&s.i_free, 4);
+    mbar_init(&s.drain, 1);
     mbar_init(&s.never, 1);
     fence_mbar_init();
     // Q, K and V are inputs of the call that no kernel of it writes: their
     // loads start before the wait on the previous kernels
     tma_prefetch_desc(&tmQ);
-    mbar_arrive_expect_tx(&s.qkv_full, 3u * kC * 64 * 2);
-    tma_load_3d(s.q, &tmQ, &s.qkv_full, 0, geo.row0, bidx * args.Hq + h);
+    mbar_arrive_expect_tx(&s.qkv_full, (uint32_t)(nh + 2) * kC * 64 * 2);
+    for (int hh = 0; hh < nh; ++hh)
+      tma_load_3d(s.q[hh], &tmQ, &s.qkv_full, 0, geo.row0, bidx * args.Hq + h0 + hh);
     tma_load_3d(s.k, &tmK, &s.qkv_full, 0, geo.ks, unit);
     tma_load_3d(s.v, &tmV, &s.qkv_full, 0, geo.ks, unit);
   }
@@ -1712,78 +1754,91 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     tmem_relinquish();
   }
   pdl_wait();   // plans of the prep kernel; the intra rows of the previous call
-  for (int n = tid; n < (int)(sizeof(KPlan) / 4); n += kTkThreads)
-    reinterpret_cast<int *>(&s.plan)[n] = reinterpret_cast<const int *>(&args.plans[h])[n];
+  for (int n = tid; n < nh * (int)(sizeof(KPlan) / 4); n += kTkThreads) {
+    const int hh = n / (int)(sizeof(KPlan) / 4), e = n % (int)(sizeof(KPlan) / 4);
+    reinterpret_cast<int *>(&s.plan[hh])[e] = reinterpret_cast<const int *>(&args.plans[h0 + hh])[e];
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = s.tmem_base;
   volatile int *abort_flag = &s.abort_flag;
-  const int mode = s.plan.tk_mode;
 
   if (warp == kIss) {
-    if (lane == 0) {
+    {
+      // Key block g = kTkKB hh + kb of head hh uses s/P, T and U sub-tiles g & 1;
+      // every barrier of a sub-tile completes once per key block, in order.
       const uint32_t id32k = idesc_bf16_f32(128, 32, 0);
       const uint32_t id64mn = idesc_bf16_f32(128, 64, 1);
-      const uint64_t qdesc = sdesc_sw128(smem_u32(s.q), 16, 1024);
       const uint64_t kdesc0 = sdesc_sw128(smem_u32(s.k), 16, 1024);
       const uint64_t vdesc0 = sdesc_sw128(smem_u32(s.v), 16, 1024);
-      const uint64_t atdesc = sdesc_sw128(smem_u32(s.aT), 16, 1024);
-      const uint64_t audesc = sdesc_sw128(smem_u32(s.aU), 16, 1024);
+      const uint64_t adesc = sdesc_sw128(smem_u32(s.a), 16, 1024);
       const uint64_t bdesc0 = sdesc_sw128(smem_u32(s.bk), 16, 1024);
-      const bool tu = mode && s.plan.tk_nlin > 0;
-      // S = Q K^T of 32-key block kb, then (tu) T and U: K = 64 and 16 features
-      auto issue_s = [&](int kb) {
-        const uint64_t koff = (uint64_t)((32 * kb * 128) >> 4);
-        const uint32_t b = kb & 1;
-        umma_ss(tb + kTkS + 32 * b, qdesc, kdesc0 + koff, id32k, 0u);
-        umma_ss(tb + kTkS + 32 * b, qdesc + 2, kdesc0 + koff + 2, id32k, 1u);
-        umma_ss(tb + kTkS + 32 * b, qdesc + 4, kdesc0 + koff + 4, id32k, 1u);
-        umma_ss(tb + kTkS + 32 * b, qdesc + 6, kdesc0 + koff + 6, id32k, 1u);
-      };
-      auto issue_tu = [&](int kb) {
-        const uint64_t koff = (uint64_t)((32 * kb * 128) >> 4);
-        const uint32_t b = kb & 1;
-        if (tu) {
-#pragma unroll
-          for (int k2 = 0; k2 < 4; ++k2)
-            umma_ss(tb + kTkT + 32 * b, atdesc + 2 * k2, bdesc0 + koff + 2 * k2, id32k, k2 > 0 ? 1u : 0u);
-          umma_ss(tb + kTkU + 32 * b, audesc, bdesc0 + koff, id32k, 0u);
-        }
-        umma_commit(&s.s_full[b]);
-      };
       const bool starve = args.status[1] == kStarveIntra;   // failure-path test only
       bool ok = mbar_wait(starve ? &s.never : &s.qkv_full, 0, abort_flag, args.status);
-      if (ok) {
+      for (int hh = 0; hh < nh && ok; ++hh) {
+        const KPlan &p = s.plan[hh];
+        const bool tu = p.tk_mode && p.tk_nlin > 0;
+        const uint64_t qdesc = sdesc_sw128(smem_u32(s.q[hh]), 16, 1024);
+        const int g0 = kTkKB * hh;
+        // S = Q K^T of key block kb, then (tu) T over K = 48 and U over K = 16
+        auto issue_s = [&](int kb) {
+          const uint64_t koff = (uint64_t)((32 * kb * 128) >> 4);
+          const uint32_t b = (g0 + kb) & 1;
+          umma_ss_warp(tb + kTkS + 32 * b, qdesc, kdesc0 + koff, id32k, 0u);
+          umma_ss_warp(tb + kTkS + 32 * b, qdesc + 2, kdesc0 + koff + 2, id32k, 1u);
+          umma_ss_warp(tb + kTkS + 32 * b, qdesc + 4, kdesc0 + koff + 4, id32k, 1u);
+          umma_ss_warp(tb + kTkS + 32 * b, qdesc + 6, kdesc0 + koff + 6, id32k, 1u);
+        };
+        auto issue_tu = [&](int kb) {
+          const uint64_t koff = (uint64_t)((32 * kb * 128) >> 4);
+          const uint32_t b = (g0 + kb) & 1;
+          if (tu) {
+#pragma unroll
+            for (int k2 = 0; k2 < kTkU0 / 16; ++k2)
+              umma_ss_warp(tb + kTkT + 32 * b, adesc + 2 * k2, bdesc0 + koff + 2 * k2, id32k, k2 > 0 ? 1u : 0u);
+            umma_ss_warp(tb + kTkU + 32 * b, adesc + kTkU0 / 8, bdesc0 + koff + kTkU0 / 8, id32k, 0u);
+          }
+          umma_commit_warp(&s.s_full[b]);
+        };
+        if (hh > 0) {
+          // the previous head's last two P V products have read their P sub-tiles
+          for (int g = g0 - 2; g < g0 && ok; ++g)
+            ok = mbar_wait(&s.s_free[g & 1], (g >> 1) & 1, abort_flag, args.status);
+          if (!ok) break;
+        }
         // the first two S blocks need only Q and K: they run while the
         // feature rows are built
         tc_fence_after();
         issue_s(0);
-        if (geo.nkb > 1) issue_s(1);
-        ok = !tu || mbar_wait(&s.phi_full, 0, abort_flag, args.status);
-      }
-      if (ok) {
+        issue_s(1);
+        if (!mbar_wait(&s.phi_full, hh & 1, abort_flag, args.status)) break;
         tc_fence_after();
         issue_tu(0);
-        if (geo.nkb > 1) issue_tu(1);
-      }
-      for (int kb = 0; kb < geo.nkb && ok; ++kb) {
-        if (!mbar_wait(&s.p_full[kb & 1], (kb >> 1) & 1, abort_flag, args.status)) break;
-        tc_fence_after();
-        const uint32_t at = tb + kTkS + 32 * (kb & 1);
-        const uint64_t vd = vdesc0 + (uint64_t)((32 * kb * 128) >> 4);
-        umma_ts(tb + kTkI, at, vd, id64mn, kb > 0 ? 1u : 0u);
-        umma_ts(tb + kTkI, at + 8, vd + (2048 >> 4), id64mn, 1u);
-        umma_commit(&s.s_free[kb & 1]);
-        if (kb + 2 < geo.nkb) {
-          if (!mbar_wait(&s.s_free[kb & 1], (kb >> 1) & 1, abort_flag, args.status)) break;
+        issue_tu(1);
+        for (int kb = 0; kb < kTkKB && ok; ++kb) {
+          const int g = g0 + kb;
+          if (!mbar_wait(&s.p_full[g & 1], (g >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
+          // the numerators of the previous head are read out of tensor memory
+          if (kb == 0 && hh > 0 &&
+              !mbar_wait(&s.i_free, (hh - 1) & 1, abort_flag, args.status)) { ok = false; break; }
           tc_fence_after();
-          issue_s(kb + 2);
-          issue_tu(kb + 2);
+          const uint32_t at = tb + kTkS + 32 * (g & 1);
+          const uint64_t vd = vdesc0 + (uint64_t)((32 * kb * 128) >> 4);
+          umma_ts_warp(tb + kTkI, at, vd, id64mn, kb > 0 ? 1u : 0u);
+          umma_ts_warp(tb + kTkI, at + 8, vd + (2048 >> 4), id64mn, 1u);
+          umma_commit_warp(&s.s_free[g & 1]);
+          if (kb + 2 < kTkKB) {
+            if (!mbar_wait(&s.s_free[g & 1], (g >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(kb + 2);
+            issue_tu(kb + 2);
+          }
         }
+        umma_commit_warp(&s.d_full);
       }
-      umma_commit(&s.d_full);
-      mbar_wait_teardown(&s.d_full, 0, args.status);   // no MMA in flight at exit
+      umma_commit_warp(&s.drain);
+      if (lane == 0) mbar_wait_teardown(&s.drain, 0, args.status);   // no MMA in flight at exit
     }
     __syncwarp();
   } else if (warp == kTma) {
@@ -1798,100 +1853,91 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const int cs = (i_tok / C) * C;                  // this row's chunk starts here
     const int rw0 = geo.row0 + 32 * warp, rw1 = rw0 + 31;
     const int csw = (rw0 / C) * C;                   // the warp's rows share one chunk (C >= 64)
-    const KPlan &p = s.plan;
-    const bool tu = mode && p.tk_nlin > 0;   // (no tail dims: T = U = 0)
     bool ok = mbar_wait(&s.qkv_full, 0, abort_flag, args.status);
-    if (ok && tu) {
-      // the query and key features of row m: the row's tail values, then the
-      // 64-feature rows in registers, eight 16-byte stores per tile
-      float qv[kTkMaxLin], kv[kTkMaxLin];
-#pragma unroll
-      for (int i = 0; i < kTkMaxLin; ++i) {
-        const bool in = i < p.tk_nlin;
-        qv[i] = in ? bf16_at(s.q, m, p.tk_dim[i]) : 0.f;
-        kv[i] = in ? bf16_at(s.k, m, p.tk_dim[i]) : 0.f;
+    // the feature rows of head hh (the key rows too unless the previous
+    // head's tail dims are the same), then one arrival on phi_full
+    auto build = [&](int hh) {
+      const KPlan &p = s.plan[hh];
+      if (p.tk_mode && p.tk_nlin > 0) {
+        bool keys = hh == 0;
+        if (!keys) {
+          const KPlan &o = s.plan[hh - 1];
+          keys = !o.tk_mode || o.tk_nlin != p.tk_nlin;
+          for (int i = 0; i < kTkMaxLin; ++i) keys = keys || o.tk_dim[i] != p.tk_dim[i];
+        }
+        tk_build_rows(s, p, s.q[hh], m, keys);
+        fence_proxy_async();   // the features are read by the tensor cores
       }
-      uint8_t *rt = reinterpret_cast<uint8_t *>(s.aT), *ru = reinterpret_cast<uint8_t *>(s.aU);
-      uint8_t *rb = reinterpret_cast<uint8_t *>(s.bk);
-      uint4 at, bk;
-#define OAL_TK_CHUNK(c)                                                  \
-  tk_row_chunk<8 * (c)>(qv, kv, p.tk_cT, at, bk);                        \
-  *reinterpret_cast<uint4 *>(rt + sw128(m, c)) = at;                     \
-  *reinterpret_cast<uint4 *>(rb + sw128(m, c)) = bk;
-      OAL_TK_CHUNK(0) OAL_TK_CHUNK(1) OAL_TK_CHUNK(2) OAL_TK_CHUNK(3)
-      OAL_TK_CHUNK(4) OAL_TK_CHUNK(5) OAL_TK_CHUNK(6) OAL_TK_CHUNK(7)
-#undef OAL_TK_CHUNK
-      // U: the linear features (positions < 16; the rest of the row is unread)
-      float u[16];
-#pragma unroll
-      for (int f = 0; f < 16; ++f) u[f] = f < kTkMaxLin ? p.tk_cU[f < kTkMaxLin ? f : 0] * qv[f < kTkMaxLin ? f : 0] : 0.f;
-      *reinterpret_cast<uint4 *>(ru + sw128(m, 0)) =
-          make_uint4(pack_bf16x2(u[0], u[1]), pack_bf16x2(u[2], u[3]), pack_bf16x2(u[4], u[5]),
-                     pack_bf16x2(u[6], u[7]));
-      *reinterpret_cast<uint4 *>(ru + sw128(m, 1)) =
-          make_uint4(pack_bf16x2(u[8], u[9]), pack_bf16x2(u[10], u[11]), pack_bf16x2(u[12], u[13]),
-                     pack_bf16x2(u[14], u[15]));
-      fence_proxy_async();   // the features are read by the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.phi_full);
-    }
-    const float c0 = p.c0, lin0 = p.lin[0], q00 = p.quad[0], eps = p.eps;
-    float dsum = 0.f;
-    for (int kb = 0; kb < geo.nkb && ok; ++kb) {
-      const int b = kb & 1;
-      if (!mbar_wait(&s.s_full[b], (kb >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
-      tc_fence_after();
-      const int jbase = 32 * kb, jg0 = geo.ks + jbase;
-      uint32_t pk[16];
-      if (jg0 + 31 >= csw && jg0 <= rw1) {
+    };
+    if (ok) build(0);
+    for (int hh = 0; hh < nh && ok; ++hh) {
+      const KPlan &p = s.plan[hh];
+      const int mode = p.tk_mode;
+      const bool tu = mode && p.tk_nlin > 0;   // (no tail dims: T = U = 0)
+      const __nv_bfloat16 *qt = s.q[hh];
+      const float c0 = p.c0, lin0 = p.lin[0], q00 = p.quad[0], eps = p.eps;
+      float dsum = 0.f;
+      for (int kb = 0; kb < kTkKB; ++kb) {
+        const int g = kTkKB * hh + kb, b = g & 1;
+        if (!mbar_wait(&s.s_full[b], (g >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
+        tc_fence_after();
+        const int jbase = 32 * kb, jg0 = geo.ks + jbase;
+        uint32_t pk[16];
+        if (jg0 + 31 >= csw && jg0 <= rw1) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t sv[16], tv[16], uv[16];
-          tmem_ld16(tmem_lane_addr(tb, warp, kTkS + 32 * b + 16 * half), sv);
-          if (tu) {
-            tmem_ld16(tmem_lane_addr(tb, warp, kTkT + 32 * b + 16 * half), tv);
-            tmem_ld16(tmem_lane_addr(tb, warp, kTkU + 32 * b + 16 * half), uv);
-          } else {
+          for (int half = 0; half < 2; ++half) {
+            uint32_t sv[16], tv[16], uv[16];
+            tmem_ld16(tmem_lane_addr(tb, warp, kTkS + 32 * b + 16 * half), sv);
+            if (tu) {
+              tmem_ld16(tmem_lane_addr(tb, warp, kTkT + 32 * b + 16 * half), tv);
+              tmem_ld16(tmem_lane_addr(tb, warp, kTkU + 32 * b + 16 * half), uv);
+            } else {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) tv[e] = uv[e] = 0u;
-          }
-          tmem_wait_ld();
-#pragma unroll
-          for (int jj = 0; jj < 16; jj += 2) {
-            const int j0 = jbase + 16 * half + jj, jg = geo.ks + j0;
-            float kap[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float sx = __uint_as_float(sv[jj + e]);
-              if (mode) {
-                const float tx = __uint_as_float(tv[jj + e]), ux = __uint_as_float(uv[jj + e]);
-                kap[e] = fmaxf(fmaf(sx, fmaf(q00, sx, lin0 + ux), c0 + tx), eps);
-              } else {
-                kap[e] = (jg + e >= cs && jg + e <= i_tok)
-                             ? kappa_generic(p, sx, s.q, s.k, m, j0 + e) : 0.f;
-              }
+              for (int e = 0; e < 16; ++e) tv[e] = uv[e] = 0u;
             }
-            pk[8 * half + (jj >> 1)] = pack_bf16x2((jg >= cs && jg <= i_tok) ? kap[0] : 0.f,
-                                                   (jg + 1 >= cs && jg + 1 <= i_tok) ? kap[1] : 0.f);
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 2) {
+              const int j0 = jbase + 16 * half + jj, jg = geo.ks + j0;
+              float kap[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float sx = __uint_as_float(sv[jj + e]);
+                if (mode) {
+                  const float tx = __uint_as_float(tv[jj + e]), ux = __uint_as_float(uv[jj + e]);
+                  kap[e] = fmaxf(fmaf(sx, fmaf(q00, sx, lin0 + ux), c0 + tx), eps);
+                } else {
+                  kap[e] = (jg + e >= cs && jg + e <= i_tok)
+                               ? kappa_generic(p, sx, qt, s.k, m, j0 + e) : 0.f;
+                }
+              }
+              pk[8 * half + (jj >> 1)] = pack_bf16x2((jg >= cs && jg <= i_tok) ? kap[0] : 0.f,
+                                                     (jg + 1 >= cs && jg + 1 <= i_tok) ? kap[1] : 0.f);
+            }
           }
-        }
-        // denominator from the same rounded weights the P.V product uses
+          // denominator from the same rounded weights the P.V product uses
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162 *>(&pk[e]);
-          dsum += __low2float(pb) + __high2float(pb);
-        }
-      } else {
+          for (int e = 0; e < 16; ++e) {
+            const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162 *>(&pk[e]);
+            dsum += __low2float(pb) + __high2float(pb);
+          }
+        } else {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = 0u;
+          for (int e = 0; e < 16; ++e) pk[e] = 0u;
+        }
+        tmem_st16(tmem_lane_addr(tb, warp, kTkS + 32 * b), pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.p_full[b]);
       }
-      tmem_st16(tmem_lane_addr(tb, warp, kTkS + 32 * b), pk);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.p_full[b]);
-    }
-    if (ok && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
+      if (!ok) break;
+      // the last T and U products of this head are complete (their s_full
+      // arrived): the next head's features may overwrite the feature rows
+      if (hh + 1 < nh) build(hh + 1);
+      if (!mbar_wait(&s.d_full, hh & 1, abort_flag, args.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t d[64];
 #pragma unroll
@@ -1902,8 +1948,11 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         for (int e = 0; e < 16; ++e) d[16 * q4 + e] = r[e];
       }
       tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.i_free);
       if (i_tok < args.T) {
-        const size_t bh = (size_t)bidx * args.Hq + h;
+        const size_t bh = (size_t)bidx * args.Hq + h0 + hh;
         uint4 *dst = intra_tile(args.intra_num, bh, args.T, t) + m;
 #pragma unroll
         for (int e = 0; e < 16; ++e)
@@ -2298,6 +2347,10 @@ size_t tc_prefill_workspace_bytes(int B, int Hq, int Hkv, int T, int chunk) {
   return tcp::plan_layout(B, Hq, Hkv, T, chunk).total;
 }
 
+// Query heads per block of the tensor-core-kappa intra kernel: 0 = automatic.
+static std::atomic<int> g_intra_heads{0};
+void set_intra_heads(int heads) { g_intra_heads.store(heads); }
+
 oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B, int Hq,
                              int Hkv, int T, const float *L, const int32_t *group, int G,
                              float eps, const float *a, const float *b, const float *C,
@@ -2407,7 +2460,15 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
                ra);
     st = oal_after_launch("tc_intra_kernel", stream);
   } else {
-    launch_pdl(tc_intra_tk_kernel, gi, dim3(kTkThreads), tksmem, stream, tmQ, tmKn, tmV, ra);
+    // two heads a block once one head a block would make four waves of two
+    // blocks per SM
+    const int forced = g_intra_heads.load();
+    const int hpb = forced ? forced
+                           : ((size_t)ra.rho * lay.nS * lay.U >= (size_t)4 * 2 * 152 ? kTkHeads : 1);
+    ReadArgs rt = ra;
+    rt.nh_per_block = hpb;
+    dim3 gtk((ra.rho + hpb - 1) / hpb, lay.nS, lay.U);
+    launch_pdl(tc_intra_tk_kernel, gtk, dim3(kTkThreads), tksmem, stream, tmQ, tmKn, tmV, rt);
     st = oal_after_launch("tc_intra_tk_kernel", stream);
   }
   if (st != OAL_OK) return st;

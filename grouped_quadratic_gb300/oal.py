@@ -81,6 +81,8 @@ def load_library(path: str = LIB_PATH):
     lib.oal_sync_status.restype = ci
     lib.oal_debug_wait_test.argtypes = [ctypes.c_uint64, ci]
     lib.oal_debug_wait_test.restype = ci
+    lib.oal_debug_intra_heads.argtypes = [ci]
+    lib.oal_debug_intra_heads.restype = ci
     lib.oal_prefill_noalloc_scratch_bytes.argtypes = []
     lib.oal_prefill_noalloc_scratch_bytes.restype = sz
     lib.oal_last_error.argtypes = []
@@ -331,6 +333,12 @@ def oal_debug_wait_test(wait_limit_cycles=0, starve=0):
     nothing arrives on (0 none, 1 readout, 2 state, 3 intra-chunk), for kernels
     launched afterwards on the current device.  (0, 0) restores normal operation."""
     _check(load_library().oal_debug_wait_test(int(wait_limit_cycles), int(starve)))
+
+
+def oal_debug_intra_heads(heads=0):
+    """Test-only: query heads per block of the bf16 prefill's intra-chunk kernel
+    at chunk sizes 64 and 128 (1 or 2; 0 restores the automatic choice)."""
+    _check(load_library().oal_debug_intra_heads(int(heads)))
 
 
 def oal_last_error():

@@ -316,6 +316,16 @@ oal_status oal_sync_status(cudaStream_t stream);
 oal_status oal_debug_wait_test(uint64_t wait_limit_cycles, int starve);
 
 /*
+ * oal_debug_intra_heads -- for tests only.  The bf16 prefill's intra-chunk
+ * kernel at chunk sizes 64 and 128 serves one or two query heads of a KV head
+ * per block, two when one head a block would fill the GPU several times over.
+ * heads = 1 or 2 forces that choice for later prefill calls of this process;
+ * 0 restores the automatic one.  The results are the same bit for bit
+ * whichever is used.  Returns OAL_ERR_INVALID_ARG for other values.
+ */
+oal_status oal_debug_intra_heads(int heads);
+
+/*
  * Launch accounting and per-kernel timing, for benchmarks and tracing.
  *  oal_launch_counter: kernels this library has launched in this process.
  *  oal_set_launch_events: thread-local hook.  While `events` is non-null,

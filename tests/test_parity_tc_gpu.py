@@ -86,7 +86,7 @@ def test_tc_prefill_many_tail_dims_of_two(oal, chunk):
     # five tail groups of two dims each: ten tail dims, every group within the
     # fast form but more tail dims than the tensor-core kappa has features for
     # (the intra-chunk kernel evaluates these heads from the Q and K tiles);
-    # a second launch keeps nine of them (the largest tensor-core case)
+    # then nine (still too many) and eight (the largest tensor-core case)
     ten = [[1, 7], [12, 20], [33, 41], [47, 52], [58, 63]]
     w = inputs.make_workload("tc-10", B=1, Hq=4, Hkv=2, T=300, G=6, seed=318,
                              fixed_outliers=([7, 20, 41, 63], 9.0), fixed_groups=ten)
@@ -95,6 +95,48 @@ def test_tc_prefill_many_tail_dims_of_two(oal, chunk):
     w = inputs.make_workload("tc-9", B=1, Hq=4, Hkv=2, T=300, G=6, seed=319,
                              fixed_outliers=([7, 20, 41, 58], 9.0), fixed_groups=nine)
     check_prefill(oal, w, chunk=chunk)
+    eight = [[1, 7], [12, 20], [33, 41], [47, 52]]
+    w = inputs.make_workload("tc-8", B=1, Hq=4, Hkv=2, T=300, G=5, seed=320,
+                             fixed_outliers=([7, 20, 41, 52], 9.0), fixed_groups=eight)
+    check_prefill(oal, w, chunk=chunk)
+
+
+def run_prefill(oal, w, chunk, layout=PACKED):
+    Q, K, V = w.torch_inputs("cuda")
+    L, group, a, b, C = params(oal, w, layout)
+    Y, S = oal.oal_prefill(Q, K, V, L, group, w.eps, a, b, C, layout, chunk=chunk)
+    oal.oal_sync_status()
+    return Y.view(torch.int16).cpu().numpy(), S.cpu().numpy()
+
+
+@pytest.mark.parametrize("chunk", [64, 128])
+def test_tc_intra_two_heads_per_block(oal, chunk):
+    # the intra-chunk kernel's blocks of two query heads (the large-grid
+    # choice) forced on small cases: odd GQA ratios (a last block of one
+    # head), ragged lengths, heads of one KV head with different group counts
+    # (one head on the generic kappa path, its neighbour on the tensor-core
+    # path; different tail dims, so the key features are rebuilt): the same
+    # bits as one head a block, and the oracle's values
+    cases = []
+    cases.append(inputs.make_workload("tc-2h-a", B=2, Hq=6, Hkv=2, T=333, G=4, seed=330))
+    cases.append(inputs.make_workload("tc-2h-b", B=1, Hq=5, Hkv=1, T=129, G=6, seed=331))
+    w = inputs.make_workload("tc-2h-c", B=1, Hq=4, Hkv=1, T=260, G=4, seed=332)
+    # head 1: a tail group of three dims (generic kappa); head 2: G = 1
+    w.group[1] = 1
+    w.group[1, [3, 17, 40]] = 2
+    w.group[1, [58]] = 3
+    w.group[2] = 1
+    cases.append(w)
+    try:
+        for w in cases:
+            oal.oal_debug_intra_heads(1)
+            y1, s1 = run_prefill(oal, w, chunk)
+            oal.oal_debug_intra_heads(2)
+            y2, s2 = run_prefill(oal, w, chunk)
+            assert np.array_equal(y1, y2) and np.array_equal(s1, s2)
+            check_prefill(oal, w, chunk=chunk)
+    finally:
+        oal.oal_debug_intra_heads(0)
 
 
 def test_tc_prefill_readout_general_weights(oal):
