@@ -195,7 +195,9 @@ struct KPlan {
   int tk_dim[kTkMaxLin];
   float tk_cT[kTkFeat];
   float tk_cU[kTkMaxLin];
+  int pad_[3];                 // (a multiple of 16 bytes: copied by bulk copy)
 };
+static_assert(sizeof(KPlan) % 16 == 0, "plan size");
 
 // The dynamic shared memory rounded up to a 1024-byte boundary (swizzled
 // tiles need it), by pointer arithmetic on the shared array itself so the
@@ -1743,7 +1745,8 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     // Q, K and V are inputs of the call that no kernel of it writes: their
     // loads start before the wait on the previous kernels
     tma_prefetch_desc(&tmQ);
-    mbar_arrive_expect_tx(&s.qkv_full, (uint32_t)(nh + 2) * kC * 64 * 2);
+    // Q, K and V now, the heads' plans (the prep kernel's) after the wait below
+    mbar_arrive_expect_tx(&s.qkv_full, (uint32_t)((nh + 2) * kC * 64 * 2 + nh * sizeof(KPlan)));
     for (int hh = 0; hh < nh; ++hh)
       tma_load_3d(s.q[hh], &tmQ, &s.qkv_full, 0, geo.row0, bidx * args.Hq + h0 + hh);
     tma_load_3d(s.k, &tmK, &s.qkv_full, 0, geo.ks, unit);
@@ -1754,10 +1757,7 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     tmem_relinquish();
   }
   pdl_wait();   // plans of the prep kernel; the intra rows of the previous call
-  for (int n = tid; n < nh * (int)(sizeof(KPlan) / 4); n += kTkThreads) {
-    const int hh = n / (int)(sizeof(KPlan) / 4), e = n % (int)(sizeof(KPlan) / 4);
-    reinterpret_cast<int *>(&s.plan[hh])[e] = reinterpret_cast<const int *>(&args.plans[h0 + hh])[e];
-  }
+  if (tid == 0) bulk_load(s.plan, args.plans + h0, (uint32_t)(nh * sizeof(KPlan)), &s.qkv_full);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -2012,7 +2012,8 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     // before the wait on the previous kernels
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmS);
-    mbar_arrive_expect_tx(&s.qkv_full, (uint32_t)nh * kC * 64 * 2);
+    // Q now, the heads' weight rows (the prep kernel's) after the wait below
+    mbar_arrive_expect_tx(&s.qkv_full, (uint32_t)nh * (kC * 64 * 2 + kCoefRow * 2));
     for (int h = 0; h < nh; ++h)
       tma_load_3d(s.q[h], &tmQ, &s.qkv_full, 0, c * kC, bidx * args.Hq + h0 + h);
   }
@@ -2033,11 +2034,9 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       if (d1 > d0) prefetch_l2(reinterpret_cast<const void *>(d0), (uint32_t)(d1 - d0));
     }
   }
-  for (int n = tid; n < nh * (kCoefRow / 8); n += kReadThreads) {
-    const int hh = n / (kCoefRow / 8), e = n % (kCoefRow / 8);
-    reinterpret_cast<uint4 *>(s.coef[hh])[e] =
-        reinterpret_cast<const uint4 *>(args.coef + (size_t)(h0 + hh) * kCoefRow)[e];
-  }
+  if (tid == 0)
+    for (int h = 0; h < nh; ++h)
+      bulk_load(s.coef[h], args.coef + (size_t)(h0 + h) * kCoefRow, kCoefRow * 2, &s.qkv_full);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
