@@ -20,7 +20,8 @@ The JSON line also carries:
   e2e           the same step through the C ABI with host buffers: pinned
                 host->device copies of the inputs and device->host copies of
                 the outputs inside the timed region, pipelined per sequence
-                on two copy streams beside the compute stream;
+                (the last one in groups of 4 KV heads) on two copy streams
+                beside two compute streams;
   config1       the Qwen2.5-0.5B-shaped prefill (B=1, Hq=14, Hkv=2, T=4096,
                 G=4) measured the same way;
   config4       the long-context prefill (B=1, Hq=14, Hkv=2, T=65536, G=4) at
@@ -319,11 +320,15 @@ class PrefillBench:
         self.y1 = torch.empty(B, Hq, D, dtype=self.Q.dtype, device=dev)
         self.ws_p = torch.empty(max(256, oal.oal_prefill_workspace_bytes(
             B, Hq, Hkv, Tp, D, D, self.dt, self.layout, chunk)), dtype=torch.uint8, device=dev)
-        # the end-to-end pipeline's pieces: one sequence x kv_piece KV heads
-        # (a multiple of 4 KV heads keeps every state slice 16-byte aligned)
-        self.kv_piece = 4 if Hkv % 4 == 0 else Hkv
+        # the end-to-end pipeline's pieces (sequence, first KV head, KV heads):
+        # whole sequences, the last one split into groups of 4 KV heads (a
+        # multiple of 4 keeps every state slice 16-byte aligned) so that the
+        # work left after the last input lands is small
+        split = 4 if Hkv % 4 == 0 and Hkv > 4 else Hkv
+        self.pieces = [(bb, 0, Hkv) for bb in range(B - 1)] + \
+            [(B - 1, g, split) for g in range(0, Hkv, split)]
         self.ws_e2e = [torch.empty(max(256, oal.oal_prefill_workspace_bytes(
-            1, Hq // Hkv * self.kv_piece, self.kv_piece, Tp, D, D, self.dt, self.layout, chunk)),
+            1, Hq, Hkv, Tp, D, D, self.dt, self.layout, chunk)),
             dtype=torch.uint8, device=dev) for _ in range(2)]
         self.ws_d = torch.empty(max(256, oal.oal_decode_workspace_bytes(B, Hq, Hkv, D, D,
                                                                         self.layout)),
@@ -458,11 +463,12 @@ class PrefillBench:
     def e2e(self, steps, warmup, world):
         """Step through the C ABI with host buffers: pinned host->device copies
         of every input and device->host copies of the outputs inside the timed
-        region.  The prefill runs one call per piece of one sequence and
-        kv_piece KV heads (with their query heads; pieces are independent), on
-        two compute streams in turn, so later pieces' inputs copy in on one
-        stream and earlier pieces' outputs copy out on another while pieces
-        compute."""
+        region.  The prefill runs one call per piece (self.pieces: a sequence's
+        KV heads with their query heads; pieces are independent), on two
+        compute streams in turn, so later pieces' inputs copy in on one stream
+        and earlier pieces' outputs copy out on another while pieces compute.
+        The host link is the bound; the small last pieces shorten the compute
+        and copy-out left after the last input lands."""
         import torch
         oal, w = self.oal, self.w
         stream, Tp, B = self.stream, self.Tp, w.B
@@ -477,9 +483,8 @@ class PrefillBench:
         d2h = Yp.numel() * Yp.element_size() + y1p.numel() * y1p.element_size()
         cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
         sc = [torch.cuda.Stream(), torch.cuda.Stream()]
-        nk = self.kv_piece
-        nq = w.Hq // w.Hkv * nk
-        pieces = [(bb, g) for bb in range(B) for g in range(w.Hkv // nk)]
+        rho = w.Hq // w.Hkv
+        pieces = self.pieces
 
         def e2e_step(ev_start):
             cin.wait_event(ev_start)
@@ -489,8 +494,8 @@ class PrefillBench:
                 e_par = torch.cuda.Event()
                 e_par.record(cin)
                 e_in = []
-                for bb, g in pieces:
-                    hs, ks = slice(g * nq, (g + 1) * nq), slice(g * nk, (g + 1) * nk)
+                for bb, k0, nk in pieces:
+                    hs, ks = slice(k0 * rho, (k0 + nk) * rho), slice(k0, k0 + nk)
                     self.Q[bb, hs].copy_(Qp[bb, hs], non_blocking=True)
                     self.K[bb, ks].copy_(Kp[bb, ks], non_blocking=True)
                     self.V[bb, ks].copy_(Vp[bb, ks], non_blocking=True)
@@ -507,9 +512,9 @@ class PrefillBench:
             e_coef = torch.cuda.Event()
             e_coef.record(stream)
             e_done = []
-            for i, (bb, g) in enumerate(pieces):
+            for i, (bb, k0, nk) in enumerate(pieces):
                 s2 = sc[i % 2]
-                hs, ks = slice(g * nq, (g + 1) * nq), slice(g * nk, (g + 1) * nk)
+                hs, ks = slice(k0 * rho, (k0 + nk) * rho), slice(k0, k0 + nk)
                 s2.wait_event(e_coef)
                 s2.wait_event(e_in[i])
                 oal.oal_prefill(self.Q[bb:bb + 1, hs], self.K[bb:bb + 1, ks],
@@ -557,8 +562,10 @@ class PrefillBench:
         return {"value": self.tokens_per_step * world * steps / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": 1e3 * e2e_s / steps,
-                "pipeline": "one prefill call per (sequence, %d KV heads) on two compute "
-                            "streams in turn; copies in and out on two more streams" % nk}
+                "pipeline": "one prefill call per piece on two compute streams in turn, "
+                            "copies in and out on two more streams; pieces: %s" % ", ".join(
+                                "(seq %d, KV heads %d..%d)" % (bb, k0, k0 + nk - 1)
+                                for bb, k0, nk in self.pieces)}
 
 
 def measure_prefill(cfg_idx, chunk, layout, steps, warmup, dev, stream, lib, pks, world=1,
