@@ -17,7 +17,9 @@
 //                 row; the entry (r, r-1) of an odd row r duplicates
 //                 (r-1, r) (H2 is symmetric) and carries readout weight 0.
 //   [2112, 2176)  H1_r
-//   2176          H0, then 15 zero features
+//   2176          H0, then 15 zero features (the state's and the snapshots'
+//                 row length; the readout's contraction stops at 2176 and
+//                 adds the H0 term a S0 in its epilogue)
 // Readout weights per head (from the oal_expand_coeffs tables):
 //   H2: C_rt q_r q_t / 64 with multiplicity 2 for t > r (App. D packed
 //   readout), H1: b_r q_r / 8, H0: a.
@@ -43,7 +45,7 @@
 //                       tail-group sums and kappa in fp32 FMA.
 //   tc_readout_kernel   per (query head, 128-row tile, batch x KV head):
 //                       inter-chunk readout Phi~(Q) S_{c-1} as a
-//                       128 x 80 x 2192 UMMA (128 x 160 for C = 64: the
+//                       128 x 80 x 2176 UMMA (128 x 160 for C = 64: the
 //                       snapshots of the tile's two chunks side by side;
 //                       A = Phi~ built by threads straight into tensor
 //                       memory, B = snapshots streamed by TMA), plus the
@@ -66,7 +68,8 @@ using namespace oal::tc;
 constexpr int kC = 128;          // tokens per chunk
 constexpr int kKP = 2192;        // internal features
 constexpr int kH2P = 2112;       // paired H2 features
-constexpr int kNKB = 35;         // readout K blocks of 64 (the last one has K = 16)
+constexpr int kNKB = 34;         // readout K blocks of 64: 33 of paired H2 features, 1 of H1
+constexpr int kH0Feat = 2176;    // the H0 feature (constant term): added in the readout epilogue
 constexpr int kTiles = 18;       // 128-feature tiles of the state kernel
 constexpr int kN = 80;           // UMMA N of [v | 1]: 64 value columns, the "1" column, 15 zeros
 constexpr int kMaxNH = 1;        // query heads per readout block (four blocks per SM)
@@ -1022,6 +1025,7 @@ struct __align__(1024) ReadSmem {
   uint32_t tmem_base;
   int abort_flag;
   int loaded;                          // snapshot K blocks whose load was issued
+  float s0[NS][kU];                    // the snapshots' H0 rows (feature kH0Feat)
 };
 static_assert(4 * (sizeof(ReadSmem<1>) + 1024) <= 228 * 1024, "four readout blocks per SM");
 static_assert(2 * (sizeof(ReadSmem<2>) + 2048) <= 228 * 1024, "two readout blocks per SM");
@@ -1034,6 +1038,7 @@ struct ReadArgs {
   const __nv_bfloat16 *coef;   // [Hq][kCoefRow]
   const KPlan *plans;          // [Hq]
   int *status;
+  const __nv_bfloat16 *snap;   // [U*nC][kSnapRows][kKP] per-chunk snapshots
 };
 
 constexpr int kReadThreads = 160;   // 5 warps
@@ -1078,24 +1083,20 @@ __device__ __forceinline__ void h2_runs(const __nv_bfloat16 *qcol, const float *
 }
 
 // Words 16 H .. 16 H + 15 of K block KB of one A row (token row of Phi~(Q)),
-// rank-one form; cw = this head's weights of block KB (H1 and H0 blocks).
+// rank-one form; cw = this head's weights of block KB (the H1 block).
 template <int KB, int H>
 __device__ __forceinline__ void build_half(const __nv_bfloat16 *qcol, const float *alpha,
                                            const uint32_t (&p)[32], const uint32_t *cw,
                                            uint32_t (&out)[16]) {
   if constexpr (KB < 33) {
     h2_runs<KB, H, 0>(qcol, alpha, p, out);
-  } else if constexpr (KB < kNKB - 1) {
+  } else {
+    static_assert(KB == kNKB - 1, "the H1 block is the last");
 #pragma unroll
     for (int w = 0; w < 16; ++w) {
       const int t = 2 * (16 * H + w);
       out[w] = hmul2(qt_ld(qcol, t) | (qt_ld(qcol, t + 1) << 16), cw[16 * H + w]);
     }
-  } else {
-    // H0 block: feature 2176 carries a, the 15 after it are zero
-#pragma unroll
-    for (int w = 0; w < 16; ++w) out[w] = 0u;
-    if constexpr (H == 0) out[0] = cw[0] & 0xffffu;
   }
 }
 
@@ -1158,7 +1159,7 @@ __device__ __forceinline__ void build_dispatch(int kb, const __nv_bfloat16 *qcol
     OAL_BUILD_CASE(20) OAL_BUILD_CASE(21) OAL_BUILD_CASE(22) OAL_BUILD_CASE(23)
     OAL_BUILD_CASE(24) OAL_BUILD_CASE(25) OAL_BUILD_CASE(26) OAL_BUILD_CASE(27)
     OAL_BUILD_CASE(28) OAL_BUILD_CASE(29) OAL_BUILD_CASE(30) OAL_BUILD_CASE(31)
-    OAL_BUILD_CASE(32) OAL_BUILD_CASE(33) OAL_BUILD_CASE(34)
+    OAL_BUILD_CASE(32) OAL_BUILD_CASE(33)
     default: break;
   }
 }
@@ -2037,6 +2038,13 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   if (tid == 0)
     for (int h = 0; h < nh; ++h)
       bulk_load(s.coef[h], args.coef + (size_t)(h0 + h) * kCoefRow, kCoefRow * 2, &s.qkv_full);
+  for (int e = tid; e < NS * kU; e += kReadThreads) {
+    const int x = e / kU, n = e % kU;
+    float v = 0.f;   // (past the last chunk: rows past T only)
+    if (snap0 + x < args.nC)
+      v = __bfloat162float(args.snap[((size_t)(unit * args.nC + snap0 + x) * kSnapRows + n) * kKP + kH0Feat]);
+    s.s0[x][n] = v;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -2081,23 +2089,18 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           break;
         const uint64_t bd = bdesc0 + kStageStep * st;
         // K block kb: halves of K = 32 in half slots (2 kb) % nhs and
-        // (2 kb + 1) % nhs of this head (the last block: one half of K = 16);
+        // (2 kb + 1) % nhs of this head;
         // its builders arrive once, on the first half slot's barrier
         const int hs1 = hs + 1 == nhs ? 0 : hs + 1;
         if (!mbar_wait(&s.a_full[a0 + hs], fph, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t at0 = tb + kTmemA<NS> + 16 * (a0 + hs), at1 = tb + kTmemA<NS> + 16 * (a0 + hs1);
-        if (kb != kNKB - 1) {
-          umma_ts_warp(dt, at0, bd, id80, kb > 0 ? 1u : 0u);
-          umma_ts_warp(dt, at0 + 8, bd + 2, id80, 1u);
-          umma_ts_warp(dt, at1, bd + 4, id80, 1u);
-          umma_ts_warp(dt, at1 + 8, bd + 6, id80, 1u);
-          umma_commit_warp(&s.a_empty[a0 + hs]);
-          umma_commit_warp(&s.a_empty[a0 + hs1]);
-        } else {
-          umma_ts_warp(dt, at0, bd, id80, 1u);
-          umma_commit_warp(&s.a_empty[a0 + hs]);
-        }
+        umma_ts_warp(dt, at0, bd, id80, kb > 0 ? 1u : 0u);
+        umma_ts_warp(dt, at0 + 8, bd + 2, id80, 1u);
+        umma_ts_warp(dt, at1, bd + 4, id80, 1u);
+        umma_ts_warp(dt, at1 + 8, bd + 6, id80, 1u);
+        umma_commit_warp(&s.a_empty[a0 + hs]);
+        umma_commit_warp(&s.a_empty[a0 + hs1]);
         hs = hs1 + 1 == nhs ? 0 : hs1 + 1;
         if (++fk == fper) { fk = 0; fph ^= 1; }
         if (++st == kNB) { st = 0; sph ^= 1; }
@@ -2171,7 +2174,6 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         // half index hx = 2 kb + H goes to half slot hx % nhs, its (hx / nhs)-th
         // use: wait for the MMAs of its previous use, store, arrive once
         const uint32_t xb = 2 * kb < 64 ? (uint32_t)(em >> (2 * kb)) & 3u : (em2 >> (2 * kb - 64)) & 3u;
-        const bool two = kb != kNKB - 1;   // the last block has one half
         const int hs1 = hs + 1 == nhs ? 0 : hs + 1;
         const uint32_t par0 = ((uph >> hs) & 1u) ^ 1u, par1 = ((uph >> hs1) & 1u) ^ 1u;
         uint64_t *e0 = &s.a_empty[a0 + hs], *e1 = &s.a_empty[a0 + hs1];
@@ -2188,10 +2190,8 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const uint32_t ta0 = tmem_lane_addr(tb, warp, kTmemA<NS> + 16 * (a0 + hs));
         const uint32_t ta1 = tmem_lane_addr(tb, warp, kTmemA<NS> + 16 * (a0 + hs1));
         tmem_st16(ta0, out0);
-        if (two) {
-          if (!mbar_test(e1, par1) && !mbar_wait(e1, par1, abort_flag, args.status)) break;
-          tmem_st16(ta1, out1);
-        }
+        if (!mbar_test(e1, par1) && !mbar_wait(e1, par1, abort_flag, args.status)) break;
+        tmem_st16(ta1, out1);
         if (xb) {
           tmem_wait_st();
           if (xb & 1u) patch_exceptions(F, 2 * kb, qcol, ta0);
@@ -2201,7 +2201,7 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.a_full[a0 + hs]);
-        uph ^= (1u << hs) | (two ? 1u << hs1 : 0u);
+        uph ^= (1u << hs) | (1u << hs1);
         hs = hs1 + 1 == nhs ? 0 : hs1 + 1;
       }
       tmem_wait_st();   // (a loop left early may have a store in flight)
@@ -2227,9 +2227,12 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       if (!*abort_flag && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
         tc_fence_after();
         uint32_t r[16];
+        // the H0 term a S0 (one product: the MMA's last K block held it before)
+        const float a0w = __bfloat162float(s.coef[hh][kH0Feat]);
+        const float *s0 = s.s0[(NS == 2 && m >= 64) ? 1 : 0];
         tmem_ld16(tmem_lane_addr(tb, warp, dcol + 64), r);
         tmem_wait_ld();
-        const float inv = 1.0f / (__uint_as_float(r[0]) + iden);
+        const float inv = 1.0f / (fmaf(a0w, s0[64], __uint_as_float(r[0])) + iden);
         uint4 *dst = reinterpret_cast<uint4 *>(args.Y + row * kDv);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -2239,10 +2242,11 @@ tc_readout_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float4 n4 = nv[4 * q4 + e];
-            pk[2 * e] = pack_bf16x2((__uint_as_float(r[4 * e]) + n4.x) * inv,
-                                    (__uint_as_float(r[4 * e + 1]) + n4.y) * inv);
-            pk[2 * e + 1] = pack_bf16x2((__uint_as_float(r[4 * e + 2]) + n4.z) * inv,
-                                        (__uint_as_float(r[4 * e + 3]) + n4.w) * inv);
+            const int n = 16 * q4 + 4 * e;
+            pk[2 * e] = pack_bf16x2((fmaf(a0w, s0[n], __uint_as_float(r[4 * e])) + n4.x) * inv,
+                                    (fmaf(a0w, s0[n + 1], __uint_as_float(r[4 * e + 1])) + n4.y) * inv);
+            pk[2 * e + 1] = pack_bf16x2((fmaf(a0w, s0[n + 2], __uint_as_float(r[4 * e + 2])) + n4.z) * inv,
+                                        (fmaf(a0w, s0[n + 3], __uint_as_float(r[4 * e + 3])) + n4.w) * inv);
           }
           if (row_ok) {
             dst[2 * q4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -2449,7 +2453,7 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   ReadArgs ra;
   ra.T = T; ra.nC = lay.nC; ra.chunk = chunk; ra.Hq = Hq; ra.Hkv = Hkv; ra.rho = Hq / Hkv;
   ra.Y = static_cast<__nv_bfloat16 *>(Y);
-  ra.coef = coef; ra.plans = plans; ra.status = status;
+  ra.coef = coef; ra.plans = plans; ra.status = status; ra.snap = snap;
   ra.intra_num = reinterpret_cast<float *>(w + lay.inum_off);
   ra.intra_den = reinterpret_cast<float *>(w + lay.iden_off);
   ra.nh_per_block = kIntraNH;
