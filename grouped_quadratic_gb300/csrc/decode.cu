@@ -518,8 +518,8 @@ static size_t decode_smem_floats(int rpb) {
 }
 
 // The cluster kernel serves batches whose clusters (one per batch x KV
-// head) all fit the GPU at once.
-static bool use_clusters(size_t units) { return units * 16 <= 2 * 152; }
+// head, of 16 blocks or, for more than 19 units, 8) all fit the GPU at once.
+static bool use_clusters(size_t units) { return units * 8 <= 2 * 152; }
 
 // Work split of the streaming kernel: items (batch x KV head, slice), runs of
 // per_block consecutive items, one run per block (a run never spans more than
@@ -619,7 +619,7 @@ static oal_status launch_decode_t(const Tin *q, const Tin *k, const Tin *v, int 
     attr_set[dev] = true;
   }
   if (use_clusters(units)) {
-    const int cs = decode_cluster_size<Tin>(packed);
+    const int cs = units * 16 <= 2 * 152 ? decode_cluster_size<Tin>(packed) : 8;
     const int rpb = ((F + cs - 1) / cs + 3) & ~3;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

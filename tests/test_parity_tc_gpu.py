@@ -236,9 +236,11 @@ def test_tc_prefill_continuation(oal, layout, chunk):
     assert rel_l2(S.cpu().numpy(), S_ref) <= TOL_S
 
 
-@pytest.mark.parametrize("B,Hq,Hkv", [(1, 16, 2), (2, 6, 3), (20, 4, 2), (24, 16, 2)])
+@pytest.mark.parametrize("B,Hq,Hkv", [(1, 16, 2), (2, 6, 3), (16, 8, 2), (20, 4, 2),
+                                      (24, 16, 2)])
 def test_decode_reductions(oal, B, Hq, Hkv):
-    # B * Hkv <= 19: slices meet in a thread-block cluster; 40 and 48: the
+    # B * Hkv <= 19: slices meet in a thread-block cluster of 16 blocks; 32:
+    # clusters of 8; 40 and 48: the
     # streaming kernel (runs of slices crossing (batch, KV head) boundaries,
     # eight query heads per KV head in the last case) and its finishing kernel
     w = inputs.make_workload("dec-red", B=B, Hq=Hq, Hkv=Hkv, T=40 + 3, G=4, seed=360 + B,
