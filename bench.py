@@ -77,7 +77,7 @@ TRAFFIC = [
     ("tc_readout_kernel", "prefill_tc.cu", (4, 32, 8, 8192, 6, "packed", 128),
      1103470848 + 120884224, "a3abf419b6d540b4b419edbb18aa5e059c07a35dd54cec53b9bd1a00ca50da0b"),
     ("decode_stream_kernel", "decode.cu", (64, 14, 2, "full"),
-     138927872 + 81893888, "dc614f7d1a9e9e3d434943fd0ae840ee4b469c5772d25043856ef3c21b3283a4"),
+     138927872 + 81893888, "0147d4d17b168bad5f1527d1d50dd9e605973467cd8f82b2714e8ac749a363fe"),
 ]
 
 
