@@ -75,7 +75,7 @@ TRAFFIC = [
     # (kernel, source file, workload key (B, Hq, Hkv, T, G, layout, chunk), bytes per
     #  launch, source sha256)
     ("tc_readout_kernel", "prefill_tc.cu", (4, 32, 8, 8192, 6, "packed", 128),
-     1103470848 + 120884224, "a3abf419b6d540b4b419edbb18aa5e059c07a35dd54cec53b9bd1a00ca50da0b"),
+     1103470848 + 120884224, "a14fccb057ced4be7cd21ff10807f399b2b408d6b5682ae689f41066d1fed96f"),
     ("decode_stream_kernel", "decode.cu", (64, 14, 2, "full"),
      138927872 + 81893888, "0147d4d17b168bad5f1527d1d50dd9e605973467cd8f82b2714e8ac749a363fe"),
 ]

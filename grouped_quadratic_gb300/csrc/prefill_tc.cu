@@ -36,13 +36,13 @@
 //                       stages with the fp32 running state in registers;
 //                       before each chunk write its bf16 snapshot S_{c-1};
 //                       the last part writes the final fp32 state.
-//   tc_intra_tk_kernel  (C = 64, 128) per (one or two query heads, 128-row tile):
+//   tc_intra_tk_kernel  per (one or two query heads, 128-row tile):
 //                       intra-chunk kappa from three UMMA products per
 //                       32-key block (s = Q K^T and the tail-dim feature
 //                       contractions T, U), three FMAs a pair, P.V by UMMA;
-//                       numerators and denominators to the workspace.
-//   tc_intra_kernel     (C = 256) the same with 256 keys a tile and the
-//                       tail-group sums and kappa in fp32 FMA.
+//                       numerators and denominators to the workspace.  The
+//                       second half of a 256-token chunk has 256 keys: its
+//                       second 128-key tile reloads K and V.
 //   tc_readout_kernel   per (query head, 128-row tile, batch x KV head):
 //                       inter-chunk readout Phi~(Q) S_{c-1} as a
 //                       128 x 80 x 2176 UMMA (128 x 160 for C = 64: the
@@ -1165,41 +1165,7 @@ __device__ __forceinline__ void build_dispatch(int kb, const __nv_bfloat16 *qcol
 }
 #undef OAL_BUILD_CASE
 
-// ---------------------------------------------------------------- intra kernel
-// Intra-chunk part of Eq. (25): sum over the keys j of the query's own chunk
-// with j <= i of kappa(q_i, k_j) u_j, per query row, written to workspace for
-// the readout's epilogue.  One block per (query head, 128-row tile, batch x KV
-// head).  The keys of a tile are those of its chunk up to the tile's last row:
-// 128 (C = 64, 128; for C = 64 the tile's two chunks are told apart by the
-// mask), or 256 for the second half of a 256-token chunk.  The chunk sizes of
-// 64 and 128 run tc_intra_tk_kernel below; this kernel serves C = 256 (256
-// keys a tile, templated on the group count).  Per 32-key block:
-// s = Q K^T by UMMA into tensor memory, the tail-group sums and kappa in fp32
-// on the CUDA cores, P = bf16(kappa) masked to the chunk's causal pairs written
-// back over s, numerators += P V by UMMA.
-constexpr int kIntraNH = 1;              // query heads per intra-chunk block
-constexpr int kTailSlots = 2 * kMaxTailG;
-constexpr int kIntraThreads = 192;       // 6 warps
-constexpr int kTmemS = 0;                // two 32-key s / P sub-tiles at 0 and 32
-constexpr int kTmemI = 64;               // numerators at [64, 128)
-constexpr uint32_t kIntraTmemCols = 128;
-
-template <bool kWide>
-struct __align__(1024) IntraSmem {
-  static constexpr int kKeys = kWide ? 256 : 128;
-  __nv_bfloat16 q[kIntraNH][kC * 64];
-  __nv_bfloat16 k[kKeys * 64];
-  __nv_bfloat16 v[kKeys * 64];
-  float kt[kIntraNH][kTailSlots][kKeys];   // tail-dim key values (fast path), key-major
-  KPlan plan[kIntraNH];
-  uint64_t qkv_full, s_full[2], p_full[2], s_free[2], d_full;
-  uint64_t never;                          // failure-path tests: nothing arrives
-  uint32_t tmem_base;
-  int abort_flag;
-};
-static_assert(sizeof(IntraSmem<true>) + 1024 <= 113 * 1024, "two wide intra blocks per SM");
-
-// Geometry of a tile's keys and of one warp's rows.
+// ---------------------------------------------------------------- intra-chunk helpers
 // Intra-chunk numerators in workspace: per (batch x query head, 128-row tile)
 // one 32 KB block [16][128][4] fp32, the 16-byte chunk e of tile row m at
 // [e][m], so the 32 rows of a warp write or read one chunk as 512 contiguous
@@ -1228,68 +1194,6 @@ __device__ __forceinline__ float bf16_at(const __nv_bfloat16 *tile, int row, int
       base + sw128(row, col >> 3) + (col & 7) * 2));
 }
 
-// ---- intra-chunk kernel evaluation (Eq. 7) for one 32-key block.
-// Fast path: every tail group has <= 2 dims, constants in registers.
-template <int G>
-struct KConst {
-  float c0, eps;
-  float lin[G];
-  float quad[G * (G + 1) / 2];
-};
-
-// kappa of one pair from s = q.k and the tail-group sums (fast path: every
-// tail group has <= 2 dims).  qt: this query's tail values; ktj: the key's.
-template <int G>
-__device__ __forceinline__ float kappa_g(const KConst<G> &k, float s, const float (&qt)[2 * kMaxTailG],
-                                         const float *ktj) {
-  float z[G];
-  z[0] = s;
-#pragma unroll
-  for (int g = 1; g < G; ++g)
-    z[g] = fmaf(qt[2 * g - 2], ktj[2 * g - 2], qt[2 * g - 1] * ktj[2 * g - 1]);
-  float kap = k.c0;
-  int qi = 0;
-#pragma unroll
-  for (int v = 0; v < G; ++v) {
-    float inner = k.lin[v];
-#pragma unroll
-    for (int w = v; w < G; ++w) inner = fmaf(k.quad[qi++], z[w], inner);
-    kap = fmaf(z[v], inner, kap);
-  }
-  return fmaxf(kap, k.eps);
-}
-
-// kappa of two keys (j, j + 1) for one query row, two lanes per packed fp32
-// instruction.  kt: this head's key-major tail values (rows of `stride` keys),
-// offset to key j.
-template <int G>
-__device__ __forceinline__ float2 kappa2_g(const KConst<G> &k, float2 s,
-                                          const float (&qt)[2 * kMaxTailG], const float *kt,
-                                          int stride) {
-  float2 z[G];
-  z[0] = s;
-#pragma unroll
-  for (int g = 1; g < G; ++g) {
-    const float2 a = *reinterpret_cast<const float2 *>(kt + (2 * g - 2) * stride);
-    const float2 b = *reinterpret_cast<const float2 *>(kt + (2 * g - 1) * stride);
-    z[g] = ffma2(make_float2(qt[2 * g - 2], qt[2 * g - 2]), a,
-                 make_float2(qt[2 * g - 1] * b.x, qt[2 * g - 1] * b.y));
-  }
-  float2 kap = make_float2(k.c0, k.c0);
-  int qi = 0;
-#pragma unroll
-  for (int v = 0; v < G; ++v) {
-    float2 inner = make_float2(k.lin[v], k.lin[v]);
-#pragma unroll
-    for (int w = v; w < G; ++w) {
-      inner = ffma2(make_float2(k.quad[qi], k.quad[qi]), z[w], inner);
-      ++qi;
-    }
-    kap = ffma2(z[v], inner, kap);
-  }
-  return make_float2(fmaxf(kap.x, k.eps), fmaxf(kap.y, k.eps));
-}
-
 // Generic path (a tail group with more than 2 dims): sums straight from the
 // Q and K tiles, constants from shared memory.
 __device__ float kappa_generic(const KPlan &p, float s, const __nv_bfloat16 *qtile,
@@ -1311,302 +1215,9 @@ __device__ float kappa_generic(const KPlan &p, float s, const __nv_bfloat16 *qti
   return kap;
 }
 
-// The intra-chunk role (warps 0-3, thread = query row): for each 32-key block
-// of the tile's keys, read s = q.k of this row from tensor memory, turn it
-// into kappa (masked to the keys j of the row's chunk with j <= i), write P
-// (bf16) back in place for the P.V UMMA, and accumulate the denominator from
-// the same rounded weights.  The two 32-key sub-tiles alternate, so the UMMAs
-// of one block overlap the kappa work of the next.  A warp skips the kappa of
-// a block none of its rows reaches (its P is zero).
-template <int G, bool kWide>
-__device__ bool intra_worker(IntraSmem<kWide> &s, const ReadArgs &args, const IntraGeom &geo,
-                             int nh, int warp, int lane, uint32_t tb,
-                             float (&den_intra)[kIntraNH]) {
-  constexpr int kKeys = IntraSmem<kWide>::kKeys;
-  volatile int *abort_flag = &s.abort_flag;
-  const int m = threadIdx.x;
-  const int C = args.chunk;
-  const int i_tok = geo.row0 + m;
-  const int cs = (i_tok / C) * C;                  // this row's chunk starts here
-  const int rw0 = geo.row0 + 32 * (warp & 3), rw1 = rw0 + 31;
-  const int csw = (rw0 / C) * C;                   // the warp's rows share one chunk (C >= 64)
-  if (!mbar_wait(&s.qkv_full, 0, abort_flag, args.status)) return false;
-  // tail-dim key values of every head (fast path); thread = key row m (and m + 128)
-  for (int hh = 0; hh < nh; ++hh) {
-    const KPlan &p = s.plan[hh];
-#pragma unroll
-    for (int x = 0; x < kKeys / kC; ++x) {
-      const int j = m + kC * x;
-#pragma unroll
-      for (int g = 0; g < kMaxTailG; ++g) {
-        float k0 = 0.f, k1 = 0.f;
-        if (g < p.ntg && p.nd[g] > 0) k0 = bf16_at(s.k, j, p.dims[g][0]);
-        if (g < p.ntg && p.nd[g] > 1) k1 = bf16_at(s.k, j, p.dims[g][1]);
-        s.kt[hh][2 * g][j] = k0;
-        s.kt[hh][2 * g + 1][j] = k1;
-      }
-    }
-  }
-  named_bar(2, 128);
-  for (int hh = 0; hh < nh; ++hh) {
-    const KPlan &p = s.plan[hh];
-    KConst<G> kc;
-    kc.c0 = p.c0;
-    kc.eps = p.eps;
-#pragma unroll
-    for (int v = 0; v < G; ++v) kc.lin[v] = p.lin[v];
-#pragma unroll
-    for (int i = 0; i < G * (G + 1) / 2; ++i) kc.quad[i] = p.quad[i];
-    float qt[2 * kMaxTailG];
-#pragma unroll
-    for (int g = 0; g < kMaxTailG; ++g) {
-      qt[2 * g] = (g < p.ntg && p.nd[g] > 0) ? bf16_at(s.q[hh], m, p.dims[g][0]) : 0.f;
-      qt[2 * g + 1] = (g < p.ntg && p.nd[g] > 1) ? bf16_at(s.q[hh], m, p.dims[g][1]) : 0.f;
-    }
-    const bool fast = p.fast != 0;
-    float dsum = 0.f;
-    for (int kb = 0; kb < geo.nkb; ++kb) {
-      const int it = hh * geo.nkb + kb, buf = it & 1;
-      const uint32_t col = kTmemS + 32 * buf;
-      if (!mbar_wait(&s.s_full[buf], (it >> 1) & 1, abort_flag, args.status)) return false;
-      tc_fence_after();
-      const int jbase = 32 * kb;                   // the block's first key, tile-local
-      const int jg0 = geo.ks + jbase;              // and global
-      uint32_t pk[16];
-      if (jg0 + 31 >= csw && jg0 <= rw1) {
-        if (fast) {
-          // branch-free: every key is evaluated (two per packed instruction),
-          // the causal mask is a select; 16 keys per tensor-memory load
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t sv[16];
-            tmem_ld16(tmem_lane_addr(tb, warp, col + 16 * half), sv);
-            tmem_wait_ld();
-#pragma unroll
-            for (int jj = 0; jj < 16; jj += 2) {
-              const int j0 = jbase + 16 * half + jj;
-              const int jg = geo.ks + j0;
-              const float2 kp = kappa2_g<G>(
-                  kc, make_float2(__uint_as_float(sv[jj]), __uint_as_float(sv[jj + 1])), qt,
-                  &s.kt[hh][0][j0], kKeys);
-              pk[8 * half + (jj >> 1)] =
-                  pack_bf16x2((jg >= cs && jg <= i_tok) ? kp.x : 0.f,
-                              (jg + 1 >= cs && jg + 1 <= i_tok) ? kp.y : 0.f);
-            }
-          }
-        } else {
-          uint32_t r0[16], r1[16];
-          tmem_ld16(tmem_lane_addr(tb, warp, col), r0);
-          tmem_ld16(tmem_lane_addr(tb, warp, col + 16), r1);
-          tmem_wait_ld();
-          float sl[32];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            sl[e] = __uint_as_float(r0[e]);
-            sl[16 + e] = __uint_as_float(r1[e]);
-          }
-          float kl[32];
-          for (int jj = 0; jj < 32; ++jj) {
-            const int jg = jg0 + jj;
-            kl[jj] = (jg >= cs && jg <= i_tok)
-                         ? kappa_generic(p, sl[jj], s.q[hh], s.k, m, jbase + jj)
-                         : 0.f;
-          }
-#pragma unroll
-          for (int jj = 0; jj < 32; jj += 2) pk[jj >> 1] = pack_bf16x2(kl[jj], kl[jj + 1]);
-        }
-        // denominator from the same rounded weights the P.V product uses
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162 *>(&pk[e]);
-          dsum += __low2float(pb) + __high2float(pb);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = 0u;
-      }
-      // P for these 32 keys -> the first 16 columns of the sub-tile (their s
-      // values are already in registers)
-      tmem_st16(tmem_lane_addr(tb, warp, col), pk);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.p_full[buf]);
-    }
-#pragma unroll
-    for (int e = 0; e < kIntraNH; ++e)
-      if (e == hh) den_intra[e] += dsum;
-  }
-  return true;
-}
-
-// The worker for a head of ge <= G variables (1 + its non-empty tail groups).
-template <int G, bool kWide>
-__device__ bool intra_dispatch(int ge, IntraSmem<kWide> &s, const ReadArgs &args,
-                               const IntraGeom &geo, int nh, int warp, int lane, uint32_t tb,
-                               float (&den_intra)[kIntraNH]) {
-  if constexpr (G > 1) {
-    if (ge < G) return intra_dispatch<G - 1, kWide>(ge, s, args, geo, nh, warp, lane, tb, den_intra);
-  }
-  return intra_worker<G, kWide>(s, args, geo, nh, warp, lane, tb, den_intra);
-}
-
-// ---------------------------------------------------------------- intra kernel
-// Warps 0-3: kappa (thread = query row) and the epilogue; warp 4: UMMA issue
-// (s = Q K^T per 32-key block, then P.V) and tensor memory; warp 5: TMA.
-// Blocks per SM by register need: four for small G, three up to G = 6 (a
-// few bytes of spill at G = 6 cost less than the third block gains); the
-// 256-key tiles of C = 256 fit two by shared memory.
-template <int G, bool kWide>
-__global__ void __launch_bounds__(kIntraThreads, kWide ? 2 : (G <= 3 ? 4 : (G <= 6 ? 3 : 2)))
-tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, ReadArgs args) {
-  extern __shared__ uint8_t smem_raw[];
-  IntraSmem<kWide> &s = *reinterpret_cast<IntraSmem<kWide> *>(smem_align1024(smem_raw));
-  const int hg = blockIdx.x, t = blockIdx.y, unit = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bidx = unit / args.Hkv, kv = unit % args.Hkv;
-  const int h0 = kv * args.rho + hg * kIntraNH;
-  const int nh = min(kIntraNH, args.rho - hg * kIntraNH);
-  const IntraGeom geo = intra_geom(t, args.chunk);
-  const int nsteps = geo.nkb * nh;        // (head, 32-key block)
-  constexpr int kIss = 4, kTma = 5;
-  pdl_trigger();
-
-  if (tid == 0) {
-    s.abort_flag = 0;
-    mbar_init(&s.qkv_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.p_full[i], 4);
-      mbar_init(&s.s_free[i], 1);
-    }
-    mbar_init(&s.d_full, 1);
-    mbar_init(&s.never, 1);
-    fence_mbar_init();
-  }
-  if (warp == kIss) {
-    tmem_alloc(&s.tmem_base, kIntraTmemCols);
-    tmem_relinquish();
-  }
-  pdl_wait();   // plans of the prep kernel; the intra rows of the previous call
-  for (int n = tid; n < nh * (int)(sizeof(KPlan) / 4); n += kIntraThreads) {
-    const int hh = n / (sizeof(KPlan) / 4), e = n % (sizeof(KPlan) / 4);
-    reinterpret_cast<int *>(&s.plan[hh])[e] =
-        reinterpret_cast<const int *>(&args.plans[h0 + hh])[e];
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tb = s.tmem_base;
-  volatile int *abort_flag = &s.abort_flag;
-
-  if (warp == kIss) {
-    if (lane == 0) {
-      const uint32_t id32k = idesc_bf16_f32(128, 32, 0);
-      const uint32_t id64mn = idesc_bf16_f32(128, 64, 1);
-      const uint64_t qdesc0 = sdesc_sw128(smem_u32(s.q[0]), 16, 1024);
-      constexpr uint64_t kQStep = (kC * 64 * 2) >> 4;       // one Q tile
-      const uint64_t kdesc0 = sdesc_sw128(smem_u32(s.k), 16, 1024);
-      const uint64_t vdesc0 = sdesc_sw128(smem_u32(s.v), 16, 1024);
-      auto issue_s = [&](int it) {
-        const int hh = it / geo.nkb, kb = it % geo.nkb;
-        const uint64_t qd = qdesc0 + kQStep * hh;
-        const uint64_t kd = kdesc0 + (uint64_t)((32 * kb * 128) >> 4);
-        const uint32_t dt = tb + kTmemS + 32 * (it & 1);
-        umma_ss(dt, qd, kd, id32k, 0u);
-        umma_ss(dt, qd + 2, kd + 2, id32k, 1u);
-        umma_ss(dt, qd + 4, kd + 4, id32k, 1u);
-        umma_ss(dt, qd + 6, kd + 6, id32k, 1u);
-        umma_commit(&s.s_full[it & 1]);
-      };
-      const bool starve = args.status[1] == kStarveIntra;   // failure-path test only
-      bool ok = mbar_wait(starve ? &s.never : &s.qkv_full, 0, abort_flag, args.status);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        if (nsteps > 1) issue_s(1);
-      }
-      for (int it = 0; it < nsteps && ok; ++it) {
-        if (!mbar_wait(&s.p_full[it & 1], (it >> 1) & 1, abort_flag, args.status)) break;
-        tc_fence_after();
-        const int hh = it / geo.nkb, kb = it % geo.nkb;
-        const uint32_t at = tb + kTmemS + 32 * (it & 1);
-        const uint64_t vd = vdesc0 + (uint64_t)((32 * kb * 128) >> 4);
-        const uint32_t dt = tb + kTmemI + 64 * hh;
-        umma_ts(dt, at, vd, id64mn, kb > 0 ? 1u : 0u);
-        umma_ts(dt, at + 8, vd + (2048 >> 4), id64mn, 1u);
-        umma_commit(&s.s_free[it & 1]);
-        if (it + 2 < nsteps) {
-          if (!mbar_wait(&s.s_free[it & 1], (it >> 1) & 1, abort_flag, args.status)) break;
-          tc_fence_after();
-          issue_s(it + 2);
-        }
-      }
-      umma_commit(&s.d_full);
-      mbar_wait_teardown(&s.d_full, 0, args.status);   // no MMA in flight at exit
-    }
-    __syncwarp();
-  } else if (warp == kTma) {
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      const int nkh = geo.nkb / 4;   // 128-key boxes
-      mbar_arrive_expect_tx(&s.qkv_full, (uint32_t)(nh + 2 * nkh) * kC * 64 * 2);
-      for (int hh = 0; hh < nh; ++hh)
-        tma_load_3d(s.q[hh], &tmQ, &s.qkv_full, 0, geo.row0, bidx * args.Hq + h0 + hh);
-      for (int x = 0; x < nkh; ++x) {
-        tma_load_3d(s.k + x * kC * 64, &tmK, &s.qkv_full, 0, geo.ks + kC * x, unit);
-        tma_load_3d(s.v + x * kC * 64, &tmV, &s.qkv_full, 0, geo.ks + kC * x, unit);
-      }
-      mbar_wait_teardown(&s.qkv_full, 0, args.status);
-    }
-    __syncwarp();
-  } else {
-    // warps 0-3: kappa, then the numerators and denominators to workspace; a
-    // head whose groups are partly empty takes the worker of its own size
-    float den_intra[kIntraNH] = {0.f};
-    const bool ok = intra_dispatch<G, kWide>(s.plan[0].ntg + 1, s, args, geo, nh, warp, lane,
-                                             tb, den_intra);
-    const int m = tid;
-    const int i_tok = geo.row0 + m;
-    if (ok && mbar_wait(&s.d_full, 0, abort_flag, args.status)) {
-      tc_fence_after();
-      for (int hh = 0; hh < nh; ++hh) {
-        uint32_t d[64];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t r[16];
-          tmem_ld16(tmem_lane_addr(tb, warp, kTmemI + 64 * hh + 16 * q4), r);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) d[16 * q4 + e] = r[e];
-        }
-        tmem_wait_ld();
-        float dsum = 0.f;
-#pragma unroll
-        for (int e = 0; e < kIntraNH; ++e)
-          if (e == hh) dsum = den_intra[e];
-        if (i_tok < args.T) {
-          const size_t bh = (size_t)bidx * args.Hq + h0 + hh;
-          uint4 *dst = intra_tile(args.intra_num, bh, args.T, geo.row0 / kC) + m;
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            dst[kC * e] = make_uint4(d[4 * e], d[4 * e + 1], d[4 * e + 2], d[4 * e + 3]);
-          args.intra_den[bh * args.T + i_tok] = dsum;
-        }
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kIss) {
-    tc_fence_after();
-    tmem_dealloc(tb, kIntraTmemCols);
-  }
-}
-
 // ---------------------------------------------------------------- intra kernel, tensor-core kappa
-// For chunks of 64 and 128 tokens.  With z_0 = s = q.k and z_g the tail-group
-// sums, the quadratic form of kappa splits into
+// With z_0 = s = q.k and z_g the tail-group sums, the quadratic form of
+// kappa splits into
 //     kappa = (c0 + T) + s (lin_0 + U + quad_00 s),
 //     U = sum_g quad_0g z_g = sum_r quad_{0 g(r)} q_r k_r,
 //     T = sum_g lin_g z_g + sum_{g <= h} quad_gh z_g z_h
@@ -1619,8 +1230,7 @@ tc_intra_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 // with B = [k_r, k_r k_r' | k_r] (key side) and A the query rows times the
 // coefficients of T, then of U.  The CUDA cores keep three FMAs per pair.
 // Heads whose features do not fit (more than 8 tail dims, or a group of more
-// than two dims) evaluate kappa from the tiles as the generic path of
-// tc_intra_kernel does.
+// than two dims) evaluate kappa from the Q and K tiles (kappa_generic).
 //
 // A block serves one or two query heads of one KV head (nh_per_block; two
 // when the grid of one head a block would still fill the GPU several times),
@@ -1643,6 +1253,7 @@ struct __align__(1024) TkSmem {
   __nv_bfloat16 bk[kC * 64];           // key features
   KPlan plan[kTkHeads];
   uint64_t qkv_full, phi_full, s_full[2], p_full[2], s_free[2], d_full, i_free, drain;
+  uint64_t kv2_full;          // (C = 256) the second 128-key tile of K and V
   uint64_t never;                      // failure-path tests: nothing arrives
   uint32_t tmem_base;
   int abort_flag;
@@ -1714,6 +1325,7 @@ __device__ __forceinline__ void tk_build_rows(TkSmem &s, const KPlan &p, const _
 #undef OAL_TK_CHUNK
 }
 
+template <bool kTwoTiles>
 __global__ void __launch_bounds__(kTkThreads, 2)
 tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, ReadArgs args) {
@@ -1725,7 +1337,11 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   const int hpb = args.nh_per_block;               // 1 or 2 (<= kTkHeads)
   const int h0 = kv * args.rho + hg * hpb;
   const int nh = min(hpb, args.rho - hg * hpb);
-  const IntraGeom geo = intra_geom(t, args.chunk);   // kTkKB key blocks (C <= 128)
+  const IntraGeom geo = intra_geom(t, args.chunk);
+  // 128-key tiles of K and V: one (C <= 128, and the first half of a 256-token
+  // chunk) or two (the second half: the second tile reloads the buffers)
+  const int ntile = kTwoTiles ? geo.nkb / kTkKB : 1;
+  const int nkb = kTkKB * ntile;
   constexpr int kIss = 4, kTma = 5;
   pdl_trigger();
 
@@ -1741,6 +1357,7 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     mbar_init(&s.d_full, 1);
     mbar_init(&s.i_free, 4);
     mbar_init(&s.drain, 1);
+    mbar_init(&s.kv2_full, 1);
     mbar_init(&s.never, 1);
     fence_mbar_init();
     // Q, K and V are inputs of the call that no kernel of it writes: their
@@ -1777,14 +1394,16 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const uint64_t bdesc0 = sdesc_sw128(smem_u32(s.bk), 16, 1024);
       const bool starve = args.status[1] == kStarveIntra;   // failure-path test only
       bool ok = mbar_wait(starve ? &s.never : &s.qkv_full, 0, abort_flag, args.status);
+      bool kv2 = false;   // the second tile's loads were issued
       for (int hh = 0; hh < nh && ok; ++hh) {
         const KPlan &p = s.plan[hh];
         const bool tu = p.tk_mode && p.tk_nlin > 0;
         const uint64_t qdesc = sdesc_sw128(smem_u32(s.q[hh]), 16, 1024);
-        const int g0 = kTkKB * hh;
+        const int g0 = nkb * hh;
         // S = Q K^T of key block kb, then (tu) T over K = 48 and U over K = 16
+        // (kb & 3: the block's place in the current 128-key tile)
         auto issue_s = [&](int kb) {
-          const uint64_t koff = (uint64_t)((32 * kb * 128) >> 4);
+          const uint64_t koff = (uint64_t)((32 * (kb & 3) * 128) >> 4);
           const uint32_t b = (g0 + kb) & 1;
           umma_ss_warp(tb + kTkS + 32 * b, qdesc, kdesc0 + koff, id32k, 0u);
           umma_ss_warp(tb + kTkS + 32 * b, qdesc + 2, kdesc0 + koff + 2, id32k, 1u);
@@ -1792,7 +1411,7 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           umma_ss_warp(tb + kTkS + 32 * b, qdesc + 6, kdesc0 + koff + 6, id32k, 1u);
         };
         auto issue_tu = [&](int kb) {
-          const uint64_t koff = (uint64_t)((32 * kb * 128) >> 4);
+          const uint64_t koff = (uint64_t)((32 * (kb & 3) * 128) >> 4);
           const uint32_t b = (g0 + kb) & 1;
           if (tu) {
 #pragma unroll
@@ -1808,38 +1427,59 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             ok = mbar_wait(&s.s_free[g & 1], (g >> 1) & 1, abort_flag, args.status);
           if (!ok) break;
         }
-        // the first two S blocks need only Q and K: they run while the
-        // feature rows are built
-        tc_fence_after();
-        issue_s(0);
-        issue_s(1);
-        if (!mbar_wait(&s.phi_full, hh & 1, abort_flag, args.status)) break;
-        tc_fence_after();
-        issue_tu(0);
-        issue_tu(1);
-        for (int kb = 0; kb < kTkKB && ok; ++kb) {
-          const int g = g0 + kb;
-          if (!mbar_wait(&s.p_full[g & 1], (g >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
-          // the numerators of the previous head are read out of tensor memory
-          if (kb == 0 && hh > 0 &&
-              !mbar_wait(&s.i_free, (hh - 1) & 1, abort_flag, args.status)) { ok = false; break; }
+        for (int j = 0; j < ntile && ok; ++j) {
+          if (kTwoTiles && j > 0) {
+            // the first tile's last P V products have read V and their P
+            // sub-tiles (its S, T, U products were read before): reload K
+            // and V with the second tile
+            for (int g = g0 + kTkKB * j - 2; g < g0 + kTkKB * j && ok; ++g)
+              ok = mbar_wait(&s.s_free[g & 1], (g >> 1) & 1, abort_flag, args.status);
+            if (!ok) break;
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&s.kv2_full, 2u * kC * 64 * 2);
+              tma_load_3d(s.k, &tmK, &s.kv2_full, 0, geo.ks + kC, unit);
+              tma_load_3d(s.v, &tmV, &s.kv2_full, 0, geo.ks + kC, unit);
+            }
+            kv2 = true;
+            __syncwarp();
+            if (!mbar_wait(&s.kv2_full, 0, abort_flag, args.status)) { ok = false; break; }
+          }
+          const int k0 = kTkKB * j;
+          // the first two S blocks of the tile need only Q and K: they run
+          // while the feature rows are built
           tc_fence_after();
-          const uint32_t at = tb + kTkS + 32 * (g & 1);
-          const uint64_t vd = vdesc0 + (uint64_t)((32 * kb * 128) >> 4);
-          umma_ts_warp(tb + kTkI, at, vd, id64mn, kb > 0 ? 1u : 0u);
-          umma_ts_warp(tb + kTkI, at + 8, vd + (2048 >> 4), id64mn, 1u);
-          umma_commit_warp(&s.s_free[g & 1]);
-          if (kb + 2 < kTkKB) {
-            if (!mbar_wait(&s.s_free[g & 1], (g >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
+          issue_s(k0);
+          issue_s(k0 + 1);
+          if (!mbar_wait(&s.phi_full, (hh * ntile + j) & 1, abort_flag, args.status)) { ok = false; break; }
+          tc_fence_after();
+          issue_tu(k0);
+          issue_tu(k0 + 1);
+          for (int kb = k0; kb < k0 + kTkKB && ok; ++kb) {
+            const int g = g0 + kb;
+            if (!mbar_wait(&s.p_full[g & 1], (g >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
+            // the numerators of the previous head are read out of tensor memory
+            if (kb == 0 && hh > 0 &&
+                !mbar_wait(&s.i_free, (hh - 1) & 1, abort_flag, args.status)) { ok = false; break; }
             tc_fence_after();
-            issue_s(kb + 2);
-            issue_tu(kb + 2);
+            const uint32_t at = tb + kTkS + 32 * (g & 1);
+            const uint64_t vd = vdesc0 + (uint64_t)((32 * (kb & 3) * 128) >> 4);
+            umma_ts_warp(tb + kTkI, at, vd, id64mn, kb > 0 ? 1u : 0u);
+            umma_ts_warp(tb + kTkI, at + 8, vd + (2048 >> 4), id64mn, 1u);
+            umma_commit_warp(&s.s_free[g & 1]);
+            if (kb + 2 < k0 + kTkKB) {
+              if (!mbar_wait(&s.s_free[g & 1], (g >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
+              tc_fence_after();
+              issue_s(kb + 2);
+              issue_tu(kb + 2);
+            }
           }
         }
+        if (!ok) break;
         umma_commit_warp(&s.d_full);
       }
       umma_commit_warp(&s.drain);
       if (lane == 0) mbar_wait_teardown(&s.drain, 0, args.status);   // no MMA in flight at exit
+      if (kTwoTiles && kv2 && lane == 0) mbar_wait_teardown(&s.kv2_full, 0, args.status);
     }
     __syncwarp();
   } else if (warp == kTma) {
@@ -1880,8 +1520,19 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const __nv_bfloat16 *qt = s.q[hh];
       const float c0 = p.c0, lin0 = p.lin[0], q00 = p.quad[0], eps = p.eps;
       float dsum = 0.f;
-      for (int kb = 0; kb < kTkKB; ++kb) {
-        const int g = kTkKB * hh + kb, b = g & 1;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int g = nkb * hh + kb, b = g & 1;
+        if (kTwoTiles && kb == kTkKB) {
+          // the second tile: its K rows land, then its key features (the
+          // first tile's T and U products are complete: their s_full arrived)
+          if (!mbar_wait(&s.kv2_full, 0, abort_flag, args.status)) { ok = false; break; }
+          if (p.tk_mode && p.tk_nlin > 0) {
+            tk_build_rows(s, p, qt, m, true);
+            fence_proxy_async();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.phi_full);
+        }
         if (!mbar_wait(&s.s_full[b], (g >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
         tc_fence_after();
         const int jbase = 32 * kb, jg0 = geo.ks + jbase;
@@ -1911,7 +1562,7 @@ tc_intra_tk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                   kap[e] = fmaxf(fmaf(sx, fmaf(q00, sx, lin0 + ux), c0 + tx), eps);
                 } else {
                   kap[e] = (jg + e >= cs && jg + e <= i_tok)
-                               ? kappa_generic(p, sx, qt, s.k, m, j0 + e) : 0.f;
+                               ? kappa_generic(p, sx, qt, s.k, m, (j0 + e) & (kC - 1)) : 0.f;
                 }
               }
               pk[8 * half + (jj >> 1)] = pack_bf16x2((jg >= cs && jg <= i_tok) ? kap[0] : 0.f,
@@ -2330,20 +1981,6 @@ static Layout plan_layout(int B, int Hq, int Hkv, int T, int chunk) {
   return L;
 }
 
-using IntraKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, ReadArgs);
-template <bool kWide>
-static IntraKernel intra_kernel_for(int G) {
-  switch (G) {
-    case 1: return tc_intra_kernel<1, kWide>;
-    case 2: return tc_intra_kernel<2, kWide>;
-    case 3: return tc_intra_kernel<3, kWide>;
-    case 4: return tc_intra_kernel<4, kWide>;
-    case 5: return tc_intra_kernel<5, kWide>;
-    case 6: return tc_intra_kernel<6, kWide>;
-    default: return tc_intra_kernel<7, kWide>;
-  }
-}
-
 }  // namespace tcp
 
 size_t tc_prefill_workspace_bytes(int B, int Hq, int Hkv, int T, int chunk) {
@@ -2396,7 +2033,6 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   const size_t rsmem1 = sizeof(ReadSmem<1>) + 1024;
   const size_t rsmem2 = sizeof(ReadSmem<2>) + 1024;
   const size_t tksmem = sizeof(TkSmem) + 1024;
-  const size_t ismem_w = sizeof(IntraSmem<true>) + 1024;
   // shared-memory limits above 48 KB: a function attribute of each device
   static std::mutex attr_mutex;
   static bool attr_set[kMaxDevices] = {};
@@ -2419,12 +2055,10 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
           cudaFuncSetAttribute(tc_readout_kernel<2>,
                                cudaFuncAttributePreferredSharedMemoryCarveout, 100) ==
               cudaSuccess &&
-          cudaFuncSetAttribute(tc_intra_tk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          cudaFuncSetAttribute(tc_intra_tk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tksmem) == cudaSuccess &&
+          cudaFuncSetAttribute(tc_intra_tk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)tksmem) == cudaSuccess;
-      for (int g = 1; ok && g <= kMaxG; ++g)
-        ok = cudaFuncSetAttribute(intra_kernel_for<true>(g),
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)ismem_w) == cudaSuccess;
       if (!ok) {
         cudaGetLastError();   // reported here, not by the next launch
         return oal_fail(OAL_ERR_CUDA, "prefill: setting the shared memory limit failed");
@@ -2456,22 +2090,21 @@ oal_status launch_prefill_tc(const void *Q, const void *K, const void *V, int B,
   ra.coef = coef; ra.plans = plans; ra.status = status; ra.snap = snap;
   ra.intra_num = reinterpret_cast<float *>(w + lay.inum_off);
   ra.intra_den = reinterpret_cast<float *>(w + lay.iden_off);
-  ra.nh_per_block = kIntraNH;
-  dim3 gi((ra.rho + kIntraNH - 1) / kIntraNH, lay.nS, lay.U);
-  if (chunk == 256) {
-    launch_pdl(intra_kernel_for<true>(G), gi, dim3(kIntraThreads), ismem_w, stream, tmQ, tmKn, tmV,
-               ra);
-    st = oal_after_launch("tc_intra_kernel", stream);
-  } else {
+  {
     // two heads a block once one head a block would make four waves of two
-    // blocks per SM
+    // blocks per SM (chunks of 64 and 128; a 256-token chunk's second half
+    // reloads K and V for its second 128-key tile, one head a block)
     const int forced = g_intra_heads.load();
-    const int hpb = forced ? forced
-                           : ((size_t)ra.rho * lay.nS * lay.U >= (size_t)4 * 2 * 152 ? kTkHeads : 1);
+    int hpb = forced ? forced
+                     : ((size_t)ra.rho * lay.nS * lay.U >= (size_t)4 * 2 * 152 ? kTkHeads : 1);
+    if (chunk == 256) hpb = 1;
     ReadArgs rt = ra;
     rt.nh_per_block = hpb;
     dim3 gtk((ra.rho + hpb - 1) / hpb, lay.nS, lay.U);
-    launch_pdl(tc_intra_tk_kernel, gtk, dim3(kTkThreads), tksmem, stream, tmQ, tmKn, tmV, rt);
+    if (chunk == 256)
+      launch_pdl(tc_intra_tk_kernel<true>, gtk, dim3(kTkThreads), tksmem, stream, tmQ, tmKn, tmV, rt);
+    else
+      launch_pdl(tc_intra_tk_kernel<false>, gtk, dim3(kTkThreads), tksmem, stream, tmQ, tmKn, tmV, rt);
     st = oal_after_launch("tc_intra_tk_kernel", stream);
   }
   if (st != OAL_OK) return st;
