@@ -102,6 +102,14 @@ def test_workspace_queries(lib):
     assert oal.oal_contribution_workspace_bytes(40, 14, 2, 4096, d=32) == 0
 
 
+def test_intra_heads_hook_validates_on_host(lib):
+    # the test hook for the intra-chunk kernel's block shape takes 0, 1 or 2
+    for bad in (-1, 3):
+        assert lib.oal_debug_intra_heads(bad) == 1   # OAL_ERR_INVALID_ARG
+    for good in (1, 2, 0):
+        assert lib.oal_debug_intra_heads(good) == 0
+
+
 def test_missing_library_fails_loudly(tmp_path):
     from grouped_quadratic_gb300 import oal
     saved = oal._lib
