@@ -283,6 +283,16 @@ def kernel_work(name, fl):
     return 0.0, False
 
 
+def e2e_pieces(B, Hkv):
+    """The end-to-end pipeline's pieces (sequence, first KV head, KV heads):
+    whole sequences, the last one split into groups of 4 KV heads (a multiple
+    of 4 keeps every state slice 16-byte aligned) so that the work left after
+    the last input lands is small."""
+    split = 4 if Hkv % 4 == 0 and Hkv > 4 else Hkv
+    return [(bb, 0, Hkv) for bb in range(B - 1)] + \
+        [(B - 1, g, split) for g in range(0, Hkv, split)]
+
+
 class PrefillBench:
     """One prefill workload on the device: inputs resident in HBM, the step
     (expand + prefill + one decode token) callable directly or from a graph."""
@@ -320,13 +330,7 @@ class PrefillBench:
         self.y1 = torch.empty(B, Hq, D, dtype=self.Q.dtype, device=dev)
         self.ws_p = torch.empty(max(256, oal.oal_prefill_workspace_bytes(
             B, Hq, Hkv, Tp, D, D, self.dt, self.layout, chunk)), dtype=torch.uint8, device=dev)
-        # the end-to-end pipeline's pieces (sequence, first KV head, KV heads):
-        # whole sequences, the last one split into groups of 4 KV heads (a
-        # multiple of 4 keeps every state slice 16-byte aligned) so that the
-        # work left after the last input lands is small
-        split = 4 if Hkv % 4 == 0 and Hkv > 4 else Hkv
-        self.pieces = [(bb, 0, Hkv) for bb in range(B - 1)] + \
-            [(B - 1, g, split) for g in range(0, Hkv, split)]
+        self.pieces = e2e_pieces(B, Hkv)
         self.ws_e2e = [torch.empty(max(256, oal.oal_prefill_workspace_bytes(
             1, Hq, Hkv, Tp, D, D, self.dt, self.layout, chunk)),
             dtype=torch.uint8, device=dev) for _ in range(2)]

@@ -67,3 +67,18 @@ def test_reference_arm_under_torchrun():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_e2e_pieces_cover_every_kv_head_once():
+    import bench
+    for B, Hkv in [(4, 8), (1, 2), (1, 8), (3, 12), (2, 3), (5, 4)]:
+        pieces = bench.e2e_pieces(B, Hkv)
+        seen = set()
+        for bb, k0, nk in pieces:
+            assert nk == Hkv or nk % 4 == 0   # 16-byte-aligned state slices
+            for kv in range(k0, k0 + nk):
+                assert (bb, kv) not in seen
+                seen.add((bb, kv))
+        assert seen == {(bb, kv) for bb in range(B) for kv in range(Hkv)}
+        # every sequence but the last is one piece
+        assert [p for p in pieces if p[0] < B - 1] == [(bb, 0, Hkv) for bb in range(B - 1)]
