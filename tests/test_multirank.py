@@ -4,7 +4,8 @@ The (batch x KV head) units are independent, so N GPUs run N replicas with no
 data exchange; what crosses ranks is the timing: a barrier around the timed
 region and the maximum of the ranks' times.  These tests run that logic as
 two CPU processes, and the reference arm under torchrun, where rank 0 alone
-runs and prints its one JSON line.
+runs and prints its one JSON line.  The end-to-end pipeline's piece plan
+(host logic of the same script) is checked here too.
 """
 import json
 import os
